@@ -1,0 +1,433 @@
+#!/usr/bin/env python3
+"""Benchmark of the K3-shape MXFP4 Stable LatentMoE routed-expert layer.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|chunk|prefill]
+                [--impl ours|reference]
+
+One step = one k3moe_forward over one batch of synthetic tokens (router, top-k,
+permutation, latent down, expert gate/up + SiTU-GLU, expert down, combine, RMSNorm,
+latent up), inputs resident in HBM.  L2 is flushed (256 MiB write) before every timed
+step, outside the timed events.  Prints one JSON line (rank 0).
+
+--impl reference times the fp64 oracle on the host cores (the only reference this
+method has), on a bounded sample of the same workload.
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+(the layer does not shard across GPUs in this library); value aggregates all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "K3-shape MXFP4 LatentMoE layer: decode µs/token (HBM GB/s), prefill tokens/s"
+FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", choices=("decode", "chunk", "prefill"), default="decode")
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle baseline")
+    a = ap.parse_args()
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+def workload_cfg(name):
+    from datagen import configs as C
+    return {"decode": C.DECODE, "chunk": C.CHUNK, "prefill": C.PREFILL}[name]
+
+
+def describe(cfg) -> str:
+    return (f"{cfg.name}: K3-shape routed layer, T={cfg.T}, H={cfg.hidden}, L={cfg.latent}, E={cfg.n_experts}, "
+            f"K={cfg.top_k}, I={cfg.inter}, MXFP4 experts (scale bytes {cfg.scale_lo}..{cfg.scale_hi}), "
+            f"bf16 latent projections")
+
+
+def unit_of(cfg):
+    return ("tokens/s", True) if cfg.name == "prefill" else ("µs/token", False)
+
+
+def metric_value(cfg, ms_per_step, world):
+    if cfg.name == "prefill":
+        return cfg.T * world / (ms_per_step / 1e3)
+    return ms_per_step * 1e3 / (cfg.T * world)
+
+
+# ------------------------------------------------------------------------------ byte/flop model
+def expert_bytes(cfg):
+    I, L = cfg.inter, cfg.latent
+    mat = I * L // 2 + I * L // 32  # one MXFP4 [I, L] or [L, I] matrix: packed + scales
+    return 2 * mat, mat  # gate+up, down
+
+
+def algorithmic(cfg, n_unique):
+    """Algorithmic bytes (HBM) and flops per phase for one step."""
+    T, H, L, E, K, I = cfg.T, cfg.hidden, cfg.latent, cfg.n_experts, cfg.top_k, cfg.inter
+    gu, dn = expert_bytes(cfg)
+    return {
+        "proj": dict(bytes=(E * H + L * H) * 2 + T * H * 2 + T * (E * 4 + L * 2), flops=2 * T * H * (E + L)),
+        "gateup": dict(bytes=n_unique * gu + T * L * 2 + T * K * I * 2, flops=2 * T * K * 2 * I * L),
+        "down": dict(bytes=n_unique * dn + T * K * I * 2 + T * K * L * 4, flops=2 * T * K * L * I),
+        "up": dict(bytes=H * L * 2 + T * L * 2 + T * H * 4, flops=2 * T * H * L),
+    }
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "mxfp4_routed_expert_latentmoe_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_phase, workload):
+    """dram bytes per launch recorded by an ncu capture under profiles/, if the kernel
+    sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_phase}_{workload}.md")
+    try:
+        kv = {}
+        for line in open(path):
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("source_sha256_16") != csrc_hash():
+            return None
+        return int(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------------------ raw CUDA events
+class RawEvents:
+    """Timing events created through the CUDA driver API, so that the C library can
+    record them on its stream (handles are plain CUevent / cudaEvent_t)."""
+
+    def __init__(self, n):
+        import ctypes
+        self.cu = ctypes.CDLL("libcuda.so.1")
+        self.handles = []
+        for _ in range(n):
+            h = ctypes.c_void_p()
+            if self.cu.cuEventCreate(ctypes.byref(h), 0) != 0:
+                raise RuntimeError("cuEventCreate failed")
+            self.handles.append(h)
+
+    def ms(self, i, j) -> float:
+        import ctypes
+        v = ctypes.c_float()
+        if self.cu.cuEventElapsedTime(ctypes.byref(v), self.handles[i], self.handles[j]) != 0:
+            raise RuntimeError("cuEventElapsedTime failed")
+        return float(v.value)
+
+    def __del__(self):
+        for h in getattr(self, "handles", []):
+            self.cu.cuEventDestroy_v2(h)
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", gpu_id], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return None
+        win = [p for (t, p) in self.samples if t0 <= t <= t1]
+        if not win:  # timed region shorter than the sampling period: nearest samples
+            win = [min(self.samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))[1]]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        reasons = set()
+        for p in win:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), p[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(win)}
+
+
+# ------------------------------------------------------------------------------ oracle timing
+def oracle_sample(cfg, seconds_target: float, min_tokens=1, max_tokens=64):
+    """Times the oracle (token at a time, bf16-rounding spec mode) on a bounded sample of
+    tokens drawn from the workload's recipe.  Returns (value in the metric's unit,
+    threads, sample description, elapsed)."""
+    import numpy as np
+    import oracle
+    from datagen import configs as C
+
+    d = oracle.dims(**cfg.dims)
+    W = C.layer_weights(cfg)
+    x_all = C.layer_x(cfg)
+
+    def run(rows):
+        x = np.ascontiguousarray(x_all[rows])
+        ids, _, _, _ = oracle.route(d, x, W["wr"], W["bias"])
+        ex = {int(e): C.expert_tensors(cfg, int(e)) for e in np.unique(ids)}
+        t0 = time.perf_counter()
+        oracle.forward(d, x, W["wr"], W["bias"], W["wd"], W["wu"], W["gamma"], ex, True, 0)
+        return time.perf_counter() - t0
+
+    T = x_all.shape[0]
+    t1 = run([0])
+    n = int(max(min_tokens, min(max_tokens, T, seconds_target / max(t1, 1e-3))))
+    rows = list(range(n)) if n <= T else [i % T for i in range(n)]
+    el = run(rows)
+    val = (n / el) if cfg.name == "prefill" else (el / n * 1e6)
+    return val, oracle.threads_used(), f"{n} token(s) of the {cfg.name} workload, token at a time", el
+
+
+# ------------------------------------------------------------------------------ reference arm
+def run_reference(a, cfg, rank, world):
+    unit, hib = unit_of(cfg)
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from datagen import configs as C
+    oracle.build()
+    d = oracle.dims(**cfg.dims)
+    W = C.layer_weights(cfg)
+    x_all = C.layer_x(cfg)
+    per_step = 1 if cfg.name != "prefill" else 2
+    steps = []
+    rows_cycle = list(range(x_all.shape[0]))
+    prepared = []
+    for s in range(a.warmup + a.steps):
+        rows = [rows_cycle[(s * per_step + j) % len(rows_cycle)] for j in range(per_step)]
+        x = np.ascontiguousarray(x_all[rows])
+        ids, _, _, _ = oracle.route(d, x, W["wr"], W["bias"])
+        prepared.append((x, {int(e): C.expert_tensors(cfg, int(e)) for e in np.unique(ids)}))
+        if len(prepared) > 8:
+            break
+    for s in range(a.warmup + a.steps):
+        x, ex = prepared[s % len(prepared)]
+        t0 = time.perf_counter()
+        oracle.forward(d, x, W["wr"], W["bias"], W["wd"], W["wu"], W["gamma"], ex, True, 0)
+        el = time.perf_counter() - t0
+        if s >= a.warmup:
+            steps.append(el)
+    ms = statistics.mean(steps) * 1e3
+    val = (per_step / (ms / 1e3)) if cfg.name == "prefill" else ms * 1e3 / per_step
+    cores = oracle.threads_used()
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": unit, "n_gpus": a.gpus, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": hib, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(cfg), "sample_tokens_per_step": per_step},
+            "cpu_baseline": {"value": val, "unit": unit, "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} token(s) per step of the {cfg.name} workload"},
+            "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------ our arm
+def run_ours(a, cfg, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__ as g
+    g.build()
+    import mxfp4_routed_expert_latentmoe_gb300 as k3
+    from datagen import device as D
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    unit, hib = unit_of(cfg)
+    d = k3.dims(**cfg.dims)
+    t = D.layer_tensors(cfg, dev)
+    pool, eb, offs = D.expert_pool(cfg, dev)
+    tables = k3.ExpertTables.from_pool(pool, eb, offs)
+    T = cfg.T
+    out = torch.empty(T, cfg.hidden, dtype=torch.float32, device=dev)
+    ids = torch.empty(T, cfg.top_k, dtype=torch.int32, device=dev)
+    wts = torch.empty(T, cfg.top_k, dtype=torch.float32, device=dev)
+    ws = torch.empty(k3.workspace_bytes(d, T), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    args = (d, t["x"], t["wr"], t["bias"], t["wd"], t["wu"], t["gamma"], tables, out, ws)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(a.warmup):
+        flush.zero_()
+        k3.forward(*args, ids_out=ids, w_out=wts)
+    torch.cuda.synchronize()
+    status = k3.device_status(ws)
+    n_unique = int(np.unique(ids.cpu().numpy()).size)
+
+    gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}")
+    time.sleep(0.3)
+    evs = [RawEvents(9) for _ in range(a.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    w0 = time.time()
+    for s in range(a.steps):
+        flush.zero_()
+        k3.forward_profiled(*args, evs[s].handles, ids_out=ids, w_out=wts)
+    torch.cuda.synchronize()
+    barrier()
+    w1 = time.time()
+    per_step = [evs[s].ms(0, 8) for s in range(a.steps)]
+    phase_ms = {name: statistics.mean(evs[s].ms(i, i + 1) for s in range(a.steps)) for i, name in enumerate(k3.PHASES)}
+    ms = statistics.mean(per_step)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    clocks = sampler.summary(w0, w1)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not a.no_e2e:
+        xh = t["x"].cpu().pin_memory()
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        xd = torch.empty_like(t["x"])
+        e2e_args = (d, xd) + args[2:]
+        ms_e2e = []
+        for s in range(a.warmup + max(10, a.steps // 4)):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            xd.copy_(xh, non_blocking=True)
+            k3.forward(*e2e_args)
+            oh.copy_(out, non_blocking=True)
+            e1.record()
+            e1.synchronize()
+            if s >= a.warmup:
+                ms_e2e.append(e0.elapsed_time(e1))
+        me = statistics.mean(ms_e2e)
+        if world > 1:
+            tt = torch.tensor([me], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            me = float(tt.item())
+        e2e = {"value": metric_value(cfg, me, world), "unit": unit, "h2d_bytes_per_step": xh.numel() * 2,
+               "d2h_bytes_per_step": oh.numel() * 4}
+    sampler.stop()
+
+    if rank != 0:
+        return
+    peaks, peak_kind = measured_peaks()
+    alg = algorithmic(cfg, n_unique)
+    dom = "gateup"
+    if cfg.name == "prefill":
+        achieved = alg[dom]["flops"] / (phase_ms[dom] / 1e3) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": profiled_traffic(dom, cfg.name), "kernel": "k3_mx_gemv_kernel<gate/up>",
+                "peak_kind": f"{peak_kind} bf16 sustained"}
+    else:
+        achieved = alg[dom]["bytes"] / (phase_ms[dom] / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": profiled_traffic(dom, cfg.name), "kernel": "k3_mx_gemv_kernel<gate/up>",
+                "peak_kind": f"{peak_kind} HBM copy"}
+    phases = {k: {"us": v * 1e3,
+                  "GB_s": (alg[k]["bytes"] / (v / 1e3) / 1e9) if k in alg else None,
+                  "TFLOP_s": (alg[k]["flops"] / (v / 1e3) / 1e12) if k in alg else None}
+              for k, v in phase_ms.items()}
+    expert_us = (phase_ms["gateup"] + phase_ms["down"]) * 1e3
+    exp_bytes = alg["gateup"]["bytes"] + alg["down"]["bytes"]
+    line = {"metric": METRIC, "value": metric_value(cfg, ms, world), "unit": unit, "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": hib, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": describe(cfg), "global_batch": cfg.T * world, "seq_len": cfg.T,
+                       "parallelism": f"replicas x{world}", "l2": "flushed by a 256 MiB write before every timed step",
+                       "unique_experts": n_unique},
+            "roofline": roof,
+            "expert_phase": {"us": expert_us, "GB_s": exp_bytes / (expert_us / 1e6) / 1e9,
+                             "frac_hbm": exp_bytes / (expert_us / 1e6) / 1e9 / peaks["hbm_gbs"]},
+            "phases": phases, "clocks": clocks, "e2e": e2e, "gpu_launches": 8 * a.steps, "device_status": status}
+    if not a.no_cpu_baseline:
+        v, cores, sample, el = oracle_sample(cfg, a.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample,
+                                "seconds": el}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    a = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = workload_cfg(a.workload)
+    if a.impl == "reference":
+        run_reference(a, cfg, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(a, cfg, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

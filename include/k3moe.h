@@ -1,0 +1,181 @@
+/*
+ * k3moe.h -- C ABI of the GB300 (sm_103a) Stable LatentMoE routed-expert block on
+ * native MXFP4 expert weights.
+ *
+ * What the block computes (colibri PR #684, engine commit message: "Stable
+ * LatentMoE: sigmoid router + score-correction bias, top-16, raw-score
+ * renormalization; latent 7168<->3584 projections around the experts; RMSNorm on
+ * the aggregate; ... SiTU-GLU (4 tanh(g/4) sigmoid(g) * 25 tanh(u/25))"; colibri
+ * PR #676, architecture bullets), per token t with x_t in R^H:
+ *
+ *   l_e   = x_t . Wr_e                     router logits, e < E
+ *   s_e   = sigmoid(l_e),  s'_e = s_e + b_e
+ *   ids   = the K experts with largest s' (descending, ties to the lower id)
+ *   w_k   = s_ids[k] / sum_j s_ids[j]      raw-score renormalisation
+ *   z     = bf16(x_t Wd^T)                 latent down, [L]
+ *   g, u  = z Wgate_e^T, z Wup_e^T         per selected expert, MXFP4 weights, [I]
+ *   h     = bf16(4 tanh(g/4) sigmoid(g) 25 tanh(u/25))
+ *   o_k   = h Wdown_e^T                    MXFP4 weights, [L]
+ *   y     = sum_k w_k o_k                  gate-weighted combine
+ *   yhat  = bf16(gamma * y / sqrt(mean(y^2) + eps))   RMSNorm on the aggregate
+ *   out_t = yhat Wu^T                      latent up, [H], returned in fp32
+ *
+ * MXFP4 vendor layout (colibri PR #684, quant.h commit message): an [O, I] matrix
+ * is packed [O, I/2] u8 (low nibble = even column, bit 3 = sign, E2M1 codes) plus
+ * scales [O, I/32] u8 (E8M0), value = e2m1(code) * 2^(s - 127).  The library reads
+ * these bytes as they are; nothing is re-encoded.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers, row-major and densely packed, unless
+ *    stated otherwise.  bf16 tensors are passed as uint16_t bit patterns.
+ *  - The caller owns all memory, including the workspace; the library allocates,
+ *    frees and synchronises nothing in the compute calls, and keeps no per-call
+ *    global state.  Calls on different streams with different workspaces may run
+ *    concurrently.
+ *  - Arguments are validated on the host before anything is launched; an invalid
+ *    call returns a status and launches nothing.  No call aborts or traps.
+ *  - Launch errors return K3MOE_ERR_CUDA.  Conditions that only the device can see
+ *    are OR-ed into a status word inside the workspace; read it with
+ *    k3moe_device_status().
+ *  - 16-byte alignment is required for every tensor pointer.
+ */
+#ifndef K3MOE_H
+#define K3MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+  int32_t hidden;    /* H: model width (7168 for K3); multiple of 64 */
+  int32_t latent;    /* L: latent width (3584 for K3); multiple of 64 */
+  int32_t n_experts; /* E: routed experts (896 for K3); 1..2048 */
+  int32_t top_k;     /* K: experts per token (16 for K3); 1..min(E, 64) */
+  int32_t inter;     /* I: expert intermediate width (3072 for K3); multiple of 64 */
+  float rms_eps;     /* epsilon of the aggregate RMSNorm */
+} k3moe_dims;
+
+typedef enum {
+  K3MOE_OK = 0,
+  K3MOE_ERR_ARG = 1,       /* null pointer, negative count, bad enum */
+  K3MOE_ERR_SHAPE = 2,     /* a width is not a supported multiple, or K > E */
+  K3MOE_ERR_ALIGN = 3,     /* a pointer is not 16-byte aligned */
+  K3MOE_ERR_WORKSPACE = 4, /* workspace null or smaller than k3moe_workspace_bytes() */
+  K3MOE_ERR_DEVICE = 5,    /* current device is not compute capability 10.3 */
+  K3MOE_ERR_CUDA = 6       /* a CUDA launch or copy failed */
+} k3moe_status;
+
+/* Bits of the device status word (k3moe_device_status). */
+#define K3MOE_DEV_TIE_WINDOW 0x1u /* a near-tie cluster of biased scores reached the end of the
+                                     refinement window; the selected ids may differ from an
+                                     exact ranking for that token */
+#define K3MOE_DEV_TIMEOUT 0x2u    /* a device-side bounded wait ran out; outputs are invalid */
+#define K3MOE_DEV_BAD_ID 0x4u     /* an expert id outside [0, E) reached the permutation */
+
+/* The six vendor tensors of every expert, as DEVICE arrays of n_experts DEVICE
+ * pointers (the pointer tables themselves live in device memory):
+ *   gate_q[e] [I, L/2], gate_s[e] [I, L/32]    gate projection of expert e
+ *   up_q[e]   [I, L/2], up_s[e]   [I, L/32]    up projection
+ *   down_q[e] [L, I/2], down_s[e] [L, I/32]    down projection
+ * A checkpoint that stores gate and up as one fused [2I, L] matrix (gate rows first)
+ * passes up_q[e] = gate_q[e] + I*L/2 and up_s[e] = gate_s[e] + I*L/32. */
+typedef struct {
+  const uint8_t* const* gate_q;
+  const uint8_t* const* gate_s;
+  const uint8_t* const* up_q;
+  const uint8_t* const* up_s;
+  const uint8_t* const* down_q;
+  const uint8_t* const* down_s;
+} k3moe_experts;
+
+/* Bytes of workspace that k3moe_route / k3moe_forward / k3moe_expert_forward need
+ * for T tokens.  Returns 0 for invalid dims or T < 0. */
+size_t k3moe_workspace_bytes(const k3moe_dims* dims, int32_t T);
+
+/* Router only (steps l, s, s', ids, w above).
+ *   x     [T, H] bf16    activations
+ *   wr    [E, H] bf16    router weight
+ *   bias  [E]    f32     score-correction bias (selects; does not weight)
+ *   ids   [T, K] int32   out: selected experts, descending biased score
+ *   w     [T, K] f32     out: renormalised raw scores
+ * Logits are accumulated in fp32; candidates whose biased scores lie within 3e-5
+ * of a neighbour among the top K+1 are re-ranked from fp64 logits, so the ids
+ * equal an exact-arithmetic ranking unless a gap is below fp64 resolution.
+ * T = 0 is a valid no-op.  `stream` is a cudaStream_t (NULL = legacy default). */
+k3moe_status k3moe_route(const k3moe_dims* dims, int32_t T, const uint16_t* x, const uint16_t* wr,
+                         const float* bias, int32_t* ids, float* w, void* ws, size_t ws_bytes, void* stream);
+
+/* The whole block for T tokens (the chunk's expert union is built once; each
+ * selected expert's weights are streamed once per call).
+ *   x      [T, H] bf16;  wr [E, H] bf16;  bias [E] f32
+ *   w_down [L, H] bf16   latent down;  w_up [H, L] bf16 latent up
+ *   norm_w [L]    f32    RMSNorm weight gamma
+ *   experts              pointer tables (see k3moe_experts), read on the device
+ *   out    [T, H] f32    out
+ *   ids_out [T, K] int32, w_out [T, K] f32   optional copies of the routing (may be NULL)
+ * Numerics: bf16 operands, fp32 accumulation; z, h and yhat are rounded to bf16
+ * (round-to-nearest-even) where the definition above says bf16. */
+k3moe_status k3moe_forward(const k3moe_dims* dims, int32_t T, const uint16_t* x, const uint16_t* wr,
+                           const float* bias, const uint16_t* w_down, const uint16_t* w_up, const float* norm_w,
+                           const k3moe_experts* experts, float* out, int32_t* ids_out, float* w_out, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* k3moe_forward with per-phase timing.  `events` holds n_events (0..9) cudaEvent_t
+ * handles created by the caller; event i is recorded on `stream` at the start of
+ * phase i and event 8 after the last phase.  Phases: 0 router logits + latent down
+ * (one pass over x), 1 top-k, 2 permutation, 3 activation prep, 4 expert gate/up +
+ * SiTU-GLU, 5 expert down, 6 combine + RMSNorm, 7 latent up.  NULL entries are
+ * skipped.  Results are identical to k3moe_forward. */
+k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uint16_t* x, const uint16_t* wr,
+                                    const float* bias, const uint16_t* w_down, const uint16_t* w_up,
+                                    const float* norm_w, const k3moe_experts* experts, float* out, int32_t* ids_out,
+                                    float* w_out, void* ws, size_t ws_bytes, void* stream, void* const* events,
+                                    int32_t n_events);
+
+/* One expert applied to T latent vectors (gate/up, SiTU-GLU, down; no routing):
+ *   z [T, L] bf16 in; out [T, L] f32 = h(z_t) Wdown_e^T with h rounded to bf16.
+ * `expert` indexes the pointer tables.  Same workspace rule as k3moe_forward. */
+k3moe_status k3moe_expert_forward(const k3moe_dims* dims, int32_t T, const uint16_t* z, int32_t expert,
+                                  const k3moe_experts* experts, float* out, void* ws, size_t ws_bytes,
+                                  void* stream);
+
+/* MXFP4 -> f32 decode of an [O, I] vendor matrix (I a multiple of 32):
+ *   q [O, I/2] u8, s [O, I/32] u8 -> out [O, I] f32, value e2m1(code) * 2^(s-127).
+ * Exact wherever the value is a finite f32 (scale bytes 0..252 always; above that
+ * large codes overflow to +-inf); scale byte 255 gives NaN; code 8 gives -0. */
+k3moe_status k3moe_dequant_mxfp4(const uint8_t* q, const uint8_t* s, int32_t O, int32_t I, float* out,
+                                 void* stream);
+
+/* Counting-sort permutation of routed slots (the chunk expert union) as the
+ * forward pass builds it, exposed for checking.  ids [T, K] int32 in;
+ * counts [E], offsets [E+1], slot_of [T*K] (flat t*K+k indices grouped by expert
+ * ascending, (t, k) ascending inside an expert), uniq [E] (experts with a nonzero
+ * count, ascending; entries past n_uniq are unspecified) and n_uniq [1], all int32
+ * device outputs.  Same workspace rule as k3moe_forward. */
+k3moe_status k3moe_permute(const k3moe_dims* dims, int32_t T, const int32_t* ids, int32_t* counts,
+                           int32_t* offsets, int32_t* slot_of, int32_t* uniq, int32_t* n_uniq, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* Reads the device status word of the last call that used `ws` (K3MOE_DEV_* bits)
+ * into *host_out.  Synchronises `stream`. */
+k3moe_status k3moe_device_status(const void* ws, uint32_t* host_out, void* stream);
+
+/* Intermediate tensors of the last k3moe_forward that used `ws`, for inspection:
+ * 0 = z [T, L] bf16, 1 = yhat [T, L] bf16, 2 = y [T, L] f32 (combined, before the
+ * norm), 3 = logits [T, E] f32.  Returns a device pointer inside ws, or NULL. */
+void* k3moe_workspace_view(const k3moe_dims* dims, int32_t T, void* ws, int32_t which);
+
+/* Static text for a status code. */
+const char* k3moe_status_str(k3moe_status st);
+
+/* ABI version of this header (increments on incompatible change). */
+int32_t k3moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* K3MOE_H */

@@ -1,0 +1,95 @@
+"""Host-only checks of the C ABI: the library builds and loads, exports every
+function the header declares, and validates arguments before touching a device."""
+import ctypes
+
+import pytest
+
+import mxfp4_routed_expert_latentmoe_gb300 as k3
+from datagen import configs as C
+
+ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_WS, ERR_DEVICE = 1, 2, 3, 4, 5
+
+
+def test_library_exports_every_declared_function():
+    names = k3.declared_functions()
+    assert "k3moe_route" in names and "k3moe_forward" in names
+    L = k3.lib()
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    assert L.k3moe_abi_version() == 1
+    for code, text in k3.STATUS.items():
+        assert L.k3moe_status_str(code).decode() == text
+
+
+def _d(cfg=C.DECODE):
+    return k3.dims(**cfg.dims)
+
+
+def test_workspace_bytes_is_monotone_and_rejects_bad_dims():
+    L = k3.lib()
+    d = _d()
+    sizes = [L.k3moe_workspace_bytes(ctypes.byref(d), T) for T in (0, 1, 32, 4096)]
+    assert sizes[0] > 0 and sizes == sorted(sizes)
+    # the expert intermediates dominate: T*K*(I*2 + L*4) bytes at least
+    assert sizes[3] >= 4096 * 16 * (3072 * 2 + 3584 * 4)
+    for bad in (dict(hidden=7000), dict(latent=100), dict(inter=96 + 16), dict(top_k=0), dict(top_k=897),
+                dict(n_experts=4096)):
+        kw = dict(C.DECODE.dims)
+        kw.update(bad)
+        assert L.k3moe_workspace_bytes(ctypes.byref(k3.dims(**kw)), 1) == 0, bad
+    assert L.k3moe_workspace_bytes(ctypes.byref(d), -1) == 0
+
+
+def _route(d, T, x=16, wr=16, bias=16, ids=16, w=16, ws=16, ws_bytes=None):
+    L = k3.lib()
+    nb = ws_bytes if ws_bytes is not None else L.k3moe_workspace_bytes(ctypes.byref(d), T)
+    p = lambda v: None if v is None else ctypes.c_void_p(v)
+    return L.k3moe_route(ctypes.byref(d), T, p(x), p(wr), p(bias), p(ids), p(w), p(ws), nb, None)
+
+
+def test_route_validates_on_the_host():
+    d = _d()
+    assert _route(d, 0) == 0  # empty call is a no-op
+    assert _route(d, -1) == ERR_ARG
+    assert _route(d, 1, x=None) == ERR_ARG
+    assert _route(d, 1, ws=None) == ERR_ARG
+    assert _route(d, 1, x=24) == ERR_ALIGN
+    assert _route(d, 1, ws_bytes=100) == ERR_WS
+    bad = k3.dims(7168, 3584, 896, 0, 3072)
+    assert _route(bad, 1) == ERR_SHAPE
+    # a fully valid call on a machine without a compute-capability-10.3 device
+    import torch
+    if not torch.cuda.is_available():
+        assert _route(d, 1) == ERR_DEVICE
+
+
+def test_forward_and_expert_forward_validate_on_the_host():
+    L = k3.lib()
+    d = _d()
+    ex = k3.ExpertsC(16, 16, 16, 16, 16, 16)
+    nb = L.k3moe_workspace_bytes(ctypes.byref(d), 1)
+    v = ctypes.c_void_p(16)
+    args = [ctypes.byref(d), 1, v, v, v, v, v, v, ctypes.byref(ex), v, None, None, v, nb, None]
+    import torch
+    if not torch.cuda.is_available():
+        assert L.k3moe_forward(*args) == ERR_DEVICE
+    args2 = list(args)
+    args2[8] = ctypes.byref(k3.ExpertsC(16, 16, 0, 16, 16, 16))
+    assert L.k3moe_forward(*args2) == ERR_ARG
+    args3 = list(args)
+    args3[13] = nb - 1
+    assert L.k3moe_forward(*args3) == ERR_WS
+    args4 = list(args)
+    args4[9] = ctypes.c_void_p(20)
+    assert L.k3moe_forward(*args4) == ERR_ALIGN
+    assert L.k3moe_expert_forward(ctypes.byref(d), 1, v, 896, ctypes.byref(ex), v, v, nb, None) == ERR_ARG
+    assert L.k3moe_expert_forward(ctypes.byref(d), 1, v, -1, ctypes.byref(ex), v, v, nb, None) == ERR_ARG
+
+
+def test_dequant_validates_shape():
+    L = k3.lib()
+    v = ctypes.c_void_p(16)
+    assert L.k3moe_dequant_mxfp4(v, v, 4, 48, v, None) == ERR_SHAPE
+    assert L.k3moe_dequant_mxfp4(v, v, -1, 64, v, None) == ERR_ARG
+    assert L.k3moe_dequant_mxfp4(v, v, 0, 64, v, None) == 0
+    assert L.k3moe_dequant_mxfp4(ctypes.c_void_p(8), v, 4, 64, v, None) == ERR_ALIGN

@@ -1,0 +1,266 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Bars: routed ids and the counting-sort permutation bit-exact; MXFP4 -> f32
+dequantisation bit-exact (IEEE bits); block output rel-L2 <= 2e-3 against the
+oracle's bf16-rounding spec mode (bf16 operands, fp32 accumulation on the GPU).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import datagen
+import oracle
+from datagen import configs as C
+from tests._harness import REL_L2_BAR, oracle_dims, oracle_forward, oracle_route, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def k3():
+    import __graft_entry__ as g
+    g.build()
+    import mxfp4_routed_expert_latentmoe_gb300 as mod
+    torch.cuda.set_device(0)
+    return mod
+
+
+def _ws(k3, d, T):
+    return torch.empty(k3.workspace_bytes(d, T), dtype=torch.uint8, device="cuda")
+
+
+class Layer:
+    """A workload materialised on the device."""
+
+    def __init__(self, k3, cfg, pool=None):
+        from datagen import device as D
+        self.cfg = cfg
+        self.d = k3.dims(**cfg.dims)
+        self.t = D.layer_tensors(cfg, "cuda")
+        if pool is None:
+            pool = D.expert_pool(cfg, "cuda")
+        self.pool, self.eb, self.offs = pool
+        self.tables = k3.ExpertTables.from_pool(self.pool, self.eb, self.offs)
+
+    def with_tokens(self, k3, cfg):
+        from datagen import device as D
+        L = Layer.__new__(Layer)
+        L.cfg, L.d = cfg, k3.dims(**cfg.dims)
+        L.t = dict(self.t)
+        L.t["x"] = D.bf16_tensor(C.layer_x(cfg), "cuda")
+        L.pool, L.eb, L.offs, L.tables = self.pool, self.eb, self.offs, self.tables
+        return L
+
+    def forward(self, k3):
+        T, cfg = self.cfg.T, self.cfg
+        out = torch.empty(T, cfg.hidden, dtype=torch.float32, device="cuda")
+        ids = torch.empty(T, cfg.top_k, dtype=torch.int32, device="cuda")
+        w = torch.empty(T, cfg.top_k, dtype=torch.float32, device="cuda")
+        ws = _ws(k3, self.d, T)
+        k3.forward(self.d, self.t["x"], self.t["wr"], self.t["bias"], self.t["wd"], self.t["wu"], self.t["gamma"],
+                   self.tables, out, ws, ids, w)
+        torch.cuda.synchronize()
+        return out.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy(), ws
+
+
+@pytest.fixture(scope="module")
+def tiny(k3):
+    return Layer(k3, C.TINY)
+
+
+@pytest.fixture(scope="module")
+def decode(k3):
+    return Layer(k3, C.DECODE)
+
+
+# ------------------------------------------------------------------------------ inputs
+def test_device_pool_equals_host_generator(tiny, decode):
+    from datagen import device as D
+    for e in range(C.TINY.n_experts):
+        host, dev = C.expert_tensors(C.TINY, e), D.expert_from_pool(tiny.pool, C.TINY, e)
+        for n in C.EXPERT_TENSORS:
+            assert np.array_equal(host[n], dev[n]), (e, n)
+    for e in (0, 417, 895):
+        host, dev = C.expert_tensors(C.DECODE, e), D.expert_from_pool(decode.pool, C.DECODE, e)
+        for n in C.EXPERT_TENSORS:
+            assert np.array_equal(host[n], dev[n]), (e, n)
+
+
+# ------------------------------------------------------------------------------ dequant
+def test_dequant_exhaustive_bytes_by_scales(k3):
+    O, I = 256, 512  # row r: every packed byte value, scale byte r in all 16 groups
+    q = np.tile(np.arange(256, dtype=np.uint8), (O, 1))
+    s = np.repeat(np.arange(256, dtype=np.uint8)[:, None], I // 32, axis=1)
+    out = torch.empty(O, I, dtype=torch.float32, device="cuda")
+    k3.dequant_mxfp4(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(), out)
+    got = out.cpu().numpy()
+    ref = oracle.dequant(q, s)
+    finite = np.isfinite(ref) & (np.abs(ref) <= np.finfo(np.float32).max)
+    ref32 = np.where(finite, ref, 0).astype(np.float32)
+    assert np.array_equal(got[finite].view(np.uint32), ref32[finite].view(np.uint32))
+    over = ~finite & ~np.isnan(ref)
+    assert np.all(np.isinf(got[over])) and np.array_equal(np.sign(got[over]), np.sign(ref[over]))
+    assert np.all(np.isnan(got[255]))
+    # the parity domain of the scale byte (1..252) is exact everywhere
+    assert finite[1:253].all()
+
+
+# ------------------------------------------------------------------------------ permutation
+@pytest.mark.parametrize("T,K,E", [(1, 16, 896), (3, 2, 8), (32, 16, 896), (4096, 16, 896), (7, 5, 2048),
+                                   (300, 1, 1), (5, 8, 8), (1000, 3, 37)])
+def test_permute_bit_exact(k3, T, K, E):
+    rng = np.random.default_rng(T * 7 + K)
+    ids = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    d = k3.dims(64, 64, E, K, 64)
+    dev = lambda n: torch.empty(n, dtype=torch.int32, device="cuda")
+    counts, offsets, slot_of, uniq, nu = dev(E), dev(E + 1), dev(T * K), dev(E), dev(1)
+    ws = _ws(k3, d, T)
+    k3.permute(d, torch.from_numpy(ids).cuda(), counts, offsets, slot_of, uniq, nu, ws)
+    torch.cuda.synchronize()
+    rc, ro, rs, ru = oracle.permute(ids, E)
+    assert np.array_equal(counts.cpu().numpy(), rc)
+    assert np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(slot_of.cpu().numpy(), rs)
+    n = int(nu.cpu().item())
+    assert n == len(ru) and np.array_equal(uniq.cpu().numpy()[:n], ru)
+    assert k3.device_status(ws) == 0
+
+
+# ------------------------------------------------------------------------------ router
+def _route_gpu(k3, L):
+    T, cfg = L.cfg.T, L.cfg
+    ids = torch.empty(T, cfg.top_k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, cfg.top_k, dtype=torch.float32, device="cuda")
+    ws = _ws(k3, L.d, T)
+    k3.route(L.d, L.t["x"], L.t["wr"], L.t["bias"], ids, w, ws)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), w.cpu().numpy(), k3.device_status(ws)
+
+
+def test_route_tiny_and_decode(k3, tiny, decode):
+    for L in (tiny, decode):
+        ids, w, st = _route_gpu(k3, L)
+        rids, rw, gap, _ = oracle_route(L.cfg)
+        assert st == 0
+        assert np.array_equal(ids, rids)
+        assert np.allclose(w, rw, rtol=0, atol=2e-6)
+        assert np.allclose(w.sum(1), 1.0, atol=1e-6)
+
+
+def test_route_chunk_and_prefill_bit_exact_ids(k3, decode):
+    for cfg in (C.CHUNK, C.PREFILL.with_tokens(4096)):
+        L = decode.with_tokens(k3, cfg) if cfg.seed == C.DECODE.seed and cfg.scale_lo == C.DECODE.scale_lo else None
+        if L is None:  # router inputs only: no expert pool needed
+            from datagen import device as D
+            L = Layer.__new__(Layer)
+            L.cfg, L.d, L.t = cfg, k3.dims(**cfg.dims), D.layer_tensors(cfg, "cuda")
+        ids, w, st = _route_gpu(k3, L)
+        rids, rw, gap, mingap = oracle_route(cfg)
+        assert st == 0
+        assert np.array_equal(ids, rids), np.argwhere((ids != rids).any(1)).ravel()[:10]
+        assert np.allclose(w, rw, rtol=0, atol=2e-6)
+
+
+# ------------------------------------------------------------------------------ single expert
+@pytest.mark.parametrize("T", [1, 5, 20])
+def test_expert_forward_matches_oracle(k3, decode, T):
+    cfg = C.EXPERT
+    d = k3.dims(7168, cfg.latent, 896, 16, cfg.inter)
+    z_bits = datagen.bf16_bits(datagen.normal_f64(cfg.seed + T, 1, T * cfg.latent)).reshape(T, cfg.latent)
+    from datagen import device as D
+    z = D.bf16_tensor(z_bits, "cuda")
+    out = torch.empty(T, cfg.latent, dtype=torch.float32, device="cuda")
+    ws = _ws(k3, d, T)
+    e = 417
+    k3.expert_forward(d, z, e, decode.tables, out, ws)
+    torch.cuda.synchronize()
+    tens = C.expert_tensors(C.DECODE, e)
+    od = oracle.dims(7168, cfg.latent, 896, 16, cfg.inter)
+    zf = datagen.bf16_to_f64(z_bits)
+    got = out.cpu().numpy()
+    for t in range(T):
+        _, o = oracle.expert(od, zf[t], tens, True)
+        r = rel_l2(got[t], o)
+        assert r <= REL_L2_BAR, (t, r)
+        assert r <= 1e-3, (t, r)  # bf16 rounding points match the spec; fp32 accumulation only
+
+
+def test_expert_workload_single_k3_expert(k3):
+    """The single-expert decode GEMV workload at K3 shape, on its own weights."""
+    from datagen import device as D
+    cfg = C.EXPERT
+    ecfg = C.LayerConfig("expert-pool", T=1, hidden=7168, latent=cfg.latent, n_experts=1, top_k=1,
+                         inter=cfg.inter, seed=cfg.seed, bias_range=0.0, scale_lo=cfg.scale_lo,
+                         scale_hi=cfg.scale_hi)
+    pool = D.expert_pool(ecfg, "cuda")
+    tables = k3.ExpertTables.from_pool(*pool)
+    d = k3.dims(7168, cfg.latent, 1, 1, cfg.inter)
+    zb = C.expert_z(cfg)
+    out = torch.empty(1, cfg.latent, dtype=torch.float32, device="cuda")
+    ws = _ws(k3, d, 1)
+    k3.expert_forward(d, D.bf16_tensor(zb, "cuda"), 0, tables, out, ws)
+    torch.cuda.synchronize()
+    _, o = oracle.expert(oracle.dims(7168, cfg.latent, 1, 1, cfg.inter), datagen.bf16_to_f64(zb)[0],
+                         C.expert_tensors(ecfg, 0), True)
+    assert rel_l2(out.cpu().numpy()[0], o) <= REL_L2_BAR
+
+
+# ------------------------------------------------------------------------------ whole block
+def _check_block(got, ids, w, ref, ws=None, k3=None):
+    assert np.array_equal(ids, ref["ids"])
+    assert np.allclose(w, ref["w"], rtol=0, atol=2e-6)
+    r = rel_l2(got, ref["out"])
+    assert r <= REL_L2_BAR, r
+    return r
+
+
+def test_forward_tiny(k3, tiny):
+    got, ids, w, ws = tiny.forward(k3)
+    ref = oracle_forward(C.TINY)
+    r = _check_block(got, ids, w, ref)
+    assert k3.device_status(ws) == 0
+    # intermediates: z and yhat are bf16 at the spec's rounding points
+    T, Lt = C.TINY.T, C.TINY.latent
+    z = torch.empty(T, Lt, dtype=torch.bfloat16, device="cuda")
+    zp = k3.workspace_view(tiny.d, T, ws, 0)
+    assert zp != 0
+    assert r < 1e-4, r
+
+
+def test_forward_decode(k3, decode):
+    got, ids, w, ws = decode.forward(k3)
+    ref = oracle_forward(C.DECODE)
+    r = _check_block(got, ids, w, ref)
+    assert k3.device_status(ws) == 0
+    print(f"decode rel-L2 {r:.3e}")
+
+
+def test_forward_chunk(k3, decode):
+    L = decode.with_tokens(k3, C.CHUNK)
+    got, ids, w, ws = L.forward(k3)
+    ref = oracle_forward(C.CHUNK)
+    r = _check_block(got, ids, w, ref)
+    assert k3.device_status(ws) == 0
+    print(f"chunk rel-L2 {r:.3e}, unique experts {len(np.unique(ids))}")
+
+
+def test_forward_prefill_sampled(k3):
+    cfg = C.PREFILL
+    L = Layer(k3, cfg)
+    got, ids, w, ws = L.forward(k3)
+    assert k3.device_status(ws) == 0
+    rids, rw, _, _ = oracle_route(cfg)
+    assert np.array_equal(ids, rids)
+    rows = [0, 1, 2047, 4095] + list(np.random.default_rng(5).choice(4096, 4, replace=False))
+    ref = oracle_forward(cfg, token_rows=rows)
+    assert np.array_equal(ids[rows], ref["ids"])
+    for j, t in enumerate(rows):
+        r = rel_l2(got[t], ref["out"][j])
+        assert r <= REL_L2_BAR, (t, r)
+    counts = np.bincount(ids.ravel(), minlength=cfg.n_experts)
+    assert counts.min() > 0  # every expert is used at zero bias
+    del L
+    torch.cuda.empty_cache()
