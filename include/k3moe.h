@@ -135,6 +135,29 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
                                     float* w_out, void* ws, size_t ws_bytes, void* stream, void* const* events,
                                     int32_t n_events);
 
+/* k3moe_forward for callers that cannot allocate device memory: no workspace
+ * argument, and no cudaMalloc / cudaFree or allocating library call inside.  This
+ * suits code that runs where the allocator is off limits, e.g. a plugin inside a
+ * host framework that owns every device allocation, or a path that must not touch
+ * the allocator once it is set up.  The pages have no counterpart to this entry
+ * point; it is a packaging variant of k3moe_forward.
+ *  - Scratch lives in one fixed 4 MiB array in device memory that every GPU which
+ *    loads the library holds until the process exits; that is enough for K3 shapes
+ *    (H 7168, L 3584, E 896, K 16, I 3072) up to 8 tokens per call.  A call whose
+ *    dims and T need more scratch than that (k3moe_workspace_bytes) returns
+ *    K3MOE_ERR_WORKSPACE and launches nothing.
+ *  - The first call on a device looks up the array's device address with
+ *    cudaGetSymbolAddress (with that device current); make that first call before
+ *    any stream capture.
+ *  - Every call shares the array and leaves its contents behind (the call clears
+ *    what must start at zero).  Calls that overlap on the GPU, on any stream, race
+ *    on the array: serialise them.
+ * Arguments, results and other errors are those of k3moe_forward. */
+k3moe_status k3moe_forward_noalloc(const k3moe_dims* dims, int32_t T, const uint16_t* x, const uint16_t* wr,
+                                   const float* bias, const uint16_t* w_down, const uint16_t* w_up,
+                                   const float* norm_w, const k3moe_experts* experts, float* out, int32_t* ids_out,
+                                   float* w_out, void* stream);
+
 /* One expert applied to T latent vectors (gate/up, SiTU-GLU, down; no routing):
  *   z [T, L] bf16 in; out [T, L] f32 = h(z_t) Wdown_e^T with h rounded to bf16.
  * `expert` indexes the pointer tables.  Same workspace rule as k3moe_forward. */

@@ -87,6 +87,7 @@ def lib():
                 "k3moe_forward": ([D, i32, p, p, p, p, p, p, X, p, p, p, p, sz, p], ctypes.c_int),
                 "k3moe_forward_profiled": ([D, i32, p, p, p, p, p, p, X, p, p, p, p, sz, p, p, i32], ctypes.c_int),
                 "k3moe_expert_forward": ([D, i32, p, i32, X, p, p, sz, p], ctypes.c_int),
+                "k3moe_forward_noalloc": ([D, i32, p, p, p, p, p, p, X, p, p, p, p], ctypes.c_int),
                 "k3moe_dequant_mxfp4": ([p, p, i32, i32, p, p], ctypes.c_int),
                 "k3moe_permute": ([D, i32, p, p, p, p, p, p, p, sz, p], ctypes.c_int),
                 "k3moe_device_status": ([p, ctypes.POINTER(ctypes.c_uint32), p], ctypes.c_int),
@@ -164,6 +165,15 @@ def forward(d: Dims, x, wr, bias, w_down, w_up, norm_w, experts: ExpertTables, o
     _check(lib().k3moe_forward(ctypes.byref(d), x.shape[0], _ptr(x), _ptr(wr), _ptr(bias), _ptr(w_down), _ptr(w_up),
                                _ptr(norm_w), ctypes.byref(experts.c), _ptr(out), _ptr(ids_out), _ptr(w_out), _ptr(ws),
                                ws.numel() * ws.element_size(), _stream(stream)), "k3moe_forward")
+
+
+def forward_noalloc(d: Dims, x, wr, bias, w_down, w_up, norm_w, experts: ExpertTables, out, ids_out=None,
+                    w_out=None, stream=None):
+    """k3moe_forward_noalloc: the block without a caller workspace (the library's own
+    fixed device scratch; see include/k3moe.h for its size limit and sharing rules)."""
+    _check(lib().k3moe_forward_noalloc(ctypes.byref(d), x.shape[0], _ptr(x), _ptr(wr), _ptr(bias), _ptr(w_down),
+                                       _ptr(w_up), _ptr(norm_w), ctypes.byref(experts.c), _ptr(out), _ptr(ids_out),
+                                       _ptr(w_out), _stream(stream)), "k3moe_forward_noalloc")
 
 
 PHASES = ("proj", "topk", "permute", "prep", "gateup", "down", "combine", "up")

@@ -444,6 +444,44 @@ void* k3moe_workspace_view(const k3moe_dims* dims, int32_t T, void* ws, int32_t 
   }
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------- allocation-free entry
+// Scratch for k3moe_forward_noalloc: a fixed array in device memory that every GPU
+// loading this library holds until the process exits.
+#define K3MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+static __device__ __align__(256) uint8_t g_k3_noalloc_scratch[K3MOE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+// device address of the scratch array, looked up once per device (host code cannot
+// use the array's name as a device pointer)
+void* g_noalloc_ptr[kMaxDevices];
+std::atomic<bool> g_noalloc_ready[kMaxDevices];
+}  // namespace
+
+extern "C" {
+
+k3moe_status k3moe_forward_noalloc(const k3moe_dims* dims, int32_t T, const uint16_t* x, const uint16_t* wr,
+                                   const float* bias, const uint16_t* w_down, const uint16_t* w_up,
+                                   const float* norm_w, const k3moe_experts* experts, float* out, int32_t* ids_out,
+                                   float* w_out, void* stream) {
+  k3moe_status st = check_dims(dims);
+  if (st != K3MOE_OK) return st;
+  if (T < 0) return K3MOE_ERR_ARG;
+  if (T == 0) return K3MOE_OK;
+  if (ws_layout(*dims, T).total > K3MOE_NOALLOC_SCRATCH_BYTES) return K3MOE_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return K3MOE_ERR_DEVICE;
+  if (!g_noalloc_ready[dev].load(std::memory_order_acquire)) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_k3_noalloc_scratch) != cudaSuccess || !p) return K3MOE_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+    g_noalloc_ready[dev].store(true, std::memory_order_release);
+  }
+  return k3moe_forward(dims, T, x, wr, bias, w_down, w_up, norm_w, experts, out, ids_out, w_out, g_noalloc_ptr[dev],
+                       K3MOE_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 const char* k3moe_status_str(k3moe_status st) {
   switch (st) {
     case K3MOE_OK: return "ok";
