@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle baseline")
+    ap.add_argument("--no-graph", action="store_true", help="launch the forward eagerly instead of replaying a graph")
+    ap.add_argument("--n-experts", type=int, default=None,
+                    help="profiling case: a smaller expert pool with the same per-expert shapes and top-k")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -317,27 +320,57 @@ def run_ours(a, cfg, rank, world, local_rank):
     status = k3.device_status(ws)
     n_unique = int(np.unique(ids.cpu().numpy()).size)
 
+    # the headline step: one k3moe_forward captured into a CUDA graph (its kernels and
+    # memsets, chained with programmatic dependent launch) and replayed
+    step = lambda: k3.forward(*args, ids_out=ids, w_out=wts)
+    graph = None
+    if not a.no_graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        step = graph.replay
+        for _ in range(a.warmup):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
     gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
     sampler = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}")
     time.sleep(0.3)
-    evs = [RawEvents(9) for _ in range(a.steps)]
+    # timed region 1: the headline number, plain k3moe_forward (kernels chained with
+    # programmatic dependent launch), one event pair per step
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
     barrier()
     torch.cuda.synchronize()
     w0 = time.time()
     for s in range(a.steps):
         flush.zero_()
-        k3.forward_profiled(*args, evs[s].handles, ids_out=ids, w_out=wts)
+        ev[s][0].record()
+        step()
+        ev[s][1].record()
     torch.cuda.synchronize()
     barrier()
     w1 = time.time()
-    per_step = [evs[s].ms(0, 8) for s in range(a.steps)]
-    phase_ms = {name: statistics.mean(evs[s].ms(i, i + 1) for s in range(a.steps)) for i, name in enumerate(k3.PHASES)}
-    ms = statistics.mean(per_step)
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
     if world > 1:
         tt = torch.tensor([ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
     clocks = sampler.summary(w0, w1)
+    # timed region 2: per-kernel durations, events recorded by the library between phases
+    nph = len(k3.PHASES)
+    pev = [RawEvents(nph + 1) for _ in range(a.steps)]
+    torch.cuda.synchronize()
+    for s in range(a.steps):
+        flush.zero_()
+        k3.forward_profiled(*args, pev[s].handles, ids_out=ids, w_out=wts)
+    torch.cuda.synchronize()
+    phase_ms = {name: statistics.mean(pev[s].ms(i, i + 1) for s in range(a.steps)) for i, name in enumerate(k3.PHASES)}
+    profiled_ms = statistics.mean(pev[s].ms(0, nph) for s in range(a.steps))
 
     # end to end through the public API with host buffers
     e2e = None
@@ -395,11 +428,12 @@ def run_ours(a, cfg, rank, world, local_rank):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": describe(cfg), "global_batch": cfg.T * world, "seq_len": cfg.T,
                        "parallelism": f"replicas x{world}", "l2": "flushed by a 256 MiB write before every timed step",
-                       "unique_experts": n_unique},
+                       "unique_experts": n_unique, "cuda_graph": graph is not None},
             "roofline": roof,
             "expert_phase": {"us": expert_us, "GB_s": exp_bytes / (expert_us / 1e6) / 1e9,
                              "frac_hbm": exp_bytes / (expert_us / 1e6) / 1e9 / peaks["hbm_gbs"]},
-            "phases": phases, "clocks": clocks, "e2e": e2e, "gpu_launches": 8 * a.steps, "device_status": status}
+            "phases": phases, "profiled_ms_per_step": profiled_ms, "clocks": clocks, "e2e": e2e,
+            "gpu_launches": (6 if cfg.T <= 64 else 8) * a.steps, "device_status": status}
     if not a.no_cpu_baseline:
         v, cores, sample, el = oracle_sample(cfg, a.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample,
@@ -413,6 +447,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     cfg = workload_cfg(a.workload)
+    if a.n_experts:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, n_experts=a.n_experts, name=cfg.name)
     if a.impl == "reference":
         run_reference(a, cfg, rank, world)
         return

@@ -123,12 +123,13 @@ k3moe_status k3moe_forward(const k3moe_dims* dims, int32_t T, const uint16_t* x,
                            const k3moe_experts* experts, float* out, int32_t* ids_out, float* w_out, void* ws,
                            size_t ws_bytes, void* stream);
 
-/* k3moe_forward with per-phase timing.  `events` holds n_events (0..9) cudaEvent_t
+/* k3moe_forward with per-phase timing.  `events` holds n_events (0..7) cudaEvent_t
  * handles created by the caller; event i is recorded on `stream` at the start of
- * phase i and event 8 after the last phase.  Phases: 0 router logits + latent down
- * (one pass over x), 1 top-k, 2 permutation, 3 activation prep, 4 expert gate/up +
- * SiTU-GLU, 5 expert down, 6 combine + RMSNorm, 7 latent up.  NULL entries are
- * skipped.  Results are identical to k3moe_forward. */
+ * phase i and event 6 after the last phase.  Phases: 0 router logits + latent down
+ * (one pass over x), 1 top-k + permutation + activation prep, 2 expert gate/up +
+ * SiTU-GLU, 3 expert down, 4 combine + RMSNorm, 5 latent up.  NULL entries are
+ * skipped.  With events the kernels run strictly one after another (k3moe_forward
+ * lets each kernel start while its predecessor drains); results are identical. */
 k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uint16_t* x, const uint16_t* wr,
                                     const float* bias, const uint16_t* w_down, const uint16_t* w_up,
                                     const float* norm_w, const k3moe_experts* experts, float* out, int32_t* ids_out,

@@ -176,12 +176,12 @@ def forward_noalloc(d: Dims, x, wr, bias, w_down, w_up, norm_w, experts: ExpertT
                                        _ptr(w_out), _stream(stream)), "k3moe_forward_noalloc")
 
 
-PHASES = ("proj", "topk", "permute", "prep", "gateup", "down", "combine", "up")
+PHASES = ("proj", "route", "gateup", "down", "combine", "up")
 
 
 def forward_profiled(d: Dims, x, wr, bias, w_down, w_up, norm_w, experts: ExpertTables, out, ws, events,
                      ids_out=None, w_out=None, stream=None):
-    """k3moe_forward recording the given CUDA event handles (up to 9, cudaEvent_t as ints or
+    """k3moe_forward recording the given CUDA event handles (up to 7, cudaEvent_t as ints or
     c_void_p) at phase boundaries."""
     arr = (ctypes.c_void_p * len(events))(*[e.value if isinstance(e, ctypes.c_void_p) else e for e in events])
     _check(lib().k3moe_forward_profiled(ctypes.byref(d), x.shape[0], _ptr(x), _ptr(wr), _ptr(bias), _ptr(w_down),

@@ -23,41 +23,28 @@ K3_DEVI void cp_async16(uint32_t dst, const void* src) {
 K3_DEVI void cp_async8(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src));
 }
-K3_DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+K3_DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 K3_DEVI void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+// Shared-memory reads as plain C++ loads (the compiler may schedule them freely
+// between the memory barriers that cp_async_wait / __syncwarp / __syncthreads are).
 K3_DEVI uint32_t lds32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(a));
-  return v;
+  return *reinterpret_cast<const uint32_t*>(__cvta_shared_to_generic(a));
 }
-K3_DEVI uint2 lds64(uint32_t a) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(a));
-  return v;
-}
+K3_DEVI uint2 lds64(uint32_t a) { return *reinterpret_cast<const uint2*>(__cvta_shared_to_generic(a)); }
 
 // read-only 16-byte / 8-byte global loads for activations (small, reused: keep in L1)
-K3_DEVI uint4 ldg128(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];\n"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-K3_DEVI uint2 ldg64(const void* p) {
-  uint2 v;
-  asm volatile("ld.global.nc.v2.b32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
-}
+K3_DEVI uint4 ldg128(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+K3_DEVI uint2 ldg64(const void* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
 
 // ------------------------------------------------------------------ tensor-core MMA (m16n8k16)
 // D = A * B + C, A 16x16 row-major fragment (4 regs), B 16x8 col fragment (2 regs), fp32 accumulate.
+// (pure register operations: not volatile, so the compiler can interleave them)
 K3_DEVI void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1, const float (&c)[4]) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%10,%11,%12,%13};\n"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -65,12 +52,23 @@ K3_DEVI void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_
         "f"(c[3]));
 }
 K3_DEVI void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1, const float (&c)[4]) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%10,%11,%12,%13};\n"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
         "f"(c[3]));
+}
+
+// d = a * b + c on two fp32 lanes at once (packed FMA)
+K3_DEVI void ffma2(float& d0, float& d1, float a0, float a1, float b, float c0, float c1) {
+  uint64_t rd;
+  const uint64_t ra = ((uint64_t)__float_as_uint(a1) << 32) | __float_as_uint(a0);
+  const uint64_t rb = ((uint64_t)__float_as_uint(b) << 32) | __float_as_uint(b);
+  const uint64_t rc = ((uint64_t)__float_as_uint(c1) << 32) | __float_as_uint(c0);
+  asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  d0 = __uint_as_float((uint32_t)rd);
+  d1 = __uint_as_float((uint32_t)(rd >> 32));
 }
 
 // ------------------------------------------------------------------ MXFP4 decode
@@ -94,6 +92,19 @@ K3_DEVI float ue8m0_to_f32(uint32_t s) {
   uint32_t bits = (s == 0u) ? 0x00400000u : ((s == 255u) ? 0x7FC00000u : (s << 23));
   return __uint_as_float(bits);
 }
+// Fast form used inside the GEMVs: byte k of a 4-byte word w placed in the f32
+// exponent field (2 integer ops).  Equal to ue8m0_to_f32 for bytes 1..254; byte 0
+// gives 0 instead of 2^-127 (a difference below 6*2^-127 per weight, far under fp32
+// resolution of any sum it enters) and byte 255 gives +inf instead of NaN (the
+// result is non-finite either way).
+template <int K>
+K3_DEVI float ue8m0_byte_to_f32(uint32_t w) {
+  if constexpr (K == 3) {
+    return __uint_as_float((w >> 1) & 0x7F800000u);
+  } else {
+    return __uint_as_float((w << (23 - 8 * K)) & 0x7F800000u);
+  }
+}
 
 // ------------------------------------------------------------------ numerics
 K3_DEVI float sigmoidf_(float a) { return 1.0f / (1.0f + expf(-a)); }
@@ -105,6 +116,26 @@ K3_DEVI uint16_t f32_to_bf16_bits(float v) {
   return *reinterpret_cast<uint16_t*>(&b);
 }
 K3_DEVI float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// ------------------------------------------------------------------ programmatic dependent launch
+// Wait until the previous kernel in the stream has completed and its writes are
+// visible (no-op when the kernel was launched without the programmatic attribute).
+K3_DEVI void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Allow the next kernel in the stream to start launching.
+K3_DEVI void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+// ------------------------------------------------------------------ token batches
+// One batch of up to MX_MAX_NB tokens routed to one expert (written by the
+// permutation, read by the expert kernels): the expert's six vendor tensors, the
+// batch's first sorted slot and size, and its tokens.  128 bytes.
+constexpr int MX_MAX_NB = 16;
+struct __align__(16) MxBatch {
+  const uint8_t* w[6];  // gate_q, gate_s, up_q, up_s, down_q, down_s
+  int32_t slot0, n;
+  int32_t tok[MX_MAX_NB];
+  int32_t pad[2];
+};
+static_assert(sizeof(MxBatch) == 128, "batch record is 128 bytes");
 
 // ------------------------------------------------------------------ status word
 K3_DEVI void flag_status(uint32_t* status, uint32_t bits) {

@@ -29,23 +29,16 @@ constexpr int MX_GPW = 8;                      // 32-element groups per warp sli
 constexpr int MX_ROWS = 16;                    // rows per item
 constexpr int MX_Q_BYTES = MX_ROWS * MX_GPW * 16;  // packed bytes per matrix per stage (2048)
 constexpr int MX_S_BYTES = MX_ROWS * MX_GPW;       // scale bytes per matrix per stage (128)
+constexpr int MX_REC_BYTES = 128;                  // batch record copy per stage
 constexpr int MX_MAX_THREADS = 512;
 
 enum { MX_GATEUP = 0, MX_DOWN = 1 };
 
 struct MxGemvParams {
-  const uint8_t* const* q0;  // gate (GATEUP) / down (DOWN) packed tables
-  const uint8_t* const* s0;
-  const uint8_t* const* q1;  // up (GATEUP)
-  const uint8_t* const* s1;
-  int R;  // rows per matrix
-  int K;  // reduction length
-  const int32_t* uniq;
-  const int32_t* n_uniq;
-  const int32_t* counts;
-  const int32_t* offsets;
-  const int32_t* nb_prefix;  // [n_uniq + 1] prefix of per-expert token batches
-  const int32_t* slot_tok;   // sorted slot -> token
+  const MxBatch* batches;    // token batches (one expert each), written by the permutation
+  const int32_t* n_batches;  // number of batches
+  int R;                     // rows per matrix
+  int K;                     // reduction length
   const __half* act;         // GATEUP: z16 [T, K]; DOWN: h16 [slots, K]
   const int32_t* act_pow;    // GATEUP: per-token exponent p (z16 = z * 2^p)
   void* out;                 // GATEUP: h16 [slots, R] (h * 2^8); DOWN: o f32 [slots, R]
@@ -53,53 +46,39 @@ struct MxGemvParams {
 
 template <int M, int STAGES>
 struct MxLayout {
-  static constexpr int STAGE_BYTES = M * (MX_Q_BYTES + MX_S_BYTES);
+  static constexpr int STAGE_BYTES = M * (MX_Q_BYTES + MX_S_BYTES) + MX_REC_BYTES;
   static constexpr int WARP_BYTES = STAGES * STAGE_BYTES;
 };
 
-struct MxItem {
-  int e, row0, slot0, n;
-};
-
-K3_DEVI void mx_item(const MxGemvParams& p, int tiles, int NB, int i, MxItem& it) {
+// lanes 0..15 each hold one 8-byte word of a batch record
+K3_DEVI uint64_t mx_load_record(const MxGemvParams& p, int tiles, int i, int lane) {
   const int gb = i / tiles;
-  const int tile = i - gb * tiles;
-  int lo = 0, hi = *p.n_uniq;  // nb_prefix[lo] <= gb < nb_prefix[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (p.nb_prefix[mid] <= gb) lo = mid;
-    else hi = mid;
-  }
-  const int e = p.uniq[lo];
-  const int b = gb - p.nb_prefix[lo];
-  it.e = e;
-  it.row0 = tile * MX_ROWS;
-  it.slot0 = p.offsets[e] + b * NB;
-  it.n = min(NB, p.counts[e] - b * NB);
+  return lane < 16 ? reinterpret_cast<const uint64_t*>(p.batches + gb)[lane] : 0ull;
 }
 
-template <int M, int STAGES>
-K3_DEVI void mx_issue(const MxGemvParams& p, const MxItem& it, int warp, int lane, int ngroups, uint32_t stage) {
+// issue the cp.async copies of item i (record `rec`, lane-distributed) into `stage`
+template <int MODE, int M>
+K3_DEVI void mx_issue(const MxGemvParams& p, int tiles, int i, uint64_t rec, int warp, int lane, int ngroups,
+                      uint32_t stage) {
   const size_t qrow = (size_t)p.K / 2, srow = (size_t)p.K / 32;
   const bool sc_async = (p.K % 256) == 0;
+  const int row0 = (i % tiles) * MX_ROWS;
+  constexpr int WOFF = (MODE == MX_GATEUP) ? 0 : 4;
 #pragma unroll
   for (int m = 0; m < M; ++m) {
-    const uint8_t* q = (m == 0 ? p.q0 : p.q1)[it.e];
-    const uint8_t* s = (m == 0 ? p.s0 : p.s1)[it.e];
+    const uint8_t* q = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, rec, WOFF + 2 * m));
+    const uint8_t* s = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, rec, WOFF + 2 * m + 1));
     const uint32_t sq = stage + m * (MX_Q_BYTES + MX_S_BYTES);
     const uint32_t ss = sq + MX_Q_BYTES;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int c = lane + 32 * i;
+    for (int k = 0; k < 4; ++k) {
+      const int c = lane + 32 * k;
       const int r = c >> 3, j = c & 7;
-      if (j < ngroups) {
-        const int row = min(it.row0 + r, p.R - 1);
-        cp_async16(sq + r * 128 + ((j ^ (r & 7)) << 4), q + (size_t)row * qrow + (size_t)warp * 128 + j * 16);
-      }
+      if (j < ngroups)
+        cp_async16(sq + r * 128 + ((j ^ (r & 7)) << 4), q + (size_t)(row0 + r) * qrow + (size_t)warp * 128 + j * 16);
     }
     if (lane < MX_ROWS) {
-      const int row = min(it.row0 + lane, p.R - 1);
-      const uint8_t* src = s + (size_t)row * srow + (size_t)warp * MX_GPW;
+      const uint8_t* src = s + (size_t)(row0 + lane) * srow + (size_t)warp * MX_GPW;
       if (sc_async) {
         cp_async8(ss + lane * 8, src);
       } else {  // partial slice or unaligned scale rows: plain byte copies (small shapes only)
@@ -108,51 +87,72 @@ K3_DEVI void mx_issue(const MxGemvParams& p, const MxItem& it, int warp, int lan
       }
     }
   }
+  // the record rides with the stage (word 15, padding in memory, carries the row tile)
+  if (lane < 16) {
+    const uint64_t v = (lane == 15) ? (uint64_t)(uint32_t)row0 : rec;
+    *reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(stage + M * (MX_Q_BYTES + MX_S_BYTES) + 8 * lane)) = v;
+  }
 }
 
-template <int MODE, int NBLK, int STAGES>
+// PRE: the expert weights of the first items are requested before waiting for the
+// previous kernel (programmatic dependent launch); only the activations wait.
+// FULL: every warp's K slice is a whole 8 groups (K a multiple of 256).
+template <int MODE, int NBLK, int STAGES, bool PRE, bool FULL>
 __global__ void __launch_bounds__(MX_MAX_THREADS) k3_mx_gemv_kernel(MxGemvParams p) {
   constexpr int M = (MODE == MX_GATEUP) ? 2 : 1;
-  constexpr int NB = 8 * NBLK;
   using Lay = MxLayout<M, STAGES>;
+  constexpr int RED = M * NBLK * 128;  // floats of one warp's partial sums
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int col_pw[2][MX_MAX_NB];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int g = lane >> 2, t = lane & 3;
-  const int ngroups = min(MX_GPW, p.K / 32 - warp * MX_GPW);
+  const int ngroups = FULL ? MX_GPW : min(MX_GPW, p.K / 32 - warp * MX_GPW);
   const uint32_t wbase = smem_u32(smem) + warp * Lay::WARP_BYTES;
-  float* red = reinterpret_cast<float*>(smem + nwarps * Lay::WARP_BYTES);
-
+  float* red = reinterpret_cast<float*>(smem + nwarps * Lay::WARP_BYTES);  // [2][nwarps][RED]
   const int tiles = p.R / MX_ROWS;
-  const int total = tiles * p.nb_prefix[*p.n_uniq];
+
+  if (!PRE) grid_dep_wait();
+  const int total = tiles * (*p.n_batches);
   const int n_mine = (total > (int)blockIdx.x) ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
-  // prologue
+  // prologue: the first STAGES-1 items
 #pragma unroll
   for (int s = 0; s < STAGES - 1; ++s) {
     if (s < n_mine) {
-      MxItem it;
-      mx_item(p, tiles, NB, blockIdx.x + s * gridDim.x, it);
-      mx_issue<M, STAGES>(p, it, warp, lane, ngroups, wbase + s * Lay::STAGE_BYTES);
+      const int i = blockIdx.x + s * gridDim.x;
+      mx_issue<MODE, M>(p, tiles, i, mx_load_record(p, tiles, i, lane), warp, lane, ngroups,
+                        wbase + s * Lay::STAGE_BYTES);
     }
     cp_async_commit();
   }
+  uint64_t rec_next = (STAGES - 1 < n_mine) ? mx_load_record(p, tiles, blockIdx.x + (STAGES - 1) * gridDim.x, lane)
+                                            : 0ull;
+  if (PRE) grid_dep_wait();
+  grid_dep_launch();
+
+  // single-token batches of the same token (decode) share their activation fragments:
+  // this warp's 8 groups stay in registers across items
+  constexpr bool CACHE_B = (MODE == MX_GATEUP) && (NBLK == 1);
+  uint4 bcache[CACHE_B ? MX_GPW : 1];
+  int bkey = -1;
 
   for (int s = 0; s < n_mine; ++s) {
     {
       const int sn = s + STAGES - 1;
-      if (sn < n_mine) {
-        MxItem itn;
-        mx_item(p, tiles, NB, blockIdx.x + sn * gridDim.x, itn);
-        mx_issue<M, STAGES>(p, itn, warp, lane, ngroups, wbase + (sn % STAGES) * Lay::STAGE_BYTES);
-      }
+      if (sn < n_mine)
+        mx_issue<MODE, M>(p, tiles, blockIdx.x + sn * gridDim.x, rec_next, warp, lane, ngroups,
+                          wbase + (sn % STAGES) * Lay::STAGE_BYTES);
       cp_async_commit();
+      if (sn + 1 < n_mine) rec_next = mx_load_record(p, tiles, blockIdx.x + (sn + 1) * gridDim.x, lane);
     }
-    MxItem it;
-    mx_item(p, tiles, NB, blockIdx.x + s * gridDim.x, it);
     cp_async_wait<STAGES - 1>();
     __syncwarp();
 
-    const uint32_t stage = wbase + (s % STAGES) * Lay::STAGE_BYTES;
+    const uint8_t* stp = smem + warp * Lay::WARP_BYTES + (s % STAGES) * Lay::STAGE_BYTES;
+    const int32_t* rec = reinterpret_cast<const int32_t*>(stp + M * (MX_Q_BYTES + MX_S_BYTES));
+    const int slot0 = rec[12], n = rec[13], row0 = rec[30];
+    if (MODE == MX_GATEUP && warp == 0 && lane < n) col_pw[s & 1][lane] = p.act_pow[rec[14 + lane]];
+
     float acc[M][NBLK][4];
 #pragma unroll
     for (int m = 0; m < M; ++m)
@@ -161,36 +161,43 @@ __global__ void __launch_bounds__(MX_MAX_THREADS) k3_mx_gemv_kernel(MxGemvParams
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[m][nb][q] = 0.f;
 
-    if (ngroups > 0) {
-      // activation pointers of this lane's token column in every 8-token block
+    if (FULL || ngroups > 0) {
+      // activation row of this lane's token column in every 8-token block (columns
+      // past the batch repeat its last token: their results are never stored)
       const __half* bptr[NBLK];
-      bool bval[NBLK];
 #pragma unroll
       for (int nb = 0; nb < NBLK; ++nb) {
-        const int col = nb * 8 + g;
-        bval[nb] = col < it.n;
-        const int slot = it.slot0 + (bval[nb] ? col : 0);
-        const int row = (MODE == MX_GATEUP) ? p.slot_tok[slot] : slot;
+        const int col = min(nb * 8 + g, n - 1);
+        const int row = (MODE == MX_GATEUP) ? rec[14 + col] : slot0 + col;
         bptr[nb] = p.act + (size_t)row * p.K + warp * 256 + 8 * t;
+      }
+      if (CACHE_B) {
+        const int key = (n == 1) ? rec[14] : -1;
+        if (key < 0 || key != bkey) {
+#pragma unroll
+          for (int j = 0; j < MX_GPW; ++j)
+            if (FULL || j < ngroups) bcache[CACHE_B ? j : 0] = ldg128(bptr[0] + 32 * j);
+          bkey = key;
+        }
       }
       uint2 sc_lo[M], sc_hi[M];
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        const uint32_t ss = stage + m * (MX_Q_BYTES + MX_S_BYTES) + MX_Q_BYTES;
-        sc_lo[m] = lds64(ss + g * 8);
-        sc_hi[m] = lds64(ss + (g + 8) * 8);
+        const uint8_t* ss = stp + m * (MX_Q_BYTES + MX_S_BYTES) + MX_Q_BYTES;
+        sc_lo[m] = *reinterpret_cast<const uint2*>(ss + g * 8);
+        sc_hi[m] = *reinterpret_cast<const uint2*>(ss + (g + 8) * 8);
       }
 #pragma unroll
       for (int j = 0; j < MX_GPW; ++j) {
-        if (j < ngroups) {
+        if (FULL || j < ngroups) {
           uint32_t a0[M][4], a1[M][4];
           float slo[M], shi[M];
 #pragma unroll
           for (int m = 0; m < M; ++m) {
-            const uint32_t sq = stage + m * (MX_Q_BYTES + MX_S_BYTES);
-            const uint32_t off = ((j ^ g) << 4) + 4 * t;
-            const uint32_t wlo = lds32(sq + g * 128 + off);
-            const uint32_t whi = lds32(sq + (g + 8) * 128 + off);
+            const uint8_t* sq = stp + m * (MX_Q_BYTES + MX_S_BYTES);
+            const int off = ((j ^ g) << 4) + 4 * t;
+            const uint32_t wlo = *reinterpret_cast<const uint32_t*>(sq + g * 128 + off);
+            const uint32_t whi = *reinterpret_cast<const uint32_t*>(sq + (g + 8) * 128 + off);
             uint32_t plo[4], phi[4];
             e2m1x8_to_f16x8(wlo, plo);
             e2m1x8_to_f16x8(whi, phi);
@@ -201,61 +208,61 @@ __global__ void __launch_bounds__(MX_MAX_THREADS) k3_mx_gemv_kernel(MxGemvParams
             a1[m][0] = plo[2]; a1[m][1] = phi[2]; a1[m][2] = plo[3]; a1[m][3] = phi[3];
             const uint32_t blo = (j < 4) ? sc_lo[m].x : sc_lo[m].y;
             const uint32_t bhi = (j < 4) ? sc_hi[m].x : sc_hi[m].y;
-            slo[m] = ue8m0_to_f32((blo >> (8 * (j & 3))) & 0xFFu);
-            shi[m] = ue8m0_to_f32((bhi >> (8 * (j & 3))) & 0xFFu);
+            if ((j & 3) == 0) { slo[m] = ue8m0_byte_to_f32<0>(blo); shi[m] = ue8m0_byte_to_f32<0>(bhi); }
+            if ((j & 3) == 1) { slo[m] = ue8m0_byte_to_f32<1>(blo); shi[m] = ue8m0_byte_to_f32<1>(bhi); }
+            if ((j & 3) == 2) { slo[m] = ue8m0_byte_to_f32<2>(blo); shi[m] = ue8m0_byte_to_f32<2>(bhi); }
+            if ((j & 3) == 3) { slo[m] = ue8m0_byte_to_f32<3>(blo); shi[m] = ue8m0_byte_to_f32<3>(bhi); }
           }
 #pragma unroll
           for (int nb = 0; nb < NBLK; ++nb) {
-            if (nb * 8 < it.n) {
-              uint4 b = make_uint4(0u, 0u, 0u, 0u);
-              if (bval[nb]) b = ldg128(bptr[nb] + 32 * j);
+            if (NBLK == 1 || nb * 8 < n) {
+              const uint4 b = CACHE_B ? bcache[CACHE_B ? j : 0] : ldg128(bptr[nb] + 32 * j);
 #pragma unroll
               for (int m = 0; m < M; ++m) {
                 const float z4[4] = {0.f, 0.f, 0.f, 0.f};
                 float d[4];
                 mma_f16(d, a0[m], b.x, b.y, z4);
                 mma_f16(d, a1[m], b.z, b.w, d);
-                acc[m][nb][0] = fmaf(d[0], slo[m], acc[m][nb][0]);
-                acc[m][nb][1] = fmaf(d[1], slo[m], acc[m][nb][1]);
-                acc[m][nb][2] = fmaf(d[2], shi[m], acc[m][nb][2]);
-                acc[m][nb][3] = fmaf(d[3], shi[m], acc[m][nb][3]);
+                ffma2(acc[m][nb][0], acc[m][nb][1], d[0], d[1], slo[m], acc[m][nb][0], acc[m][nb][1]);
+                ffma2(acc[m][nb][2], acc[m][nb][3], d[2], d[3], shi[m], acc[m][nb][2], acc[m][nb][3]);
               }
             }
           }
         }
       }
     }
-    __syncwarp();
-    // per-warp partials -> shared memory: red[warp][m][nb][row 16][col 8]
+    // per-warp partials -> shared memory: red[s & 1][warp][m][nb][row 16][col 8]; the
+    // buffer alternates between items, so one barrier per item suffices
+    float* rb = red + ((s & 1) * nwarps + warp) * RED;
 #pragma unroll
     for (int m = 0; m < M; ++m)
 #pragma unroll
       for (int nb = 0; nb < NBLK; ++nb) {
-        float* r = red + ((warp * M + m) * NBLK + nb) * 128;
+        float* r = rb + (m * NBLK + nb) * 128;
         *reinterpret_cast<float2*>(r + g * 8 + 2 * t) = make_float2(acc[m][nb][0], acc[m][nb][1]);
         *reinterpret_cast<float2*>(r + (g + 8) * 8 + 2 * t) = make_float2(acc[m][nb][2], acc[m][nb][3]);
       }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < MX_ROWS * it.n; idx += blockDim.x) {
+    const float* rs = red + (s & 1) * nwarps * RED;
+    for (int idx = threadIdx.x; idx < MX_ROWS * n; idx += blockDim.x) {
       const int row = idx & 15, col = idx >> 4, nb = col >> 3, cc = col & 7;
       float v[M];
 #pragma unroll
       for (int m = 0; m < M; ++m) {
         float sum = 0.f;
-        for (int w = 0; w < nwarps; ++w) sum += red[((w * M + m) * NBLK + nb) * 128 + row * 8 + cc];
+        for (int w = 0; w < nwarps; ++w) sum += rs[w * RED + (m * NBLK + nb) * 128 + row * 8 + cc];
         v[m] = sum;
       }
-      const int slot = it.slot0 + col;
+      const int slot = slot0 + col;
       if (MODE == MX_GATEUP) {
-        const int pw = p.act_pow[p.slot_tok[slot]];
+        const int pw = col_pw[s & 1][col];
         const float gg = scalbnf(v[0], -pw), uu = scalbnf(v[M - 1], -pw);
         const float h = __uint_as_float((uint32_t)f32_to_bf16_bits(situf(gg, uu)) << 16);  // bf16 rounding
-        reinterpret_cast<__half*>(p.out)[(size_t)slot * p.R + it.row0 + row] = __float2half_rn(h * 256.0f);
+        reinterpret_cast<__half*>(p.out)[(size_t)slot * p.R + row0 + row] = __float2half_rn(h * 256.0f);
       } else {
-        reinterpret_cast<float*>(p.out)[(size_t)slot * p.R + it.row0 + row] = v[0] * (1.0f / 256.0f);
+        reinterpret_cast<float*>(p.out)[(size_t)slot * p.R + row0 + row] = v[0] * (1.0f / 256.0f);
       }
     }
-    __syncthreads();
   }
   cp_async_wait<0>();
 }
@@ -263,7 +270,7 @@ __global__ void __launch_bounds__(MX_MAX_THREADS) k3_mx_gemv_kernel(MxGemvParams
 // ============================================================================ bf16 GEMV
 constexpr int DN_CHUNK = 64;  // elements per row per stage
 constexpr int DN_WARPS = 8;
-constexpr int DN_STAGE_BYTES = 16 * DN_CHUNK * 2;  // 2048
+constexpr int DN_A_BYTES = 16 * DN_CHUNK * 2;  // 2048: 16 weight rows
 
 enum { DN_PROJ = 0, DN_PLAIN = 1 };
 
@@ -280,29 +287,42 @@ struct DenseParams {
   uint32_t* zmax;   // PROJ: per-token max |z| (f32 bits)
 };
 
+// bytes of one stage: 16 weight rows and NB activation rows of one 64-element chunk
+__host__ __device__ constexpr int dn_stage_bytes(int nblk) { return DN_A_BYTES + 8 * nblk * DN_CHUNK * 2; }
+
 // smem row layout: 16-byte chunk j of row r sits at position j ^ (2 * (r & 3)); with the
 // per-thread 8-byte reads of an m16n8k16 fragment this keeps both half-warps conflict-free
 K3_DEVI uint32_t dn_pos(int r, int j) { return r * 128 + ((j ^ (2 * (r & 3))) << 4); }
 
-template <int STAGES>
-K3_DEVI void dn_issue(const DenseParams& p, const uint16_t* W, int R, int row0, int chunk, int lane, uint32_t stage) {
+template <int NBLK>
+K3_DEVI void dn_issue(const DenseParams& p, const uint16_t* W, int R, int row0, int t0, int n, int chunk, int lane,
+                      uint32_t stage) {
+  const size_t k0 = (size_t)chunk * DN_CHUNK;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int c = lane + 32 * i;
     const int r = c >> 3, j = c & 7;
     const int row = min(row0 + r, R - 1);
-    cp_async16(stage + dn_pos(r, j), W + (size_t)row * p.K + (size_t)chunk * DN_CHUNK + j * 8);
+    cp_async16(stage + dn_pos(r, j), W + (size_t)row * p.K + k0 + j * 8);
+  }
+  // activation rows of the batch (rows past n keep stale data: their columns are never stored)
+#pragma unroll
+  for (int i = 0; i < NBLK * 2; ++i) {
+    const int c = lane + 32 * i;
+    const int r = c >> 3, j = c & 7;
+    if (r < n) cp_async16(stage + DN_A_BYTES + dn_pos(r, j), p.act + (size_t)(t0 + r) * p.K + k0 + j * 8);
   }
 }
 
 template <int EPI, int NBLK, int STAGES>
 __global__ void __launch_bounds__(DN_WARPS * 32) k3_dense_gemv_kernel(DenseParams p) {
   constexpr int NB = 8 * NBLK;
+  constexpr int SB = dn_stage_bytes(NBLK);
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
-  const uint32_t wbase = smem_u32(smem) + warp * STAGES * DN_STAGE_BYTES;
-  float* red = reinterpret_cast<float*>(smem + DN_WARPS * STAGES * DN_STAGE_BYTES);
+  const uint32_t wbase = smem_u32(smem) + warp * STAGES * SB;
+  float* red = reinterpret_cast<float*>(smem + DN_WARPS * STAGES * SB);
 
   const int tiles0 = (p.R0 + 15) / 16, tiles1 = (p.R1 + 15) / 16, tiles = tiles0 + tiles1;
   const int nbatch = (p.T + NB - 1) / NB;
@@ -313,18 +333,40 @@ __global__ void __launch_bounds__(DN_WARPS * 32) k3_dense_gemv_kernel(DenseParam
   const int c0 = warp * cpw;
   const int units = n_mine * cpw;
 
+  auto unit_rows = [&](int u, const uint16_t*& W, int& R, int& row0, int& t0, int& n) {
+    const int i = blockIdx.x + (u / cpw) * gridDim.x;
+    const int tile = i % tiles, bt = i / tiles;
+    const bool m1 = tile >= tiles0;
+    W = m1 ? p.W1 : p.W0;
+    R = m1 ? p.R1 : p.R0;
+    row0 = (m1 ? tile - tiles0 : tile) * 16;
+    t0 = bt * NB;
+    n = min(NB, p.T - t0);
+  };
   auto unit_issue = [&](int u) {
-    const int k = u / cpw, c = u - k * cpw;
-    const int chunk = c0 + c;
+    const int chunk = c0 + u % cpw;
     if (chunk < nchunks) {
-      const int i = blockIdx.x + k * gridDim.x;
-      const int tile = i % tiles;
-      const bool m1 = tile >= tiles0;
-      dn_issue<STAGES>(p, m1 ? p.W1 : p.W0, m1 ? p.R1 : p.R0, (m1 ? tile - tiles0 : tile) * 16, chunk, lane,
-                       wbase + (u % STAGES) * DN_STAGE_BYTES);
+      const uint16_t* W;
+      int R, row0, t0, n;
+      unit_rows(u, W, R, row0, t0, n);
+      dn_issue<NBLK>(p, W, R, row0, t0, n, chunk, lane, wbase + (u % STAGES) * SB);
     }
   };
 
+  // the weights of the first stages do not depend on the previous kernel: pull them
+  // into L2 before waiting for it
+  for (int u = 0; u < STAGES - 1 && u < units; ++u) {
+    const int chunk = c0 + u % cpw;
+    if (chunk < nchunks && lane < 16) {
+      const uint16_t* W;
+      int R, row0, t0, n;
+      unit_rows(u, W, R, row0, t0, n);
+      const uint16_t* a = W + (size_t)min(row0 + lane, R - 1) * p.K + (size_t)chunk * DN_CHUNK;
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a));
+    }
+  }
+  grid_dep_wait();
+  grid_dep_launch();
 #pragma unroll
   for (int s = 0; s < STAGES - 1; ++s) {
     if (s < units) unit_issue(s);
@@ -335,8 +377,8 @@ __global__ void __launch_bounds__(DN_WARPS * 32) k3_dense_gemv_kernel(DenseParam
   for (int u = 0; u < units; ++u) {
     if (u + STAGES - 1 < units) unit_issue(u + STAGES - 1);
     cp_async_commit();
-    const int k = u / cpw, c = u - k * cpw;
-    const int i = blockIdx.x + k * gridDim.x;
+    const int c = u % cpw;
+    const int i = blockIdx.x + (u / cpw) * gridDim.x;
     const int tile = i % tiles, bt = i / tiles;
     const int t0 = bt * NB;
     const int n = min(NB, p.T - t0);
@@ -350,19 +392,17 @@ __global__ void __launch_bounds__(DN_WARPS * 32) k3_dense_gemv_kernel(DenseParam
     __syncwarp();
     const int chunk = c0 + c;
     if (chunk < nchunks) {
-      const uint32_t stage = wbase + (u % STAGES) * DN_STAGE_BYTES;
+      const uint8_t* stp = smem + warp * STAGES * SB + (u % STAGES) * SB;
 #pragma unroll
       for (int s = 0; s < DN_CHUNK / 16; ++s) {
         const int j = 2 * s + (t >> 1);
-        const uint2 alo = lds64(stage + dn_pos(g, j) + (t & 1) * 8);
-        const uint2 ahi = lds64(stage + dn_pos(g + 8, j) + (t & 1) * 8);
+        const uint2 alo = *reinterpret_cast<const uint2*>(stp + dn_pos(g, j) + (t & 1) * 8);
+        const uint2 ahi = *reinterpret_cast<const uint2*>(stp + dn_pos(g + 8, j) + (t & 1) * 8);
         const uint32_t a[4] = {alo.x, ahi.x, alo.y, ahi.y};
 #pragma unroll
         for (int nb = 0; nb < NBLK; ++nb) {
-          if (nb * 8 < n) {
-            const int col = nb * 8 + g;
-            uint2 b = make_uint2(0u, 0u);
-            if (col < n) b = ldg64(p.act + (size_t)(t0 + col) * p.K + (size_t)chunk * DN_CHUNK + 16 * s + 4 * t);
+          if (NBLK == 1 || nb * 8 < n) {
+            const uint2 b = *reinterpret_cast<const uint2*>(stp + DN_A_BYTES + dn_pos(nb * 8 + g, j) + (t & 1) * 8);
             mma_bf16(acc[nb], a, b.x, b.y, acc[nb]);
           }
         }

@@ -12,7 +12,8 @@ namespace k3 {
 // id); every candidate whose biased score lies within `tau` of a neighbour, in a
 // near-tie cluster that reaches the top K + 1, gets its logit recomputed exactly in
 // fp64 from the bf16 inputs; candidates are then ranked on the refined values.
-constexpr int TOPK_WARPS = 4;
+// The ranking compares 64-bit integer images of the (exact) double values: the fp64
+// unit is used only for the rare refinements.
 constexpr int REFINE_EXTRA = 8;
 constexpr int TOPK_MAX_P = 64 + REFINE_EXTRA;
 constexpr int TOPK_MAX_E = 2048;
@@ -31,20 +32,65 @@ struct TopkParams {
   uint32_t* status;
 };
 
-__global__ void __launch_bounds__(TOPK_WARPS * 32) k3_topk_kernel(TopkParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int t = blockIdx.x * TOPK_WARPS + warp;
-  if (t >= p.T) return;
-  float* sb = reinterpret_cast<float*>(smem) + warp * (2 * p.E);  // biased scores (consumed)
-  float* sr = sb + p.E;                                            // raw scores
-  __shared__ float cv[TOPK_WARPS][TOPK_MAX_P];
-  __shared__ float cs[TOPK_WARPS][TOPK_MAX_P];
-  __shared__ int ci[TOPK_WARPS][TOPK_MAX_P];
-  __shared__ double rv[TOPK_WARPS][TOPK_MAX_P];
-  __shared__ double rs[TOPK_WARPS][TOPK_MAX_P];
-  __shared__ int rf[TOPK_WARPS][TOPK_MAX_P];
+struct TopkScratch {         // per warp
+  float cv[TOPK_MAX_P];      // fp32 biased score of candidate
+  float cs[TOPK_MAX_P];      // raw score used for the weight
+  int ci[TOPK_MAX_P];        // expert id
+  int rf[TOPK_MAX_P];        // refine flag
+  long long key[TOPK_MAX_P]; // ranking key
+};
 
+// exact double bit pattern of a float, by integer operations
+K3_DEVI uint64_t f32_as_f64_bits(float f) {
+  const uint32_t b = __float_as_uint(f);
+  const uint64_t sign = (uint64_t)(b >> 31) << 63;
+  uint32_t e = (b >> 23) & 0xFFu, m = b & 0x7FFFFFu;
+  if (e == 0 && m == 0) return sign;
+  if (e == 0xFFu) return sign | 0x7FF0000000000000ull | ((uint64_t)m << 29);
+  int ee = (int)e;
+  if (e == 0) {  // subnormal float: normalise
+    const int sh = __clz(m) - 8;
+    m = (m << sh) & 0x7FFFFFu;
+    ee = 1 - sh;
+  }
+  return sign | ((uint64_t)(ee + 1023 - 127) << 52) | ((uint64_t)m << 29);
+}
+// order-preserving signed integer image of a (non-NaN) double bit pattern
+K3_DEVI long long order_key(uint64_t bits) { return (long long)(bits ^ ((uint64_t)((long long)bits >> 63) >> 1)); }
+
+// sb, sr: per-warp [E] buffers in shared memory
+// Selection: every lane keeps the three best (value desc, id asc) of its experts
+// e = lane + 32 i in registers; a tournament over the lanes' heads (warp argmax by
+// shuffles) picks the next candidate, the winning lane pops its head, and rescans
+// its experts only when its three are used up.
+K3_DEVI bool topk_better(float va, int ia, float vb, int ib) { return va > vb || (va == vb && ia < ib); }
+
+K3_DEVI void topk_lane_top3(const float* sb, int E, int lane, float (&v)[3], int (&id)[3]) {
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    v[k] = -INFINITY;
+    id[k] = 0x7fffffff;
+  }
+  for (int e = lane; e < E; e += 32) {
+    const float x = sb[e];
+    if (x != x) continue;  // taken
+    if (topk_better(x, e, v[2], id[2])) {
+      if (topk_better(x, e, v[1], id[1])) {
+        v[2] = v[1]; id[2] = id[1];
+        if (topk_better(x, e, v[0], id[0])) {
+          v[1] = v[0]; id[1] = id[0];
+          v[0] = x; id[0] = e;
+        } else {
+          v[1] = x; id[1] = e;
+        }
+      } else {
+        v[2] = x; id[2] = e;
+      }
+    }
+  }
+}
+
+K3_DEVI void topk_token(const TopkParams& p, int t, float* sb, float* sr, TopkScratch& S, int lane) {
   // sb: NaN marks an expert already taken; a NaN score ranks last (-inf)
   for (int e = lane; e < p.E; e += 32) {
     const float s = sigmoidf_(p.logits[(size_t)t * p.E + e]);
@@ -54,51 +100,67 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) k3_topk_kernel(TopkParams p) 
   }
   __syncwarp();
   const int P = min(p.E, p.K + REFINE_EXTRA);
+  float hv[3];
+  int hi[3];
+  topk_lane_top3(sb, p.E, lane, hv, hi);
+  int used = 0;  // entries of this lane's top-3 already taken
   for (int k = 0; k < P; ++k) {
-    float best = -INFINITY;
-    int bid = 0x7fffffff;
-    for (int e = lane; e < p.E; e += 32) {
-      const float v = sb[e];
-      if (v != v) continue;
-      if (v > best || (v == best && e < bid)) {
-        best = v;
-        bid = e;
-      }
-    }
+    float best = hv[0];
+    int bid = hi[0];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, best, off);
       const int oi = __shfl_xor_sync(0xffffffffu, bid, off);
-      if (ov > best || (ov == best && oi < bid)) {
+      if (topk_better(ov, oi, best, bid)) {
         best = ov;
         bid = oi;
       }
     }
     if (lane == 0) {
-      cv[warp][k] = best;
-      ci[warp][k] = bid;
-      cs[warp][k] = sr[bid];
+      S.cv[k] = best;
+      S.ci[k] = bid;
+      S.cs[k] = sr[bid];
+    }
+    if (hi[0] == bid) {  // this lane owned the winner: pop it
       sb[bid] = __int_as_float(0x7fc00000);
+      hv[0] = hv[1]; hi[0] = hi[1];
+      hv[1] = hv[2]; hi[1] = hi[2];
+      hv[2] = -INFINITY; hi[2] = 0x7fffffff;
+      if (++used == 3) {
+        topk_lane_top3(sb, p.E, lane, hv, hi);
+        used = 0;
+      }
     }
     __syncwarp();
   }
   // near-tie clusters: consecutive candidates closer than tau are linked; a cluster
   // is refined when it starts at or before position K (it can change the top K or
   // their order)
-  if (lane == 0) {
-    int start = 0;
-    for (int k = 0; k < P; ++k) {
-      const bool linked_prev = k > 0 && (cv[warp][k - 1] - cv[warp][k]) < p.tau;
-      const bool linked_next = k + 1 < P && (cv[warp][k] - cv[warp][k + 1]) < p.tau;
-      if (!linked_prev) start = k;
-      rf[warp][k] = (linked_prev || linked_next) && start <= p.K;
+  __syncwarp();
+  {
+    // lane k handles candidate k (P <= 72: up to three rounds); the start of k's cluster
+    // is the last unlinked position at or before k, found with a warp ballot scan
+    int base_start = 0;  // cluster start carried from the previous round
+    for (int k0 = 0; k0 < P; k0 += 32) {
+      const int k = k0 + lane;
+      const bool in = k < P;
+      const bool linked_prev = in && k > 0 && (S.cv[k - 1] - S.cv[k]) < p.tau;
+      const bool linked_next = in && k + 1 < P && (S.cv[k] - S.cv[k + 1]) < p.tau;
+      const unsigned unl = __ballot_sync(0xffffffffu, in && !linked_prev);  // cluster starts in this round
+      const unsigned le = unl & ((2u << lane) - 1u);
+      const int start = le ? k0 + 31 - __clz(le) : base_start;
+      if (in) {
+        S.rf[k] = (linked_prev || linked_next) && start <= p.K;
+        S.key[k] = order_key(f32_as_f64_bits(S.cv[k]));
+      }
+      base_start = __shfl_sync(0xffffffffu, start, 31);
     }
-    if (P < p.E && rf[warp][P - 1]) flag_status(p.status, K3MOE_DEV_TIE_WINDOW);
   }
   __syncwarp();
+  if (lane == 0 && P < p.E && S.rf[P - 1]) flag_status(p.status, K3MOE_DEV_TIE_WINDOW);
   for (int k = 0; k < P; ++k) {
-    if (!rf[warp][k]) continue;  // warp-uniform
-    const int e = ci[warp][k];
+    if (!S.rf[k]) continue;  // warp-uniform
+    const int e = S.ci[k];
     double acc = 0.0;
     const uint16_t* xr = p.x + (size_t)t * p.H;
     const uint16_t* wrr = p.wr + (size_t)e * p.H;
@@ -108,42 +170,55 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) k3_topk_kernel(TopkParams p) 
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (lane == 0) {
       const double s = 1.0 / (1.0 + exp(-acc));
-      rs[warp][k] = s;
-      rv[warp][k] = s + (double)p.bias[e];
+      S.cs[k] = (float)s;
+      S.key[k] = order_key((uint64_t)__double_as_longlong(s + (double)p.bias[e]));
     }
     __syncwarp();
   }
-  if (lane == 0) {
-    // rank the P candidates on (refined value when refined, else the fp32 value) desc, id asc
-    for (int k = 0; k < P; ++k) {
-      if (!rf[warp][k]) {
-        rv[warp][k] = (double)cv[warp][k];
-        rs[warp][k] = (double)cs[warp][k];
-      }
-    }
-    for (int a = 0; a < p.K; ++a) {
+  // without refinements the tournament order is already the final order
+  bool any_rf = false;
+  for (int k = 0; k < P; ++k) any_rf |= (S.rf[k] != 0);
+  if (lane == 0 && any_rf) {
+    for (int a = 0; a < p.K; ++a) {  // selection sort of the first K by (key desc, id asc)
       int b = a;
-      for (int c = a + 1; c < P; ++c) {
-        const double vc = rv[warp][c], vb = rv[warp][b];
-        if (vc > vb || (vc == vb && ci[warp][c] < ci[warp][b])) b = c;
-      }
+      for (int c = a + 1; c < P; ++c)
+        if (S.key[c] > S.key[b] || (S.key[c] == S.key[b] && S.ci[c] < S.ci[b])) b = c;
       if (b != a) {
-        double tv = rv[warp][a]; rv[warp][a] = rv[warp][b]; rv[warp][b] = tv;
-        double ts = rs[warp][a]; rs[warp][a] = rs[warp][b]; rs[warp][b] = ts;
-        int ti = ci[warp][a]; ci[warp][a] = ci[warp][b]; ci[warp][b] = ti;
+        const long long tk = S.key[a]; S.key[a] = S.key[b]; S.key[b] = tk;
+        const float ts = S.cs[a]; S.cs[a] = S.cs[b]; S.cs[b] = ts;
+        const int ti = S.ci[a]; S.ci[a] = S.ci[b]; S.ci[b] = ti;
       }
     }
+  }
+  __syncwarp();
+  {
+    // the sum runs in k order (as a serial loop would), then lane k writes entry k
     float sum = 0.f;
-    for (int k = 0; k < p.K; ++k) sum += (float)rs[warp][k];
-    for (int k = 0; k < p.K; ++k) {
-      const int id = ci[warp][k];
-      const float wk = (float)rs[warp][k] / sum;
+    for (int k = 0; k < p.K; ++k) sum += S.cs[k];
+    for (int k = lane; k < p.K; k += 32) {
+      const int id = S.ci[k];
+      const float wk = S.cs[k] / sum;
       p.ids[(size_t)t * p.K + k] = id;
       p.w[(size_t)t * p.K + k] = wk;
       if (p.ids_out) p.ids_out[(size_t)t * p.K + k] = id;
       if (p.w_out) p.w_out[(size_t)t * p.K + k] = wk;
     }
   }
+  __syncwarp();
+}
+
+constexpr int TOPK_WARPS = 4;
+
+__global__ void __launch_bounds__(TOPK_WARPS * 32) k3_topk_kernel(TopkParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ TopkScratch S[TOPK_WARPS];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * TOPK_WARPS + warp;
+  if (t >= p.T) return;
+  float* sb = reinterpret_cast<float*>(smem) + warp * (2 * p.E);
+  topk_token(p, t, sb, sb + p.E, S[warp], lane);
 }
 
 // ============================================================================ permutation
@@ -151,13 +226,16 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) k3_topk_kernel(TopkParams p) 
 // expert union with per-expert position lists).  Each warp owns a contiguous range
 // of slots and a private histogram; positions are handed out in slot order inside
 // a warp (warp-synchronous ranking with __match_any_sync) and in warp order across
-// warps, so the result is the stable sort by (expert, t*K + k).
+// warps, so the result is the stable sort by (expert, t*K + k).  The expert kernels'
+// token batches (up to NB tokens of one expert each, with the expert's weight
+// pointers) are written last.
 constexpr int PERM_WARPS = 16;
 
 struct PermParams {
   const int32_t* ids;  // [T*K], or null: every slot routes to fixed_expert
   int fixed_expert;
   int T, K, E, NB;
+  k3moe_experts ex;    // pointer tables (device arrays of E pointers)
   int32_t* counts;     // [E]
   int32_t* offsets;    // [E+1]
   int32_t* slot_of;    // [T*K] sorted slot -> flat index t*K+k
@@ -166,10 +244,12 @@ struct PermParams {
   int32_t* uniq;       // [E]
   int32_t* n_uniq;     // [1]
   int32_t* nb_prefix;  // [E+1] over unique experts: prefix of ceil(count/NB)
+  MxBatch* batches;    // [nb_prefix[n_uniq]] token batches
+  int32_t* n_batches;  // [1]
   uint32_t* status;
 };
 
-// exclusive scan of 4 values per thread over a 512-thread block (values in order
+// exclusive scan of 4 values per thread over a PERM_WARPS-warp block (values in order
 // thread 0 v0..v3, thread 1 v0..v3, ...); returns the block total
 K3_DEVI int block_scan4(int (&v)[4], int* wsum) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -206,9 +286,8 @@ K3_DEVI int block_scan4(int (&v)[4], int* wsum) {
   return total;
 }
 
-__global__ void __launch_bounds__(PERM_WARPS * 32) k3_permute_kernel(PermParams p) {
-  extern __shared__ __align__(16) int32_t hist[];  // [PERM_WARPS][E]
-  __shared__ int wsum[PERM_WARPS + 1];
+// hist: PERM_WARPS * E ints of shared memory; wsum: PERM_WARPS + 1 ints
+K3_DEVI void permute_block(const PermParams& p, int32_t* hist, int* wsum) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n = p.T * p.K;
   const int chunk = (n + PERM_WARPS - 1) / PERM_WARPS;
@@ -265,9 +344,8 @@ __global__ void __launch_bounds__(PERM_WARPS * 32) k3_permute_kernel(PermParams 
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     const int leader = __ffs(peers) - 1;
-    int pos = 0;
     if (valid) {
-      pos = hist[warp * p.E + e] + rank;
+      const int pos = hist[warp * p.E + e] + rank;
       p.slot_of[pos] = i;
       p.slot_tok[pos] = i / p.K;
       p.inv[i] = pos;
@@ -277,31 +355,148 @@ __global__ void __launch_bounds__(PERM_WARPS * 32) k3_permute_kernel(PermParams 
     __syncwarp();
   }
   // unique experts (ascending) and their token-batch prefix
-  int flag[4], nbv[4];
+  int flag[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) flag[q] = cnt[q] > 0 ? 1 : 0;
   const int nu = block_scan4(flag, wsum);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int e = threadIdx.x * 4 + q;
-    nbv[q] = 0;
     if (e < p.E && cnt[q] > 0) p.uniq[flag[q]] = e;
   }
   if (threadIdx.x == 0) *p.n_uniq = nu;
   __syncthreads();
-  // nb over unique experts in order: thread handles unique indices 4*tid .. 4*tid+3
+  int nbv[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int u = threadIdx.x * 4 + q;
     nbv[q] = (u < nu) ? (p.counts[p.uniq[u]] + p.NB - 1) / p.NB : 0;
   }
-  const int nbt = block_scan4(nbv, wsum);
+  int nbx[4] = {nbv[0], nbv[1], nbv[2], nbv[3]};
+  const int nbt = block_scan4(nbx, wsum);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int u = threadIdx.x * 4 + q;
-    if (u < nu) p.nb_prefix[u] = nbv[q];
+    if (u < nu) {
+      p.nb_prefix[u] = nbx[q];
+      if (!p.ex.gate_q) continue;  // permutation only: no expert tables, no batch records
+      const int e = p.uniq[u];
+      const int cntu = p.counts[e], offu = p.offsets[e];
+      const uint8_t* wp[6] = {p.ex.gate_q[e], p.ex.gate_s[e], p.ex.up_q[e], p.ex.up_s[e], p.ex.down_q[e],
+                              p.ex.down_s[e]};
+      for (int b = 0; b < nbv[q]; ++b) {
+        MxBatch* r = p.batches + nbx[q] + b;
+#pragma unroll
+        for (int k = 0; k < 6; ++k) r->w[k] = wp[k];
+        const int s0 = offu + b * p.NB;
+        const int nn = min(p.NB, cntu - b * p.NB);
+        r->slot0 = s0;
+        r->n = nn;
+        for (int j = 0; j < MX_MAX_NB; ++j) r->tok[j] = (j < nn) ? p.slot_tok[s0 + j] : 0;
+        r->pad[0] = r->pad[1] = 0;
+      }
+    }
   }
-  if (threadIdx.x == 0) p.nb_prefix[nu] = nbt;
+  if (threadIdx.x == 0) {
+    p.nb_prefix[nu] = nbt;
+    *p.n_batches = nbt;
+  }
+}
+
+// The same permutation for at most 32 routed slots, by one warp: a bitonic sort of
+// (expert, flat index) pairs across the lanes gives the stable order; runs of equal
+// experts are the unique experts.  counts/offsets are written for the routed experts
+// only (nothing downstream reads the others).
+K3_DEVI void permute_warp(const PermParams& p, int lane) {
+  const int n = p.T * p.K;
+  int e = 0x7fffffff, f = 0x7fffffff;
+  if (lane < n) {
+    e = p.ids ? p.ids[lane] : p.fixed_expert;
+    if (e < 0 || e >= p.E) {
+      flag_status(p.status, K3MOE_DEV_BAD_ID);
+      e = min(max(e, 0), p.E - 1);
+    }
+    f = lane;
+  }
+  // bitonic sort ascending by (e, f)
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const int oe = __shfl_xor_sync(0xffffffffu, e, stride);
+      const int of = __shfl_xor_sync(0xffffffffu, f, stride);
+      const bool up = ((lane & size) == 0);
+      const bool lower = ((lane & stride) == 0);
+      const bool other_less = (oe < e) || (oe == e && of < f);
+      const bool take = (lower == up) ? other_less : !other_less;
+      if (take) {
+        e = oe;
+        f = of;
+      }
+    }
+  }
+  const bool valid = lane < n;
+  const int pe = __shfl_up_sync(0xffffffffu, e, 1);
+  const bool start = valid && (lane == 0 || pe != e);
+  const unsigned starts = __ballot_sync(0xffffffffu, start);
+  const int u = __popc(starts & ((1u << lane) - 1u)) + (start ? 0 : -1);  // run index of this lane
+  const int nu = __popc(starts);
+  // run start and length of this lane's run
+  const unsigned le = starts & ((2u << lane) - 1u);
+  const int run0 = valid ? 31 - __clz(le) : 0;
+  const unsigned after = starts & ~((2u << lane) - 1u);
+  const int run1 = after ? __ffs(after) - 1 : n;
+  if (valid) {
+    p.slot_of[lane] = f;
+    p.slot_tok[lane] = f / p.K;
+    p.inv[f] = lane;
+  }
+  __syncwarp();  // slot_tok is read back below by other lanes
+  // per run: batches of NB tokens
+  const int cnt = run1 - run0;
+  const int nbr = start ? (cnt + p.NB - 1) / p.NB : 0;
+  int pre = nbr;  // inclusive scan over lanes
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, pre, off);
+    if (lane >= off) pre += o;
+  }
+  const int total = __shfl_sync(0xffffffffu, pre, 31);
+  if (start) {
+    p.counts[e] = cnt;
+    p.offsets[e] = run0;
+    p.uniq[u] = e;
+    p.nb_prefix[u] = pre - nbr;
+    if (p.ex.gate_q) {
+      const uint8_t* wp[6] = {p.ex.gate_q[e], p.ex.gate_s[e], p.ex.up_q[e], p.ex.up_s[e], p.ex.down_q[e],
+                              p.ex.down_s[e]};
+      for (int b = 0; b < nbr; ++b) {
+        MxBatch* r = p.batches + (pre - nbr) + b;
+#pragma unroll
+        for (int k = 0; k < 6; ++k) r->w[k] = wp[k];
+        const int s0 = run0 + b * p.NB;
+        const int nn = min(p.NB, cnt - b * p.NB);
+        r->slot0 = s0;
+        r->n = nn;
+        for (int j = 0; j < MX_MAX_NB; ++j) r->tok[j] = (j < nn) ? p.slot_tok[s0 + j] : 0;
+        r->pad[0] = r->pad[1] = 0;
+      }
+    }
+  }
+  if (lane == 0) {
+    *p.n_uniq = nu;
+    p.nb_prefix[nu] = total;
+    *p.n_batches = total;
+    p.offsets[p.E] = n;
+  }
+}
+
+__global__ void __launch_bounds__(PERM_WARPS * 32) k3_permute_kernel(PermParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int wsum[PERM_WARPS + 1];
+  grid_dep_wait();
+  grid_dep_launch();
+  permute_block(p, reinterpret_cast<int32_t*>(smem), wsum);
 }
 
 // ============================================================================ activation prep
@@ -314,24 +509,73 @@ struct Z16Params {
   int32_t* pow2;
 };
 
-__global__ void k3_z16_kernel(Z16Params p) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= p.T) return;
-  const uint16_t* zr = p.z + (size_t)t * p.L;
+// one warp converts one token (L a multiple of 64: 16-byte vectors)
+K3_DEVI void z16_token(const Z16Params& p, int t, int lane) {
+  const uint4* zr = reinterpret_cast<const uint4*>(p.z + (size_t)t * p.L);
+  const int nv = p.L / 8;
   uint32_t mx = 0;
-  for (int c = lane; c < p.L; c += 32) mx = max(mx, (uint32_t)(zr[c] & 0x7FFFu));
+  for (int c = lane; c < nv; c += 32) {
+    const uint4 v = zr[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   int pw = 0;
   if (mx != 0u && mx < 0x7F80u) {
-    const int ex = (int)(mx >> 7);  // biased exponent field of the largest |z|
+    const int ex = (int)(mx >> 7);               // biased exponent field of the largest |z|
     const int E2 = (ex == 0) ? -127 : ex - 127;  // floor(log2) (subnormal: below -126)
     pw = 14 - E2;
   }
   if (lane == 0) p.pow2[t] = pw;
-  __half* o = p.z16 + (size_t)t * p.L;
-  for (int c = lane; c < p.L; c += 32) o[c] = __float2half_rn(scalbnf(bf16_bits_to_f32(zr[c]), pw));
+  uint4* o = reinterpret_cast<uint4*>(p.z16 + (size_t)t * p.L);
+  for (int c = lane; c < nv; c += 32) {
+    const uint4 v = zr[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t r[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 h = __floats2half2_rn(scalbnf(bf16_bits_to_f32(w[k] & 0xFFFFu), pw),
+                                          scalbnf(bf16_bits_to_f32(w[k] >> 16), pw));
+      r[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    o[c] = make_uint4(r[0], r[1], r[2], r[3]);
+  }
+}
+
+__global__ void k3_z16_kernel(Z16Params p) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t < p.T) z16_token(p, t, threadIdx.x & 31);
+}
+
+// ============================================================================ fused route tail
+// For small token counts one CTA runs top-k, the permutation and the activation
+// prep back to back (one launch instead of three).
+constexpr int TAIL_MAX_T = 64;
+
+__global__ void __launch_bounds__(PERM_WARPS * 32) k3_route_tail_kernel(TopkParams tp, PermParams pp, Z16Params zp) {
+  extern __shared__ __align__(128) uint8_t smem[];  // max(PERM_WARPS * 2E floats, PERM_WARPS * E ints)
+  __shared__ TopkScratch S[PERM_WARPS];
+  __shared__ int wsum[PERM_WARPS + 1];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  grid_dep_wait();
+  grid_dep_launch();
+  // top-k of token t on warp t % 16; the activation prep (independent of routing) of
+  // token t on warp (t + 8) % 16, so both run at once
+  for (int t = warp; t < tp.T; t += PERM_WARPS) {
+    float* sb = reinterpret_cast<float*>(smem) + warp * (2 * tp.E);
+    topk_token(tp, t, sb, sb + tp.E, S[warp], lane);
+  }
+  for (int t = (warp + PERM_WARPS / 2) % PERM_WARPS; t < zp.T; t += PERM_WARPS) z16_token(zp, t, lane);
+  __syncthreads();
+  if (pp.T * pp.K <= 32) {
+    if (warp == 0) permute_warp(pp, lane);
+  } else {
+    permute_block(pp, reinterpret_cast<int32_t*>(smem), wsum);
+  }
 }
 
 // ============================================================================ combine + RMSNorm
@@ -344,34 +588,82 @@ struct CombineParams {
   float eps;
   float* y;            // [T, L] f32 combined
   uint16_t* yhat;      // [T, L] bf16
+  float* part;         // [T, COMB_MAX_SPLIT] partial sums of squares
+  uint32_t* count;     // [T] arrival counters (zero on entry; reset by the last CTA)
 };
 
 constexpr int COMB_THREADS = 256;
+constexpr int COMB_MAX_SPLIT = 32;
 
+// grid (T, split): CTA sp of token t combines float4 columns [sp*256, sp*256+256) in k
+// order -- one column per thread, the K expert rows read with independent loads --,
+// writes y and its partial sum of squares; the last CTA of the token to finish adds
+// the partials in split order and writes yhat for the whole row.
 __global__ void __launch_bounds__(COMB_THREADS) k3_combine_norm_kernel(CombineParams p) {
-  extern __shared__ __align__(16) float ybuf[];  // [L]
-  __shared__ float part[COMB_THREADS / 32];
-  const int t = blockIdx.x;
+  __shared__ float wpart[COMB_THREADS / 32];
+  __shared__ const float* rows[64];
+  __shared__ float wk[64];
+  __shared__ int last;
+  __shared__ float r_sh;
+  grid_dep_wait();
+  grid_dep_launch();
+  const int t = blockIdx.x, sp = blockIdx.y, nsplit = gridDim.y;
+  if ((int)threadIdx.x < p.K) {
+    rows[threadIdx.x] = p.o + (size_t)p.inv[(size_t)t * p.K + threadIdx.x] * p.L;
+    wk[threadIdx.x] = p.w[(size_t)t * p.K + threadIdx.x];
+  }
+  __syncthreads();
+  const int c4 = sp * COMB_THREADS + threadIdx.x;
   float ss = 0.f;
-  for (int c = threadIdx.x; c < p.L; c += blockDim.x) {
-    float y = 0.f;
-    for (int k = 0; k < p.K; ++k) {
-      const int slot = p.inv[(size_t)t * p.K + k];
-      y = fmaf(p.w[(size_t)t * p.K + k], p.o[(size_t)slot * p.L + c], y);
+  if (c4 < p.L / 4) {
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < p.K; k0 += 16) {
+      float4 v[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (k0 + q < p.K) v[q] = reinterpret_cast<const float4*>(rows[k0 + q])[c4];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        if (k0 + q < p.K) {
+          const float wq = wk[k0 + q];
+          y.x = fmaf(wq, v[q].x, y.x);
+          y.y = fmaf(wq, v[q].y, y.y);
+          y.z = fmaf(wq, v[q].z, y.z);
+          y.w = fmaf(wq, v[q].w, y.w);
+        }
+      }
     }
-    ybuf[c] = y;
-    ss = fmaf(y, y, ss);
+    reinterpret_cast<float4*>(p.y + (size_t)t * p.L)[c4] = y;
+    ss = fmaf(y.x, y.x, ss);
+    ss = fmaf(y.y, y.y, ss);
+    ss = fmaf(y.z, y.z, ss);
+    ss = fmaf(y.w, y.w, ss);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  if ((threadIdx.x & 31) == 0) wpart[threadIdx.x >> 5] = ss;
   __syncthreads();
-  float tot = 0.f;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += part[w];
-  const float r = 1.0f / sqrtf(tot / (float)p.L + p.eps);
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += wpart[w];
+    p.part[(size_t)t * COMB_MAX_SPLIT + sp] = tot;
+    __threadfence();
+    const uint32_t prev = atomicAdd(p.count + t, 1u);
+    last = (prev == (uint32_t)nsplit - 1u);
+    if (last) p.count[t] = 0;  // ready for the next call
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int q = 0; q < nsplit; ++q) tot += __ldcg(p.part + (size_t)t * COMB_MAX_SPLIT + q);
+    r_sh = 1.0f / sqrtf(tot / (float)p.L + p.eps);
+  }
+  __syncthreads();
+  const float r = r_sh;
   for (int c = threadIdx.x; c < p.L; c += blockDim.x) {
-    const float y = ybuf[c];
-    p.y[(size_t)t * p.L + c] = y;
+    const float y = __ldcg(p.y + (size_t)t * p.L + c);
     p.yhat[(size_t)t * p.L + c] = f32_to_bf16_bits(p.gamma[c] * (y * r));
   }
 }

@@ -1,0 +1,334 @@
+// k3_tc.cuh -- tensor-core (tcgen05 / TMEM / TMA) GEMMs for large token counts.
+//
+// D[M, N] = A[M, K] . B[N, K]^T, both operands K-major bf16, fp32 accumulation in
+// tensor memory.  One CTA per SM, persistent over output tiles of 128 x 256:
+//   warp 0      TMA producer: A and B k-blocks (64 wide, 128-byte swizzle) into a
+//               STAGES-deep shared-memory ring (mbarrier full/empty pairs);
+//   warp 1      allocates 512 TMEM columns (two 256-column accumulators) and issues
+//               tcgen05.mma (M 128, N 256, K 16) from one elected lane; completion
+//               of each k-block frees its stage (tcgen05.commit -> empty), completion
+//               of a tile hands its accumulator to the epilogue;
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, conversion, stores;
+//               the accumulator is released for the tile after next.
+// Every mbarrier wait is bounded (about 2 s of clock); a wait that runs out sets
+// K3MOE_DEV_TIMEOUT in the status word and all roles drain and exit (TMEM is freed).
+#pragma once
+
+#include <cuda.h>
+
+#include "k3_common.cuh"
+
+namespace k3 {
+
+// ---------------------------------------------------------------------------- PTX wrappers
+K3_DEVI void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+K3_DEVI void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+K3_DEVI void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+K3_DEVI bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity.  Returns false when the CTA's
+// abort flag is set (by this or another thread) or the wait exceeds ~2^32 cycles.
+K3_DEVI bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > (1ll << 32)) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+K3_DEVI void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+          dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+K3_DEVI void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];\n" ::"l"(map) : "memory");
+}
+
+K3_DEVI void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+K3_DEVI void tmem_relinquish() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory"); }
+K3_DEVI void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+K3_DEVI void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+K3_DEVI void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+// make generic-proxy shared-memory writes visible to the async proxy (tensor core reads)
+K3_DEVI void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+K3_DEVI void fence_barrier_init() { asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory"); }
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16 in, fp32 accumulate)
+K3_DEVI void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.u32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive on `bar` once all previously issued tcgen05.mma of this thread have completed
+K3_DEVI void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns (this warp's lane quarter)
+K3_DEVI void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+K3_DEVI void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, rows of 128 bytes with the 128-byte
+// swizzle, 8-row groups 1024 bytes apart (the layout TMA writes with SWIZZLE_128B and a
+// 64 x bf16 inner box).  Advancing along K inside the 128-byte row adds to the address.
+K3_DEVI uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                            // leading-dimension byte offset (unused here)
+  d |= (uint64_t)(1024 >> 4) << 32;                  // stride-dimension byte offset
+  d |= (uint64_t)1 << 46;                            // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                            // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------- dense GEMM
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4;
+constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
+constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;  // 32 KB
+constexpr int TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;
+constexpr int TC_THREADS = 192;
+constexpr int TC_SMEM = 1024 + TC_STAGES * TC_STAGE_BYTES + 256;  // alignment slack, ring, barriers
+
+enum { TC_PROJ = 0, TC_PLAIN = 1 };
+
+struct TcDenseParams {
+  int M;       // rows of A (tokens)
+  int N0, N1;  // output features from B map 0 and from B map 1 (0: none)
+  int K;       // reduction length (multiple of 64)
+  float* out0;     // PROJ: logits [M, N0]; PLAIN: out [M, N0]
+  uint16_t* out1;  // PROJ: z [M, N1] bf16
+  uint32_t* zmax;  // PROJ: per-row max |z| (f32 bits)
+  uint32_t* status;
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    k3_tc_dense_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
+                       const __grid_constant__ CUtensorMap mapB1, TcDenseParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1024-byte alignment
+  const uint32_t bars = base + TC_STAGES * TC_STAGE_BYTES;
+  auto full_bar = [&](int s) { return bars + 8 * s; };
+  auto empty_bar = [&](int s) { return bars + 8 * (TC_STAGES + s); };
+  auto tfull_bar = [&](int b) { return bars + 8 * (2 * TC_STAGES + b); };
+  auto tempty_bar = [&](int b) { return bars + 8 * (2 * TC_STAGES + 2 + b); };
+  const uint32_t done_bar = bars + 8 * (2 * TC_STAGES + 4);
+  volatile int* abort_flag = &abort_sh;
+
+  const int m_tiles = (p.M + TC_BM - 1) / TC_BM;
+  const int n_t0 = (p.N0 + TC_BN - 1) / TC_BN, n_t1 = (p.N1 + TC_BN - 1) / TC_BN;
+  const int tiles = m_tiles * (n_t0 + n_t1);
+  const int kblocks = p.K / TC_BK;
+
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    for (int s = 0; s < TC_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 128);
+    }
+    mbar_init(done_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB0);
+    if (p.N1 > 0) tma_prefetch_desc(&mapB1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  grid_dep_wait();
+  grid_dep_launch();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int it = 0;
+      for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x) {
+        const int tm = tile % m_tiles, tn = tile / m_tiles;
+        const bool b1 = tn >= n_t0;
+        const CUtensorMap* mb = b1 ? &mapB1 : &mapB0;
+        const int n0 = (b1 ? tn - n_t0 : tn) * TC_BN;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % TC_STAGES;
+          if (!mbar_wait(empty_bar(s), ((it / TC_STAGES) & 1) ^ 1, abort_flag)) break;
+          const uint32_t st = base + s * TC_STAGE_BYTES;
+          mbar_expect_tx(full_bar(s), TC_STAGE_BYTES);
+          tma_load_2d(st, &mapA, kb * TC_BK, tm * TC_BM, full_bar(s));
+          tma_load_2d(st + TC_A_BYTES, mb, kb * TC_BK, n0, full_bar(s));
+        }
+      }
+      // drain: every issued stage must have landed before the CTA exits
+      for (int s = 0; s < TC_STAGES; ++s) {
+        const int last = it - 1 - ((it - 1 - s) % TC_STAGES + TC_STAGES) % TC_STAGES;  // last issue into stage s
+        if (last >= 0 && last < it) {
+          volatile int never = 0;
+          mbar_wait(full_bar(s), (last / TC_STAGES) & 1, &never);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(TC_BM, TC_BN);
+      int it = 0, lt = 0;
+      for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x, ++lt) {
+        const int b = lt & 1;
+        if (!mbar_wait(tempty_bar(b), ((lt >> 1) & 1) ^ 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + b * TC_BN;
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % TC_STAGES;
+          if (!mbar_wait(full_bar(s), (it / TC_STAGES) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = base + s * TC_STAGE_BYTES;
+#pragma unroll
+          for (int k = 0; k < TC_BK / 16; ++k)
+            tc_mma(d, sdesc_sw128(st + k * 32), sdesc_sw128(st + TC_A_BYTES + k * 32), idesc, (kb | k) != 0);
+          tc_commit(empty_bar(s));
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(b));
+      }
+      // all MMAs issued by this thread have completed once done_bar flips
+      tc_commit(done_bar);
+      volatile int never = 0;
+      mbar_wait(done_bar, 0, &never);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
+      const int b = lt & 1;
+      if (!mbar_wait(tfull_bar(b), (lt >> 1) & 1, abort_flag)) break;
+      tc_fence_after();
+      const int tm = tile % m_tiles, tn = tile / m_tiles;
+      const bool b1 = tn >= n_t0;
+      const int n0 = (b1 ? tn - n_t0 : tn) * TC_BN;
+      const int row = tm * TC_BM + q * 32 + lane;
+      const int N = b1 ? p.N1 : p.N0;
+      float zm = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < TC_BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + b * TC_BN + c * 32, r);
+        tmem_ld_wait();
+        const int col0 = n0 + c * 32;
+        if (row < p.M && col0 < N) {
+          if (EPI == TC_PROJ && b1) {
+            uint16_t* dst = p.out1 + (size_t)row * p.N1 + col0;
+            if (col0 + 32 <= N) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const uint16_t lo = f32_to_bf16_bits(__uint_as_float(r[8 * v + 2 * e]));
+                  const uint16_t hi = f32_to_bf16_bits(__uint_as_float(r[8 * v + 2 * e + 1]));
+                  zm = fmaxf(zm, fmaxf(fabsf(bf16_bits_to_f32(lo)), fabsf(bf16_bits_to_f32(hi))));
+                  w[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+                }
+                reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            } else {
+              for (int e = 0; e < 32 && col0 + e < N; ++e) {
+                const uint16_t h = f32_to_bf16_bits(__uint_as_float(r[e]));
+                zm = fmaxf(zm, fabsf(bf16_bits_to_f32(h)));
+                dst[e] = h;
+              }
+            }
+          } else {
+            float* dst = p.out0 + (size_t)row * p.N0 + col0;
+            if (col0 + 32 <= N && (p.N0 % 4) == 0) {
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                reinterpret_cast<float4*>(dst)[v] =
+                    make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]), __uint_as_float(r[4 * v + 2]),
+                                __uint_as_float(r[4 * v + 3]));
+            } else {
+              for (int e = 0; e < 32 && col0 + e < N; ++e) dst[e] = __uint_as_float(r[e]);
+            }
+          }
+        }
+      }
+      if (EPI == TC_PROJ && b1 && row < p.M) atomicMax(p.zmax + row, __float_as_uint(zm));
+      tc_fence_before();
+      mbar_arrive(tempty_bar(b));
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) flag_status(p.status, K3MOE_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace k3

@@ -3,10 +3,12 @@
 // no synchronisation (except k3moe_device_status, which is documented to sync).
 #include <atomic>
 #include <cstring>
+#include <utility>
 
 #include "k3_common.cuh"
 #include "k3_gemv.cuh"
 #include "k3_route.cuh"
+#include "k3_tc.cuh"
 
 namespace {
 
@@ -18,8 +20,8 @@ constexpr int kMaxDevices = 64;
 size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t status, logits, ids, w, zmax, zpow, counts, offsets, slot_of, slot_tok, inv, uniq, n_uniq, nb_prefix, z,
-      z16, h16, o, y, yhat, total;
+  size_t status, logits, ids, w, zmax, zpow, counts, offsets, slot_of, slot_tok, inv, uniq, n_uniq, nb_prefix,
+      n_batches, batches, z, z16, h16, o, y, yhat, cpart, ccount, total;
 };
 
 WsLayout ws_layout(const k3moe_dims& d, int T) {
@@ -47,12 +49,17 @@ WsLayout ws_layout(const k3moe_dims& d, int T) {
   L.uniq = take(E * 4);
   L.n_uniq = take(4);
   L.nb_prefix = take((E + 1) * 4);
+  L.n_batches = take(4);
+  // token batches of at least 8 tokens: at most ceil(slots / 8) + min(E, slots) of them
+  L.batches = take((slots / 8 + 1 + (E < slots ? E : slots)) * sizeof(MxBatch));
   L.z = take(Tz * Lt * 2);
   L.z16 = take(Tz * Lt * 2);
   L.h16 = take(slots * I * 2);
   L.o = take(slots * Lt * 4);
   L.y = take(Tz * Lt * 4);
   L.yhat = take(Tz * Lt * 2);
+  L.cpart = take(Tz * COMB_MAX_SPLIT * 4);
+  L.ccount = take(Tz * 4);
   L.total = off;
   return L;
 }
@@ -113,76 +120,181 @@ bool set_smem(int dev, int bytes) {
   return true;
 }
 
-// ---------------------------------------------------------------------------- launch helpers
-constexpr int kDnStages = 5;
-constexpr int kMxStages = 3;
+// ---------------------------------------------------------------------------- TMA descriptors
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load(std::memory_order_acquire);
+  if (!f) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    f = reinterpret_cast<EncodeTiledFn>(p);
+    fn.store(f, std::memory_order_release);
+  }
+  return f;
+}
 
-int dn_smem(int nblk) { return DN_WARPS * kDnStages * DN_STAGE_BYTES + DN_WARPS * nblk * 128 * 4; }
+// row-major [rows, cols] bf16 matrix, boxes of box_rows x 64 with the 128-byte swizzle
+bool map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------- launch helpers
+// Launch with programmatic stream serialization: the kernel may start while its
+// predecessor finishes; it waits (griddepcontrol.wait) before reading its inputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, int smem, cudaStream_t st, bool pdl,
+                   Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// ring depth per activation batch width: two CTAs per SM for NBLK 1 and 2
+constexpr int dn_stages(int nblk) { return nblk == 1 ? 4 : 3; }
+constexpr int dn_smem(int nblk) {
+  return DN_WARPS * dn_stages(nblk) * dn_stage_bytes(nblk) + DN_WARPS * nblk * 128 * 4;
+}
 
 template <int EPI, int NBLK>
-cudaError_t launch_dense_t(const DenseParams& p, int dev, int sms, cudaStream_t st) {
-  auto kern = k3_dense_gemv_kernel<EPI, NBLK, kDnStages>;
-  const int smem = dn_smem(NBLK);
-  if (!set_smem<k3_dense_gemv_kernel<EPI, NBLK, kDnStages>>(dev, smem)) return cudaErrorInvalidValue;
+cudaError_t launch_dense_t(const DenseParams& p, int dev, int sms, cudaStream_t st, bool pdl) {
+  constexpr int STAGES = dn_stages(NBLK);
+  constexpr int smem = dn_smem(NBLK);
+  if (!set_smem<k3_dense_gemv_kernel<EPI, NBLK, STAGES>>(dev, smem)) return cudaErrorInvalidValue;
+  const int per_sm = (2 * smem + 2048 <= 228 * 1024) ? 2 : 1;
   const int tiles = (p.R0 + 15) / 16 + (p.R1 + 15) / 16;
   const int total = tiles * ((p.T + 8 * NBLK - 1) / (8 * NBLK));
-  const int grid = total < 2 * sms ? total : 2 * sms;
+  const int grid = total < per_sm * sms ? total : per_sm * sms;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, DN_WARPS * 32, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch(k3_dense_gemv_kernel<EPI, NBLK, STAGES>, dim3(grid), dim3(DN_WARPS * 32), smem, st, pdl, p);
 }
 
 template <int EPI>
-cudaError_t launch_dense(const DenseParams& p, int dev, int sms, cudaStream_t st) {
-  if (p.T <= 8) return launch_dense_t<EPI, 1>(p, dev, sms, st);
-  if (p.T <= 16) return launch_dense_t<EPI, 2>(p, dev, sms, st);
-  return launch_dense_t<EPI, 4>(p, dev, sms, st);
+cudaError_t launch_dense(const DenseParams& p, int dev, int sms, cudaStream_t st, bool pdl) {
+  if (p.T <= 8) return launch_dense_t<EPI, 1>(p, dev, sms, st, pdl);
+  if (p.T <= 16) return launch_dense_t<EPI, 2>(p, dev, sms, st, pdl);
+  return launch_dense_t<EPI, 4>(p, dev, sms, st, pdl);
 }
 
 int mx_nblk(int T) { return T <= 8 ? 1 : 2; }
 
-template <int MODE, int NBLK>
-cudaError_t launch_mx_t(const MxGemvParams& p, int dev, int sms, cudaStream_t st) {
-  constexpr int M = MODE == MX_GATEUP ? 2 : 1;
-  auto kern = k3_mx_gemv_kernel<MODE, NBLK, kMxStages>;
-  const int warps = (p.K / 32 + MX_GPW - 1) / MX_GPW;
-  const int smem = warps * MxLayout<M, kMxStages>::WARP_BYTES + warps * M * NBLK * 128 * 4;
-  if (warps * 32 > MX_MAX_THREADS || smem > 227 * 1024) return cudaErrorInvalidValue;
-  if (!set_smem<k3_mx_gemv_kernel<MODE, NBLK, kMxStages>>(dev, smem)) return cudaErrorInvalidValue;
+// token count from which the dense projections run on the tcgen05 GEMM
+constexpr int kTcMinT = 256;
+
+// D[M, N0 (+N1)] = A[M, K] . [B0; B1]^T on tcgen05 (A, B bf16 row-major)
+template <int EPI>
+cudaError_t launch_tc_dense(const uint16_t* A, int M, int K, const uint16_t* B0, int N0, const uint16_t* B1, int N1,
+                            TcDenseParams p, int dev, int sms, cudaStream_t st, bool pdl) {
+  CUtensorMap ma, mb0, mb1;
+  if (!map_bf16(&ma, A, M, K, TC_BM) || !map_bf16(&mb0, B0, N0, K, TC_BN)) return cudaErrorInvalidValue;
+  if (N1 > 0) {
+    if (!map_bf16(&mb1, B1, N1, K, TC_BN)) return cudaErrorInvalidValue;
+  } else {
+    mb1 = mb0;
+  }
+  p.M = M;
+  p.N0 = N0;
+  p.N1 = N1;
+  p.K = K;
+  if (!set_smem<k3_tc_dense_kernel<EPI>>(dev, TC_SMEM)) return cudaErrorInvalidValue;
+  const int tiles = ((M + TC_BM - 1) / TC_BM) * ((N0 + TC_BN - 1) / TC_BN + (N1 + TC_BN - 1) / TC_BN);
+  const int grid = tiles < sms ? tiles : sms;
+  return launch(k3_tc_dense_kernel<EPI>, dim3(grid), dim3(TC_THREADS), TC_SMEM, st, pdl, ma, mb0, mb1, p);
+}
+
+template <int MODE, int NBLK, int STAGES, bool FULL>
+cudaError_t launch_mx_s(const MxGemvParams& p, int dev, int sms, cudaStream_t st, bool pdl, int smem, int warps) {
+  constexpr bool PRE = MODE == MX_DOWN;  // its batches were written two kernels earlier
+  if (!set_smem<k3_mx_gemv_kernel<MODE, NBLK, STAGES, PRE, FULL>>(dev, smem)) return cudaErrorInvalidValue;
   const int per_sm = (2 * smem + 2048 <= 228 * 1024) ? 2 : 1;
-  kern<<<sms * per_sm, warps * 32, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch(k3_mx_gemv_kernel<MODE, NBLK, STAGES, PRE, FULL>, dim3(sms * per_sm), dim3(warps * 32), smem, st, pdl,
+                p);
+}
+
+template <int MODE, int NBLK>
+cudaError_t launch_mx_t(const MxGemvParams& p, int dev, int sms, cudaStream_t st, bool pdl) {
+  constexpr int M = MODE == MX_GATEUP ? 2 : 1;
+  const int warps = (p.K / 32 + MX_GPW - 1) / MX_GPW;
+  if (warps * 32 > MX_MAX_THREADS) return cudaErrorInvalidValue;
+  const int red = 2 * warps * M * NBLK * 128 * 4;  // double-buffered partial sums
+  const bool full = p.K % 256 == 0;
+  const int smem3 = warps * MxLayout<M, 3>::WARP_BYTES + red;
+  const int smem2 = warps * MxLayout<M, 2>::WARP_BYTES + red;
+  if (smem3 <= 227 * 1024)
+    return full ? launch_mx_s<MODE, NBLK, 3, true>(p, dev, sms, st, pdl, smem3, warps)
+                : launch_mx_s<MODE, NBLK, 3, false>(p, dev, sms, st, pdl, smem3, warps);
+  if (smem2 <= 227 * 1024)
+    return full ? launch_mx_s<MODE, NBLK, 2, true>(p, dev, sms, st, pdl, smem2, warps)
+                : launch_mx_s<MODE, NBLK, 2, false>(p, dev, sms, st, pdl, smem2, warps);
+  return cudaErrorInvalidValue;
 }
 
 template <int MODE>
-cudaError_t launch_mx(const MxGemvParams& p, int nblk, int dev, int sms, cudaStream_t st) {
-  return nblk == 1 ? launch_mx_t<MODE, 1>(p, dev, sms, st) : launch_mx_t<MODE, 2>(p, dev, sms, st);
+cudaError_t launch_mx(const MxGemvParams& p, int nblk, int dev, int sms, cudaStream_t st, bool pdl) {
+  return nblk == 1 ? launch_mx_t<MODE, 1>(p, dev, sms, st, pdl) : launch_mx_t<MODE, 2>(p, dev, sms, st, pdl);
 }
 
-cudaError_t launch_topk(const TopkParams& p, int dev, cudaStream_t st) {
+cudaError_t launch_topk(const TopkParams& p, int dev, cudaStream_t st, bool pdl) {
   const int smem = TOPK_WARPS * 2 * p.E * 4;
   if (!set_smem<k3_topk_kernel>(dev, smem)) return cudaErrorInvalidValue;
-  k3_topk_kernel<<<(p.T + TOPK_WARPS - 1) / TOPK_WARPS, TOPK_WARPS * 32, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch(k3_topk_kernel, dim3((p.T + TOPK_WARPS - 1) / TOPK_WARPS), dim3(TOPK_WARPS * 32), smem, st, pdl, p);
 }
 
-cudaError_t launch_permute(const PermParams& p, int dev, cudaStream_t st) {
+cudaError_t launch_permute(const PermParams& p, int dev, cudaStream_t st, bool pdl) {
   const int smem = PERM_WARPS * p.E * 4;
   if (!set_smem<k3_permute_kernel>(dev, smem)) return cudaErrorInvalidValue;
-  k3_permute_kernel<<<1, PERM_WARPS * 32, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch(k3_permute_kernel, dim3(1), dim3(PERM_WARPS * 32), smem, st, pdl, p);
 }
 
-cudaError_t launch_z16(const Z16Params& p, cudaStream_t st) {
-  k3_z16_kernel<<<(p.T + 7) / 8, 256, 0, st>>>(p);
-  return cudaGetLastError();
+cudaError_t launch_z16(const Z16Params& p, cudaStream_t st, bool pdl) {
+  return launch(k3_z16_kernel, dim3((p.T + 7) / 8), dim3(256), 0, st, pdl, p);
 }
 
-cudaError_t launch_combine(const CombineParams& p, int dev, cudaStream_t st) {
-  const int smem = p.L * 4;
-  if (!set_smem<k3_combine_norm_kernel>(dev, smem)) return cudaErrorInvalidValue;
-  k3_combine_norm_kernel<<<p.T, COMB_THREADS, smem, st>>>(p);
-  return cudaGetLastError();
+int tail_smem(int E) { return PERM_WARPS * 2 * E * 4; }
+bool tail_fits(int T, int E) {
+  return T <= TAIL_MAX_T && tail_smem(E) + (int)(PERM_WARPS * sizeof(TopkScratch)) + 1024 <= 227 * 1024;
+}
+
+// top-k, permutation and activation prep: one fused launch for small T, else three
+cudaError_t launch_route_tail(const TopkParams& tp, const PermParams& pp, const Z16Params& zp, int dev, cudaStream_t st,
+                              bool pdl) {
+  if (tail_fits(tp.T, tp.E)) {
+    const int smem = tail_smem(tp.E);
+    if (!set_smem<k3_route_tail_kernel>(dev, smem)) return cudaErrorInvalidValue;
+    return launch(k3_route_tail_kernel, dim3(1), dim3(PERM_WARPS * 32), smem, st, pdl, tp, pp, zp);
+  }
+  cudaError_t e = launch_topk(tp, dev, st, pdl);
+  if (e == cudaSuccess) e = launch_permute(pp, dev, st, pdl);
+  if (e == cudaSuccess) e = launch_z16(zp, st, pdl);
+  return e;
+}
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
+  const int split = (p.L / 4 + COMB_THREADS - 1) / COMB_THREADS;  // one float4 column per thread
+  if (split > COMB_MAX_SPLIT) return cudaErrorInvalidValue;
+  return launch(k3_combine_norm_kernel, dim3(p.T, split), dim3(COMB_THREADS), 0, st, pdl, p);
 }
 
 // records event i of a caller-supplied list (no-op when absent)
@@ -197,8 +309,11 @@ cudaError_t mark(void* const* events, int n_events, int i, cudaStream_t s) {
   } while (0)
 
 PermParams perm_params(const k3moe_dims& d, int T, int K, const int32_t* ids, int fixed, int NB, void* ws,
-                       const WsLayout& L) {
+                       const WsLayout& L, const k3moe_experts* ex) {
   PermParams pp{};
+  if (ex) pp.ex = *ex;
+  pp.batches = at<MxBatch>(ws, L.batches);
+  pp.n_batches = at<int32_t>(ws, L.n_batches);
   pp.ids = ids;
   pp.fixed_expert = fixed;
   pp.T = T;
@@ -217,23 +332,18 @@ PermParams perm_params(const k3moe_dims& d, int T, int K, const int32_t* ids, in
   return pp;
 }
 
-MxGemvParams mx_params(const k3moe_dims& d, const WsLayout& L, void* ws, const k3moe_experts& ex, int mode,
-                       const __half* act, void* out) {
+MxGemvParams mx_params(const k3moe_dims& d, const WsLayout& L, void* ws, int mode, const __half* act, void* out) {
   MxGemvParams p{};
   if (mode == MX_GATEUP) {
-    p.q0 = ex.gate_q; p.s0 = ex.gate_s; p.q1 = ex.up_q; p.s1 = ex.up_s;
-    p.R = d.inter; p.K = d.latent;
+    p.R = d.inter;
+    p.K = d.latent;
     p.act_pow = at<int32_t>(ws, L.zpow);
   } else {
-    p.q0 = ex.down_q; p.s0 = ex.down_s; p.q1 = ex.down_q; p.s1 = ex.down_s;
-    p.R = d.latent; p.K = d.inter;
+    p.R = d.latent;
+    p.K = d.inter;
   }
-  p.uniq = at<int32_t>(ws, L.uniq);
-  p.n_uniq = at<int32_t>(ws, L.n_uniq);
-  p.counts = at<int32_t>(ws, L.counts);
-  p.offsets = at<int32_t>(ws, L.offsets);
-  p.nb_prefix = at<int32_t>(ws, L.nb_prefix);
-  p.slot_tok = at<int32_t>(ws, L.slot_tok);
+  p.batches = at<MxBatch>(ws, L.batches);
+  p.n_batches = at<int32_t>(ws, L.n_batches);
   p.act = act;
   p.out = out;
   return p;
@@ -267,15 +377,22 @@ k3moe_status k3moe_route(const k3moe_dims* dims, int32_t T, const uint16_t* x, c
   if ((st = check_device(&dev, &sms)) != K3MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   K3_TRY(cudaMemsetAsync(at<void>(ws, L.status), 0, 256, s));
-  DenseParams dp{};
-  dp.W0 = wr; dp.R0 = d.n_experts; dp.W1 = nullptr; dp.R1 = 0; dp.K = d.hidden; dp.act = x; dp.T = T;
-  dp.out0 = at<float>(ws, L.logits);
-  K3_TRY(launch_dense<DN_PROJ>(dp, dev, sms, s));
+  if (T >= kTcMinT) {
+    TcDenseParams tcp{};
+    tcp.out0 = at<float>(ws, L.logits);
+    tcp.status = at<uint32_t>(ws, L.status);
+    K3_TRY(launch_tc_dense<TC_PLAIN>(x, T, d.hidden, wr, d.n_experts, nullptr, 0, tcp, dev, sms, s, false));
+  } else {
+    DenseParams dp{};
+    dp.W0 = wr; dp.R0 = d.n_experts; dp.W1 = nullptr; dp.R1 = 0; dp.K = d.hidden; dp.act = x; dp.T = T;
+    dp.out0 = at<float>(ws, L.logits);
+    K3_TRY(launch_dense<DN_PROJ>(dp, dev, sms, s, false));
+  }
   TopkParams tp{};
   tp.logits = at<float>(ws, L.logits); tp.bias = bias; tp.x = x; tp.wr = wr;
   tp.T = T; tp.E = d.n_experts; tp.K = d.top_k; tp.H = d.hidden; tp.tau = kTieTau;
   tp.ids = ids; tp.w = w; tp.status = at<uint32_t>(ws, L.status);
-  K3_TRY(launch_topk(tp, dev, s));
+  K3_TRY(launch_topk(tp, dev, s, true));
   return K3MOE_OK;
 }
 
@@ -301,49 +418,62 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   uint32_t* status = at<uint32_t>(ws, L.status);
 
   if (n_events < 0 || (n_events > 0 && !events)) return K3MOE_ERR_ARG;
+  const bool pdl = n_events == 0;  // phase events between kernels would serialise them anyway
   K3_TRY(mark(events, n_events, 0, s));
   K3_TRY(cudaMemsetAsync(status, 0, 256, s));
   K3_TRY(cudaMemsetAsync(at<void>(ws, L.zmax), 0, (size_t)T * 4, s));
+  K3_TRY(cudaMemsetAsync(at<void>(ws, L.ccount), 0, (size_t)T * 4, s));
   // router logits and latent down in one weight-streaming pass over x
-  DenseParams dp{};
-  dp.W0 = wr; dp.R0 = d.n_experts; dp.W1 = w_down; dp.R1 = d.latent; dp.K = d.hidden; dp.act = x; dp.T = T;
-  dp.out0 = at<float>(ws, L.logits); dp.out1 = at<uint16_t>(ws, L.z); dp.zmax = at<uint32_t>(ws, L.zmax);
-  K3_TRY(launch_dense<DN_PROJ>(dp, dev, sms, s));
+  if (T >= kTcMinT) {
+    TcDenseParams tcp{};
+    tcp.out0 = at<float>(ws, L.logits); tcp.out1 = at<uint16_t>(ws, L.z); tcp.zmax = at<uint32_t>(ws, L.zmax);
+    tcp.status = status;
+    K3_TRY(launch_tc_dense<TC_PROJ>(x, T, d.hidden, wr, d.n_experts, w_down, d.latent, tcp, dev, sms, s, false));
+  } else {
+    DenseParams dp{};
+    dp.W0 = wr; dp.R0 = d.n_experts; dp.W1 = w_down; dp.R1 = d.latent; dp.K = d.hidden; dp.act = x; dp.T = T;
+    dp.out0 = at<float>(ws, L.logits); dp.out1 = at<uint16_t>(ws, L.z); dp.zmax = at<uint32_t>(ws, L.zmax);
+    K3_TRY(launch_dense<DN_PROJ>(dp, dev, sms, s, false));
+  }
   K3_TRY(mark(events, n_events, 1, s));
-  // top-k with fp64 near-tie refinement
+  // top-k with fp64 near-tie refinement, chunk expert union, z -> f16 operand
   TopkParams tp{};
   tp.logits = at<float>(ws, L.logits); tp.bias = bias; tp.x = x; tp.wr = wr;
   tp.T = T; tp.E = d.n_experts; tp.K = d.top_k; tp.H = d.hidden; tp.tau = kTieTau;
   tp.ids = at<int32_t>(ws, L.ids); tp.w = at<float>(ws, L.w); tp.ids_out = ids_out; tp.w_out = w_out;
   tp.status = status;
-  K3_TRY(launch_topk(tp, dev, s));
-  K3_TRY(mark(events, n_events, 2, s));
-  // chunk expert union
   const int nblk = mx_nblk(T);
-  K3_TRY(launch_permute(perm_params(d, T, d.top_k, at<int32_t>(ws, L.ids), 0, 8 * nblk, ws, L), dev, s));
-  K3_TRY(mark(events, n_events, 3, s));
-  // z -> f16 operand
-  Z16Params zp{at<uint16_t>(ws, L.z), T, d.latent, at<__half>(ws, L.z16), at<int32_t>(ws, L.zpow)};
-  K3_TRY(launch_z16(zp, s));
-  K3_TRY(mark(events, n_events, 4, s));
+  const PermParams pp = perm_params(d, T, d.top_k, at<int32_t>(ws, L.ids), 0, 8 * nblk, ws, L, experts);
+  const Z16Params zp{at<uint16_t>(ws, L.z), T, d.latent, at<__half>(ws, L.z16), at<int32_t>(ws, L.zpow)};
+  K3_TRY(launch_route_tail(tp, pp, zp, dev, s, pdl));
+  K3_TRY(mark(events, n_events, 2, s));
   // experts
-  const k3moe_experts ex = *experts;
-  K3_TRY(launch_mx<MX_GATEUP>(mx_params(d, L, ws, ex, MX_GATEUP, at<__half>(ws, L.z16), at<void>(ws, L.h16)), nblk,
-                              dev, sms, s));
-  K3_TRY(mark(events, n_events, 5, s));
-  K3_TRY(launch_mx<MX_DOWN>(mx_params(d, L, ws, ex, MX_DOWN, at<__half>(ws, L.h16), at<void>(ws, L.o)), nblk, dev,
-                            sms, s));
-  K3_TRY(mark(events, n_events, 6, s));
+  K3_TRY(launch_mx<MX_GATEUP>(mx_params(d, L, ws, MX_GATEUP, at<__half>(ws, L.z16), at<void>(ws, L.h16)), nblk, dev,
+                              sms, s, pdl));
+  K3_TRY(mark(events, n_events, 3, s));
+  K3_TRY(launch_mx<MX_DOWN>(mx_params(d, L, ws, MX_DOWN, at<__half>(ws, L.h16), at<void>(ws, L.o)), nblk, dev, sms, s,
+                            pdl));
+  K3_TRY(mark(events, n_events, 4, s));
   // combine + RMSNorm
-  CombineParams cp{at<float>(ws, L.o), at<int32_t>(ws, L.inv), at<float>(ws, L.w), norm_w, T, d.top_k, d.latent,
-                   d.rms_eps, at<float>(ws, L.y), at<uint16_t>(ws, L.yhat)};
-  K3_TRY(launch_combine(cp, dev, s));
-  K3_TRY(mark(events, n_events, 7, s));
+  CombineParams cp{at<float>(ws, L.o),     at<int32_t>(ws, L.inv),  at<float>(ws, L.w),
+                   norm_w,                 T,                       d.top_k,
+                   d.latent,               d.rms_eps,               at<float>(ws, L.y),
+                   at<uint16_t>(ws, L.yhat), at<float>(ws, L.cpart), at<uint32_t>(ws, L.ccount)};
+  K3_TRY(launch_combine(cp, s, pdl));
+  K3_TRY(mark(events, n_events, 5, s));
   // latent up
-  DenseParams up{};
-  up.W0 = w_up; up.R0 = d.hidden; up.K = d.latent; up.act = at<uint16_t>(ws, L.yhat); up.T = T; up.out0 = out;
-  K3_TRY(launch_dense<DN_PLAIN>(up, dev, sms, s));
-  K3_TRY(mark(events, n_events, 8, s));
+  if (T >= kTcMinT) {
+    TcDenseParams tcp{};
+    tcp.out0 = out;
+    tcp.status = status;
+    K3_TRY(launch_tc_dense<TC_PLAIN>(at<uint16_t>(ws, L.yhat), T, d.latent, w_up, d.hidden, nullptr, 0, tcp, dev, sms,
+                                     s, pdl));
+  } else {
+    DenseParams up{};
+    up.W0 = w_up; up.R0 = d.hidden; up.K = d.latent; up.act = at<uint16_t>(ws, L.yhat); up.T = T; up.out0 = out;
+    K3_TRY(launch_dense<DN_PLAIN>(up, dev, sms, s, pdl));
+  }
+  K3_TRY(mark(events, n_events, 6, s));
   return K3MOE_OK;
 }
 
@@ -371,14 +501,13 @@ k3moe_status k3moe_expert_forward(const k3moe_dims* dims, int32_t T, const uint1
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   K3_TRY(cudaMemsetAsync(at<void>(ws, L.status), 0, 256, s));
   const int nblk = mx_nblk(T);
-  K3_TRY(launch_permute(perm_params(d, T, 1, nullptr, expert, 8 * nblk, ws, L), dev, s));
+  K3_TRY(launch_permute(perm_params(d, T, 1, nullptr, expert, 8 * nblk, ws, L, experts), dev, s, false));
   Z16Params zp{z, T, d.latent, at<__half>(ws, L.z16), at<int32_t>(ws, L.zpow)};
-  K3_TRY(launch_z16(zp, s));
-  const k3moe_experts ex = *experts;
-  K3_TRY(launch_mx<MX_GATEUP>(mx_params(d, L, ws, ex, MX_GATEUP, at<__half>(ws, L.z16), at<void>(ws, L.h16)), nblk,
-                              dev, sms, s));
+  K3_TRY(launch_z16(zp, s, true));
+  K3_TRY(launch_mx<MX_GATEUP>(mx_params(d, L, ws, MX_GATEUP, at<__half>(ws, L.z16), at<void>(ws, L.h16)), nblk, dev,
+                              sms, s, true));
   // one expert: sorted slots are the tokens in order, so the down output lands in `out` directly
-  K3_TRY(launch_mx<MX_DOWN>(mx_params(d, L, ws, ex, MX_DOWN, at<__half>(ws, L.h16), out), nblk, dev, sms, s));
+  K3_TRY(launch_mx<MX_DOWN>(mx_params(d, L, ws, MX_DOWN, at<__half>(ws, L.h16), out), nblk, dev, sms, s, true));
   return K3MOE_OK;
 }
 
@@ -414,13 +543,13 @@ k3moe_status k3moe_permute(const k3moe_dims* dims, int32_t T, const int32_t* ids
   if ((st = check_device(&dev, &sms)) != K3MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   K3_TRY(cudaMemsetAsync(at<void>(ws, L.status), 0, 256, s));
-  PermParams pp = perm_params(d, T, d.top_k, ids, 0, 8, ws, L);
+  PermParams pp = perm_params(d, T, d.top_k, ids, 0, 8, ws, L, nullptr);
   pp.counts = counts;
   pp.offsets = offsets;
   pp.slot_of = slot_of;
   pp.uniq = uniq;
   pp.n_uniq = n_uniq;
-  K3_TRY(launch_permute(pp, dev, s));
+  K3_TRY(launch_permute(pp, dev, s, false));
   return K3MOE_OK;
 }
 

@@ -247,9 +247,39 @@ def test_forward_chunk(k3, decode):
     print(f"chunk rel-L2 {r:.3e}, unique experts {len(np.unique(ids))}")
 
 
-def test_forward_prefill_sampled(k3):
+@pytest.fixture(scope="module")
+def prefill(k3):
+    L = Layer(k3, C.PREFILL)
+    yield L
+    del L
+    torch.cuda.empty_cache()
+
+
+def test_forward_tensor_core_path_ragged_tokens(k3, prefill):
+    """300 tokens: the projections run on the tcgen05 GEMM with a ragged last M tile."""
+    cfg = C.PREFILL.with_tokens(300, x_seed=11)
+    L = prefill.with_tokens(k3, cfg)
+    got, ids, w, ws = L.forward(k3)
+    assert k3.device_status(ws) == 0
+    rids, rw, _, _ = oracle_route(cfg)
+    assert np.array_equal(ids, rids)
+    assert np.allclose(w, rw, rtol=0, atol=2e-6)
+    # z (bf16, the latent-down GEMM output) against the oracle's spec rounding for all tokens
+    zp = k3.workspace_view(L.d, cfg.T, ws, 0)
+    off = zp - ws.data_ptr()
+    z = ws[off: off + cfg.T * cfg.latent * 2].view(torch.bfloat16).view(cfg.T, cfg.latent).float().cpu().numpy()
+    W = C.layer_weights(cfg)
+    zref = oracle.latent_down(oracle_dims(cfg), C.layer_x(cfg), W["wd"], True)
+    assert rel_l2(z, zref) < 1e-3
+    assert np.mean(z != zref) < 1e-2  # only rounding-boundary flips (tensor-core fp32 accumulation)
+    rows = [0, 127, 128, 255, 256, 299]
+    ref = oracle_forward(cfg, token_rows=rows)
+    assert rel_l2(got[rows], ref["out"]) <= REL_L2_BAR
+
+
+def test_forward_prefill_sampled(k3, prefill):
     cfg = C.PREFILL
-    L = Layer(k3, cfg)
+    L = prefill
     got, ids, w, ws = L.forward(k3)
     assert k3.device_status(ws) == 0
     rids, rw, _, _ = oracle_route(cfg)
@@ -257,10 +287,8 @@ def test_forward_prefill_sampled(k3):
     rows = [0, 1, 2047, 4095] + list(np.random.default_rng(5).choice(4096, 4, replace=False))
     ref = oracle_forward(cfg, token_rows=rows)
     assert np.array_equal(ids[rows], ref["ids"])
-    for j, t in enumerate(rows):
-        r = rel_l2(got[t], ref["out"][j])
-        assert r <= REL_L2_BAR, (t, r)
+    r = rel_l2(got[rows], ref["out"])
+    assert r <= REL_L2_BAR, r
+    print(f"prefill sampled rel-L2 {r:.3e}")
     counts = np.bincount(ids.ravel(), minlength=cfg.n_experts)
     assert counts.min() > 0  # every expert is used at zero bias
-    del L
-    torch.cuda.empty_cache()
