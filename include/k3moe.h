@@ -74,6 +74,9 @@ typedef enum {
                                      exact ranking for that token */
 #define K3MOE_DEV_TIMEOUT 0x2u    /* a device-side bounded wait ran out; outputs are invalid */
 #define K3MOE_DEV_BAD_ID 0x4u     /* an expert id outside [0, E) reached the permutation */
+#define K3MOE_DEV_SCALE_RANGE 0x8u /* the tensor-core expert path (T >= 256) met a scale byte
+                                      outside 105..142, where its f16 weight decode is not
+                                      exact; the affected outputs are approximate */
 
 /* The six vendor tensors of every expert, as DEVICE arrays of n_experts DEVICE
  * pointers (the pointer tables themselves live in device memory):

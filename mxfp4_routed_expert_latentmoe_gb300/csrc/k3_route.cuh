@@ -551,6 +551,23 @@ __global__ void k3_z16_kernel(Z16Params p) {
   if (t < p.T) z16_token(p, t, threadIdx.x & 31);
 }
 
+// ============================================================================ slot-order activation rows
+// act16_perm[s] = z16[slot_tok[s]] and slot_pow[s] = pow2[slot_tok[s]] for every routed
+// slot (the B operand rows of the tensor-core expert GEMM, one expert's tokens contiguous)
+__global__ void k3_gather_rows_kernel(const __half* z16, const int32_t* pow2, const int32_t* slot_tok, int slots, int L,
+                                      __half* out, int32_t* slot_pow) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int per = L / 8;  // 16-byte chunks per row
+  const size_t total = (size_t)slots * per;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int s = (int)(i / per), c = (int)(i - (size_t)s * per);
+    const int t = __ldg(slot_tok + s);
+    reinterpret_cast<uint4*>(out + (size_t)s * L)[c] = __ldg(reinterpret_cast<const uint4*>(z16 + (size_t)t * L) + c);
+    if (c == 0) slot_pow[s] = __ldg(pow2 + t);
+  }
+}
+
 // ============================================================================ fused route tail
 // For small token counts one CTA runs top-k, the permutation and the activation
 // prep back to back (one launch instead of three).

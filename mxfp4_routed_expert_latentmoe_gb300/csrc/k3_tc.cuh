@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int lt = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
       const int b = lt & 1;
-      if (!mbar_wait(tfull_bar(b), (lt >> 1) & 1, abort_flag)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(b), (lt >> 1) & 1, abort_flag))) break;
       tc_fence_after();
       const int tm = tile % m_tiles, tn = tile / m_tiles;
       const bool b1 = tn >= n_t0;
@@ -322,6 +322,282 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc_fence_before();
       mbar_arrive(tempty_bar(b));
     }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) flag_status(p.status, K3MOE_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace k3
+
+namespace k3 {
+
+// ---------------------------------------------------------------------------- grouped MXFP4 GEMM
+// Per token batch (up to 128 tokens of one expert) and 128-row tile of the expert's
+// weight matrix:  D[rows, tokens] = W[rows, K] . Act[tokens, K]^T  with
+//   A = W decoded in shared memory by producer warps from the vendor MXFP4 bytes:
+//       cvt.rn.f16x2.e2m1x2 gives the exact E2M1 values in f16 and one f16x2 multiply
+//       applies the power-of-two scale; exact for scale bytes 105..142 (the value set
+//       e2m1 * 2^k, k in [-23, 15]); other scale bytes set K3MOE_DEV_SCALE_RANGE;
+//   B = the batch's activation rows in slot order (f16, exactly prescaled by a power
+//       of two per token) loaded by TMA;
+//   fp32 accumulation in TMEM (kind::f16, M 128, N = tokens rounded up to 16).
+// GATEUP: two matrices (gate rows, up rows) share B; the epilogue applies SiTU-GLU,
+// rounds h to bf16 and stores it (x 2^8, f16) in slot order.  DOWN: one matrix; the
+// epilogue stores o (fp32) in slot order.
+constexpr int TM_ROWS = 128;       // weight rows per tile (MMA M)
+constexpr int TM_NB = 128;         // tokens per batch (MMA N <= 128)
+constexpr int TM_BK = 64;          // k-block
+constexpr int TM_PRODUCERS = 8;    // decode warps
+constexpr int TM_THREADS = (6 + TM_PRODUCERS) * 32;
+constexpr int TM_A_BYTES = TM_ROWS * TM_BK * 2;  // 16 KB per matrix
+constexpr int TM_B_BYTES = TM_NB * TM_BK * 2;    // 16 KB
+
+template <int MODE>
+struct TmLayout {
+  static constexpr int M = (MODE == 0) ? 2 : 1;
+  static constexpr int STAGE = M * TM_A_BYTES + TM_B_BYTES;
+  static constexpr int STAGES = (MODE == 0) ? 4 : 6;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + 512;
+};
+
+struct TcMoeParams {
+  const MxBatch* batches;    // token batches of up to 128 tokens (one expert each)
+  const int32_t* n_batches;
+  int R;                     // rows per matrix (I for gate/up, L for down)
+  int K;                     // reduction length (L or I)
+  const int32_t* slot_pow;   // GATEUP: per-slot exponent p of its activation row (act = value * 2^p)
+  void* out;                 // GATEUP: h16 [slots, R]; DOWN: o f32 [slots, R]
+  uint32_t* status;
+};
+
+// E8M0 scale byte -> f16x2 of 2^(s-127) in both halves (0 when not representable);
+// *bad is set when the byte is outside the exact range 105..142
+K3_DEVI uint32_t ue8m0_to_f16x2(uint32_t s, bool& bad) {
+  uint32_t h;
+  if (s >= 113u && s <= 142u) h = (s - 112u) << 10;  // normal f16
+  else if (s >= 103u && s < 113u) h = 1u << (s - 103u);  // subnormal f16
+  else h = 0u;
+  bad |= (s < 105u || s > 142u);
+  return h | (h << 16);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_constant__ CUtensorMap mapB,
+                                                                  TcMoeParams p) {
+  using Lay = TmLayout<MODE>;
+  constexpr int M = Lay::M, S = Lay::STAGES;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bars = base + S * Lay::STAGE;
+  auto fullA = [&](int s) { return bars + 8 * s; };
+  auto fullB = [&](int s) { return bars + 8 * (S + s); };
+  auto empty = [&](int s) { return bars + 8 * (2 * S + s); };
+  auto tfull = [&](int b) { return bars + 8 * (3 * S + b); };
+  auto tempty = [&](int b) { return bars + 8 * (3 * S + 2 + b); };
+  const uint32_t done_bar = bars + 8 * (3 * S + 4);
+  volatile int* abort_flag = &abort_sh;
+
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(fullA(s), TM_PRODUCERS);
+      mbar_init(fullB(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull(b), 1);
+      mbar_init(tempty(b), 128);
+    }
+    mbar_init(done_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&mapB);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  grid_dep_wait();
+  grid_dep_launch();
+
+  const int mtiles = p.R / TM_ROWS;
+  const int tiles = mtiles * (*p.n_batches);
+  const int kblocks = p.K / TM_BK;
+  constexpr int WOFF = (MODE == 0) ? 0 : 4;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (B)
+    if (lane == 0) {
+      int it = 0;
+      for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x) {
+        const int slot0 = p.batches[tile / mtiles].slot0;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % S;
+          if (!mbar_wait(empty(s), ((it / S) & 1) ^ 1, abort_flag)) break;
+          mbar_expect_tx(fullB(s), TM_B_BYTES);
+          tma_load_2d(base + s * Lay::STAGE + M * TM_A_BYTES, &mapB, kb * TM_BK, slot0, fullB(s));
+        }
+      }
+      for (int s = 0; s < S; ++s) {  // drain issued loads
+        const int last = it - 1 - ((it - 1 - s) % S + S) % S;
+        if (last >= 0 && last < it) {
+          volatile int never = 0;
+          mbar_wait(fullB(s), (last / S) & 1, &never);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int it = 0, lt = 0;
+      for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x, ++lt) {
+        const int n = p.batches[tile / mtiles].n;
+        const int N = (n + 15) & ~15;
+        const uint32_t idesc = (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(TM_ROWS >> 4) << 24);  // f16 x f16 -> f32
+        const int b = lt & 1;
+        if (!mbar_wait(tempty(b), ((lt >> 1) & 1) ^ 1, abort_flag)) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % S;
+          if (!mbar_wait(fullA(s), (it / S) & 1, abort_flag) || !mbar_wait(fullB(s), (it / S) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = base + s * Lay::STAGE;
+#pragma unroll
+          for (int k = 0; k < TM_BK / 16; ++k) {
+#pragma unroll
+            for (int m = 0; m < M; ++m)
+              tc_mma(tmem + b * 256 + m * 128, sdesc_sw128(st + m * TM_A_BYTES + k * 32),
+                     sdesc_sw128(st + M * TM_A_BYTES + k * 32), idesc, (kb | k) != 0);
+          }
+          tc_commit(empty(s));
+        }
+        if (!ok) break;
+        tc_commit(tfull(b));
+      }
+      tc_commit(done_bar);
+      volatile int never = 0;
+      mbar_wait(done_bar, 0, &never);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
+      const int b = lt & 1;
+      // warp-uniform outcome: the tcgen05.ld below must be executed by all 32 lanes
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull(b), (lt >> 1) & 1, abort_flag))) break;
+      tc_fence_after();
+      const MxBatch* rec = p.batches + tile / mtiles;
+      const int slot0 = rec->slot0, n = rec->n;
+      const int row = (tile % mtiles) * TM_ROWS + q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c * 32 < n; ++c) {
+        uint32_t r0[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + b * 256 + c * 32, r0);
+        if (MODE == 0) {
+          uint32_t r1[32];
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + b * 256 + 128 + c * 32, r1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = c * 32 + j;
+            if (col < n) {
+              const int pw = __ldg(p.slot_pow + slot0 + col);
+              const float gg = scalbnf(__uint_as_float(r0[j]), -pw), uu = scalbnf(__uint_as_float(r1[j]), -pw);
+              const float h = __uint_as_float((uint32_t)f32_to_bf16_bits(situf(gg, uu)) << 16);  // bf16 rounding
+              reinterpret_cast<__half*>(p.out)[(size_t)(slot0 + col) * p.R + row] = __float2half_rn(h * 256.0f);
+            }
+          }
+        } else {
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = c * 32 + j;
+            if (col < n)
+              reinterpret_cast<float*>(p.out)[(size_t)(slot0 + col) * p.R + row] = __uint_as_float(r0[j]) * (1.0f / 256.0f);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty(b));
+    }
+  } else {
+    // ------------------------------------------------------------ decode producers (warps 6..13)
+    const int pt = threadIdx.x - 6 * 32;  // 0..255
+    // GATEUP: thread = (matrix, row), 64 elements per k-block; DOWN: thread = (row, group), 32 elements
+    const int m = (MODE == 0) ? (pt >> 7) : 0;
+    const int r = pt & 127;
+    const int g0 = (MODE == 0) ? 0 : (pt >> 7);  // first group handled
+    constexpr int NG = (MODE == 0) ? 2 : 1;      // groups per thread per k-block
+    const size_t qrow = (size_t)p.K / 2, srow = (size_t)p.K / 32;
+    bool bad = false;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x) {
+      const MxBatch* rec = p.batches + tile / mtiles;
+      const uint8_t* q = rec->w[WOFF + 2 * m];
+      const uint8_t* sc = rec->w[WOFF + 2 * m + 1];
+      const size_t row = (size_t)(tile % mtiles) * TM_ROWS + r;
+      const uint8_t* qr = q + row * qrow + g0 * 16;
+      const uint8_t* sr = sc + row * srow + g0;
+      // register double buffer: the next k-block's bytes are loaded while this one decodes
+      uint4 nq[NG];
+      uint32_t ns;
+#pragma unroll
+      for (int g = 0; g < NG; ++g) nq[g] = __ldg(reinterpret_cast<const uint4*>(qr) + g);
+      ns = (NG == 2) ? __ldg(reinterpret_cast<const uint16_t*>(sr)) : __ldg(sr);
+      for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        uint4 cq[NG];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) cq[g] = nq[g];
+        const uint32_t cs = ns;
+        if (kb + 1 < kblocks) {
+#pragma unroll
+          for (int g = 0; g < NG; ++g) nq[g] = __ldg(reinterpret_cast<const uint4*>(qr + (kb + 1) * 32) + g);
+          ns = (NG == 2) ? __ldg(reinterpret_cast<const uint16_t*>(sr + (kb + 1) * 2)) : __ldg(sr + (kb + 1) * 2);
+          if (kb + 8 < kblocks && (kb & 3) == 0) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(qr + (kb + 8) * 32));
+        }
+        const int s = it % S;
+        if (!mbar_wait(empty(s), ((it / S) & 1) ^ 1, abort_flag)) break;
+        uint8_t* arow = base_ptr + s * Lay::STAGE + m * TM_A_BYTES + r * 128;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          const uint32_t sc2 = ue8m0_to_f16x2((cs >> (8 * g)) & 0xFFu, bad);
+          const uint32_t w4[4] = {cq[g].x, cq[g].y, cq[g].z, cq[g].w};
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {  // 16-byte output chunk: 8 elements = 4 packed bytes
+            uint32_t h[4];
+            e2m1x8_to_f16x8(w4[cc], h);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h[e]), *reinterpret_cast<const __half2*>(&sc2));
+              h[e] = *reinterpret_cast<uint32_t*>(&v);
+            }
+            const int chunk = (g0 + g) * 4 + cc;  // 16-byte chunk of the 128-byte row
+            *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(fullA(s));
+      }
+    }
+    if (bad) flag_status(p.status, K3MOE_DEV_SCALE_RANGE);
   }
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) flag_status(p.status, K3MOE_DEV_TIMEOUT);

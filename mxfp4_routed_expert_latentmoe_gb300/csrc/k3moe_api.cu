@@ -21,7 +21,7 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 struct WsLayout {
   size_t status, logits, ids, w, zmax, zpow, counts, offsets, slot_of, slot_tok, inv, uniq, n_uniq, nb_prefix,
-      n_batches, batches, z, z16, h16, o, y, yhat, cpart, ccount, total;
+      n_batches, batches, z, z16, h16, o, y, yhat, cpart, ccount, z16p, spow, total;
 };
 
 WsLayout ws_layout(const k3moe_dims& d, int T) {
@@ -60,6 +60,10 @@ WsLayout ws_layout(const k3moe_dims& d, int T) {
   L.yhat = take(Tz * Lt * 2);
   L.cpart = take(Tz * COMB_MAX_SPLIT * 4);
   L.ccount = take(Tz * 4);
+  // slot-order activation rows for the tensor-core expert path (large T only)
+  const bool tc = T >= 256;
+  L.z16p = take(tc ? slots * Lt * 2 : 0);
+  L.spow = take(tc ? slots * 4 : 0);
   L.total = off;
   return L;
 }
@@ -200,8 +204,32 @@ cudaError_t launch_dense(const DenseParams& p, int dev, int sms, cudaStream_t st
 
 int mx_nblk(int T) { return T <= 8 ? 1 : 2; }
 
-// token count from which the dense projections run on the tcgen05 GEMM
+// token count from which the projections and experts run on the tcgen05 GEMMs
+// (must match the workspace layout's choice)
 constexpr int kTcMinT = 256;
+
+// row-major [rows, cols] f16 matrix, boxes of box_rows x 64 with the 128-byte swizzle
+bool map_f16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// grouped MXFP4 expert GEMM on tcgen05; act [slots, K] f16 in slot order
+template <int MODE>
+cudaError_t launch_tc_moe(const __half* act, int slots, TcMoeParams p, int dev, int sms, cudaStream_t st, bool pdl) {
+  CUtensorMap mb;
+  if (!map_f16(&mb, act, slots, p.K, TM_NB)) return cudaErrorInvalidValue;
+  constexpr int smem = TmLayout<MODE>::SMEM;
+  if (!set_smem<k3_tc_moe_kernel<MODE>>(dev, smem)) return cudaErrorInvalidValue;
+  return launch(k3_tc_moe_kernel<MODE>, dim3(sms), dim3(TM_THREADS), smem, st, pdl, mb, p);
+}
 
 // D[M, N0 (+N1)] = A[M, K] . [B0; B1]^T on tcgen05 (A, B bf16 row-major)
 template <int EPI>
@@ -442,17 +470,36 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   tp.T = T; tp.E = d.n_experts; tp.K = d.top_k; tp.H = d.hidden; tp.tau = kTieTau;
   tp.ids = at<int32_t>(ws, L.ids); tp.w = at<float>(ws, L.w); tp.ids_out = ids_out; tp.w_out = w_out;
   tp.status = status;
+  const bool tc = T >= kTcMinT;
   const int nblk = mx_nblk(T);
-  const PermParams pp = perm_params(d, T, d.top_k, at<int32_t>(ws, L.ids), 0, 8 * nblk, ws, L, experts);
+  const int NB = tc ? TM_NB : 8 * nblk;  // tokens per expert batch
+  const PermParams pp = perm_params(d, T, d.top_k, at<int32_t>(ws, L.ids), 0, NB, ws, L, experts);
   const Z16Params zp{at<uint16_t>(ws, L.z), T, d.latent, at<__half>(ws, L.z16), at<int32_t>(ws, L.zpow)};
   K3_TRY(launch_route_tail(tp, pp, zp, dev, s, pdl));
   K3_TRY(mark(events, n_events, 2, s));
   // experts
-  K3_TRY(launch_mx<MX_GATEUP>(mx_params(d, L, ws, MX_GATEUP, at<__half>(ws, L.z16), at<void>(ws, L.h16)), nblk, dev,
+  const int slots = T * d.top_k;
+  if (tc) {
+    const int per = d.latent / 8;
+    const int gblocks = (int)(((size_t)slots * per + 255) / 256 < (size_t)sms * 8 ? ((size_t)slots * per + 255) / 256
+                                                                                     : (size_t)sms * 8);
+    K3_TRY(launch(k3_gather_rows_kernel, dim3(gblocks), dim3(256), 0, s, pdl, (const __half*)at<__half>(ws, L.z16),
+                  (const int32_t*)at<int32_t>(ws, L.zpow), (const int32_t*)at<int32_t>(ws, L.slot_tok), slots,
+                  (int)d.latent, at<__half>(ws, L.z16p), at<int32_t>(ws, L.spow)));
+    TcMoeParams gp{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.inter, d.latent,
+                   at<int32_t>(ws, L.spow), at<void>(ws, L.h16), status};
+    K3_TRY(launch_tc_moe<0>(at<__half>(ws, L.z16p), slots, gp, dev, sms, s, pdl));
+    K3_TRY(mark(events, n_events, 3, s));
+    TcMoeParams dp2{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.latent, d.inter, nullptr,
+                    at<void>(ws, L.o), status};
+    K3_TRY(launch_tc_moe<1>(at<__half>(ws, L.h16), slots, dp2, dev, sms, s, pdl));
+  } else {
+    K3_TRY(launch_mx<MX_GATEUP>(mx_params(d, L, ws, MX_GATEUP, at<__half>(ws, L.z16), at<void>(ws, L.h16)), nblk,
+                                dev, sms, s, pdl));
+    K3_TRY(mark(events, n_events, 3, s));
+    K3_TRY(launch_mx<MX_DOWN>(mx_params(d, L, ws, MX_DOWN, at<__half>(ws, L.h16), at<void>(ws, L.o)), nblk, dev,
                               sms, s, pdl));
-  K3_TRY(mark(events, n_events, 3, s));
-  K3_TRY(launch_mx<MX_DOWN>(mx_params(d, L, ws, MX_DOWN, at<__half>(ws, L.h16), at<void>(ws, L.o)), nblk, dev, sms, s,
-                            pdl));
+  }
   K3_TRY(mark(events, n_events, 4, s));
   // combine + RMSNorm
   CombineParams cp{at<float>(ws, L.o),     at<int32_t>(ws, L.inv),  at<float>(ws, L.w),
