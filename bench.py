@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-graph", action="store_true", help="launch the forward eagerly instead of replaying a graph")
     ap.add_argument("--n-experts", type=int, default=None,
                     help="profiling case: a smaller expert pool with the same per-expert shapes and top-k")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="profiling case: this many tokens instead of the workload's")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -450,6 +452,8 @@ def main():
     if a.n_experts:
         import dataclasses
         cfg = dataclasses.replace(cfg, n_experts=a.n_experts, name=cfg.name)
+    if a.tokens:
+        cfg = cfg.with_tokens(a.tokens, x_seed=cfg.x_seed)
     if a.impl == "reference":
         run_reference(a, cfg, rank, world)
         return

@@ -43,6 +43,22 @@ K3_DEVI bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// As mbar_try_wait, but a thread whose phase is still open is suspended until the
+// phase completes or about `ns` nanoseconds pass (so waiting warps leave the issue
+// slots to the warps doing work).
+K3_DEVI bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait for the phase with the given parity.  Returns false when the CTA's
 // abort flag is set (by this or another thread) or the wait exceeds ~2^32 cycles.
 K3_DEVI bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -51,7 +67,7 @@ K3_DEVI bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) 
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait_sleep(bar, parity, 10000u)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > (1ll << 32)) {
       *abort_flag = 1;
@@ -336,36 +352,48 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 namespace k3 {
 
 // ---------------------------------------------------------------------------- grouped MXFP4 GEMM
-// Per token batch (up to 128 tokens of one expert) and 128-row tile of the expert's
+// Per token batch (up to TM_NB tokens of one expert) and 128-row tile of the expert's
 // weight matrix:  D[rows, tokens] = W[rows, K] . Act[tokens, K]^T  with
-//   A = W decoded in shared memory by producer warps from the vendor MXFP4 bytes:
+//   A = W decoded by producer warps from the vendor MXFP4 bytes into TENSOR MEMORY
+//       (tcgen05.st; row i in lane i, two f16 per 32-bit column, K along columns):
 //       cvt.rn.f16x2.e2m1x2 gives the exact E2M1 values in f16 and one f16x2 multiply
 //       applies the power-of-two scale; exact for scale bytes 105..142 (the value set
 //       e2m1 * 2^k, k in [-23, 15]); other scale bytes set K3MOE_DEV_SCALE_RANGE;
 //   B = the batch's activation rows in slot order (f16, exactly prescaled by a power
-//       of two per token) loaded by TMA;
+//       of two per token) loaded by TMA into shared memory (128-byte swizzle);
 //   fp32 accumulation in TMEM (kind::f16, M 128, N = tokens rounded up to 16).
+// Keeping A out of shared memory leaves shared-memory bandwidth to B and the raw bytes
+// (with A in shared memory the decoded tile is written and then read again by the
+// tensor core, which made the kernel shared-memory bound at these small N).
 // GATEUP: two matrices (gate rows, up rows) share B; the epilogue applies SiTU-GLU,
 // rounds h to bf16 and stores it (x 2^8, f16) in slot order.  DOWN: one matrix; the
 // epilogue stores o (fp32) in slot order.
 constexpr int TM_ROWS = 128;       // weight rows per tile (MMA M)
-constexpr int TM_NB = 128;         // tokens per batch (MMA N <= 128)
+constexpr int TM_NB = 96;          // tokens per batch (MMA N <= 96): bounded by TMEM columns
 constexpr int TM_BK = 64;          // k-block
 constexpr int TM_PRODUCERS = 8;    // decode warps
 constexpr int TM_THREADS = (6 + TM_PRODUCERS) * 32;
-constexpr int TM_A_BYTES = TM_ROWS * TM_BK * 2;  // 16 KB per matrix
-constexpr int TM_B_BYTES = TM_NB * TM_BK * 2;    // 16 KB
+constexpr int TM_B_BYTES = TM_NB * TM_BK * 2;  // 12 KB
+constexpr int TM_CHUNK_KB = 4;     // k-blocks per raw chunk: 128 bytes (one cache line) of every row
 
 template <int MODE>
 struct TmLayout {
   static constexpr int M = (MODE == 0) ? 2 : 1;
-  static constexpr int STAGE = M * TM_A_BYTES + TM_B_BYTES;
-  static constexpr int STAGES = (MODE == 0) ? 4 : 6;
-  static constexpr int SMEM = 1024 + STAGES * STAGE + 512;
+  static constexpr int MROWS = M * TM_ROWS;             // weight rows per tile over all matrices
+  // TMEM columns: accumulators (2 buffers) then the A stages (32 columns per matrix per stage)
+  static constexpr int ACC = (MODE == 0) ? 2 * TM_NB : 128;  // per buffer; GATEUP: gate, then up at +TM_NB
+  static constexpr int SA = (MODE == 0) ? 2 : 4;             // A stages
+  static constexpr int A_COL0 = 2 * ACC;
+  static_assert(A_COL0 + SA * M * 32 <= 512, "TMEM columns");
+  static constexpr int SB = 4;                               // B stages (shared memory)
+  static constexpr int RC = 3;                               // raw chunks in flight
+  static constexpr int RAW_SLOT = MROWS * 128;
+  static constexpr int SC_SLOT = MROWS * 8;
+  static constexpr int SMEM = 1024 + SB * TM_B_BYTES + RC * (RAW_SLOT + SC_SLOT) + 512;
 };
 
 struct TcMoeParams {
-  const MxBatch* batches;    // token batches of up to 128 tokens (one expert each)
+  const MxBatch* batches;    // token batches of up to TM_NB tokens (one expert each)
   const int32_t* n_batches;
   int R;                     // rows per matrix (I for gate/up, L for down)
   int K;                     // reduction length (L or I)
@@ -385,33 +413,113 @@ K3_DEVI uint32_t ue8m0_to_f16x2(uint32_t s, bool& bad) {
   return h | (h << 16);
 }
 
+// bulk prefetch of `bytes` contiguous global bytes into L2 (16-byte aligned, multiple of 16)
+K3_DEVI void l2_prefetch_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// 2^e as f32 for e in [-126, 127]
+K3_DEVI float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// e^x - 1 to a few ulp without cancellation near 0: the Taylor series through x^9 for
+// |x| < 1/2 (truncation below 1e-9 relative), expf(x) - 1 elsewhere.
+K3_DEVI float expm1_k3(float x) {
+  float t = 1.0f / 362880.0f;
+  t = fmaf(t, x, 1.0f / 40320.0f);
+  t = fmaf(t, x, 1.0f / 5040.0f);
+  t = fmaf(t, x, 1.0f / 720.0f);
+  t = fmaf(t, x, 1.0f / 120.0f);
+  t = fmaf(t, x, 1.0f / 24.0f);
+  t = fmaf(t, x, 1.0f / 6.0f);
+  t = fmaf(t, x, 0.5f);
+  t = fmaf(t, x, 1.0f);
+  const float small = t * x;
+  return (fabsf(x) < 0.5f) ? small : expf(x) - 1.0f;
+}
+
+// SiTU-GLU with one exponential per input:  with A = e^(g/2) - 1 and B = e^(2u/25) - 1,
+//   tanh(g/4) = A / (A + 2),  sigmoid(g) = (A+1)^2 / ((A+1)^2 + 1),  tanh(u/25) = B / (B + 2),
+// so h = 100 * A/(A+2) * (A+1)^2/((A+1)^2+1) * B/(B+2).  g is clamped to 80 and u/25 to
+// [-40, 40], where every factor is already 1 (or -1) in f32; NaN passes through.
+K3_DEVI float situ_fast(float g, float u) {
+  g = (g > 80.0f) ? 80.0f : g;
+  float v = u * 0.08f;  // 2u/25
+  v = (v > 80.0f) ? 80.0f : ((v < -80.0f) ? -80.0f : v);
+  const float A = expm1_k3(0.5f * g), B = expm1_k3(v);
+  const float E = (A + 1.0f) * (A + 1.0f);
+  return 100.0f * __fdividef(A, A + 2.0f) * __fdividef(E, E + 1.0f) * __fdividef(B, B + 2.0f);
+}
+
+// TMEM store: each lane of the warp writes 32 (or 16) consecutive 32-bit columns of its
+// own lane of the warp's lane quarter
+K3_DEVI void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+K3_DEVI void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+K3_DEVI void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16
+K3_DEVI void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.u32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// named barrier over the producer warps
+K3_DEVI void producers_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(TM_PRODUCERS * 32) : "memory"); }
+
 template <int MODE>
 __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_constant__ CUtensorMap mapB,
                                                                   TcMoeParams p) {
   using Lay = TmLayout<MODE>;
-  constexpr int M = Lay::M, S = Lay::STAGES;
+  constexpr int M = Lay::M, SA = Lay::SA, SB = Lay::SB, RC = Lay::RC;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t base = (raw + 1023u) & ~1023u;  // B stages [SB][TM_NB rows][128 bytes]
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t bars = base + S * Lay::STAGE;
+  const uint32_t raw_base = base + SB * TM_B_BYTES;           // [RC][MROWS rows][128 bytes]
+  const uint32_t sraw_base = raw_base + RC * Lay::RAW_SLOT;    // [RC][MROWS rows][8 bytes]
+  const uint32_t bars = sraw_base + RC * Lay::SC_SLOT;
   auto fullA = [&](int s) { return bars + 8 * s; };
-  auto fullB = [&](int s) { return bars + 8 * (S + s); };
-  auto empty = [&](int s) { return bars + 8 * (2 * S + s); };
-  auto tfull = [&](int b) { return bars + 8 * (3 * S + b); };
-  auto tempty = [&](int b) { return bars + 8 * (3 * S + 2 + b); };
-  const uint32_t done_bar = bars + 8 * (3 * S + 4);
+  auto emptyA = [&](int s) { return bars + 8 * (SA + s); };
+  auto fullB = [&](int s) { return bars + 8 * (2 * SA + s); };
+  auto emptyB = [&](int s) { return bars + 8 * (2 * SA + SB + s); };
+  auto tfull = [&](int b) { return bars + 8 * (2 * SA + 2 * SB + b); };
+  auto tempty = [&](int b) { return bars + 8 * (2 * SA + 2 * SB + 2 + b); };
+  const uint32_t done_bar = bars + 8 * (2 * SA + 2 * SB + 4);
   volatile int* abort_flag = &abort_sh;
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < SA; ++s) {
       mbar_init(fullA(s), TM_PRODUCERS);
+      mbar_init(emptyA(s), 1);
+    }
+    for (int s = 0; s < SB; ++s) {
       mbar_init(fullB(s), 1);
-      mbar_init(empty(s), 1);
+      mbar_init(emptyB(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull(b), 1);
@@ -444,23 +552,26 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x) {
         const int slot0 = p.batches[tile / mtiles].slot0;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const int s = it % S;
-          if (!mbar_wait(empty(s), ((it / S) & 1) ^ 1, abort_flag)) break;
+          const int s = it % SB;
+          if (!mbar_wait(emptyB(s), ((it / SB) & 1) ^ 1, abort_flag)) break;
           mbar_expect_tx(fullB(s), TM_B_BYTES);
-          tma_load_2d(base + s * Lay::STAGE + M * TM_A_BYTES, &mapB, kb * TM_BK, slot0, fullB(s));
+          tma_load_2d(base + s * TM_B_BYTES, &mapB, kb * TM_BK, slot0, fullB(s));
         }
       }
-      for (int s = 0; s < S; ++s) {  // drain issued loads
-        const int last = it - 1 - ((it - 1 - s) % S + S) % S;
+      for (int s = 0; s < SB; ++s) {  // drain issued loads
+        const int last = it - 1 - ((it - 1 - s) % SB + SB) % SB;
         if (last >= 0 && last < it) {
           volatile int never = 0;
-          mbar_wait(fullB(s), (last / S) & 1, &never);
+          mbar_wait(fullB(s), (last / SB) & 1, &never);
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // B descriptors differ only in their start-address field: add (offset >> 4) to the
+      // stage-0 descriptor (addresses stay below 2^18, so the 14-bit field never carries)
+      const uint64_t dB = sdesc_sw128(base);
       int it = 0, lt = 0;
       for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x, ++lt) {
         const int n = p.batches[tile / mtiles].n;
@@ -471,21 +582,22 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
         tc_fence_after();
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const int s = it % S;
-          if (!mbar_wait(fullA(s), (it / S) & 1, abort_flag) || !mbar_wait(fullB(s), (it / S) & 1, abort_flag)) {
+          const int sa = it % SA, sb = it % SB;
+          if (!mbar_wait(fullA(sa), (it / SA) & 1, abort_flag) || !mbar_wait(fullB(sb), (it / SB) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t st = base + s * Lay::STAGE;
+          const uint64_t db = dB + ((uint32_t)(sb * TM_B_BYTES) >> 4);
 #pragma unroll
           for (int k = 0; k < TM_BK / 16; ++k) {
 #pragma unroll
             for (int m = 0; m < M; ++m)
-              tc_mma(tmem + b * 256 + m * 128, sdesc_sw128(st + m * TM_A_BYTES + k * 32),
-                     sdesc_sw128(st + M * TM_A_BYTES + k * 32), idesc, (kb | k) != 0);
+              tc_mma_ts(tmem + b * Lay::ACC + m * TM_NB, tmem + Lay::A_COL0 + (sa * M + m) * 32 + 8 * k, db + 2 * k,
+                        idesc, (kb | k) != 0);
           }
-          tc_commit(empty(s));
+          tc_commit(emptyA(sa));
+          tc_commit(emptyB(sb));
         }
         if (!ok) break;
         tc_commit(tfull(b));
@@ -506,21 +618,26 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       const MxBatch* rec = p.batches + tile / mtiles;
       const int slot0 = rec->slot0, n = rec->n;
       const int row = (tile % mtiles) * TM_ROWS + q * 32 + lane;
+      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + b * Lay::ACC;
 #pragma unroll 1
       for (int c = 0; c * 32 < n; ++c) {
         uint32_t r0[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + b * 256 + c * 32, r0);
+        tmem_ld32(tq + c * 32, r0);
         if (MODE == 0) {
           uint32_t r1[32];
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + b * 256 + 128 + c * 32, r1);
+          tmem_ld32(tq + TM_NB + c * 32, r1);
+          // lane j fetches column j's activation exponent p; the accumulators carry 2^p,
+          // removed exactly by two power-of-two factors (p lies in [-113, 141])
+          const int pw = (c * 32 + lane < n) ? __ldg(p.slot_pow + slot0 + c * 32 + lane) : 0;
+          const float f1 = pow2f(-(pw >> 1)), f2 = pow2f((pw >> 1) - pw);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
+            const float a1 = __shfl_sync(0xffffffffu, f1, j), a2 = __shfl_sync(0xffffffffu, f2, j);
             const int col = c * 32 + j;
             if (col < n) {
-              const int pw = __ldg(p.slot_pow + slot0 + col);
-              const float gg = scalbnf(__uint_as_float(r0[j]), -pw), uu = scalbnf(__uint_as_float(r1[j]), -pw);
-              const float h = __uint_as_float((uint32_t)f32_to_bf16_bits(situf(gg, uu)) << 16);  // bf16 rounding
+              const float gg = __uint_as_float(r0[j]) * a1 * a2, uu = __uint_as_float(r1[j]) * a1 * a2;
+              const float h = __uint_as_float((uint32_t)f32_to_bf16_bits(situ_fast(gg, uu)) << 16);  // bf16 rounding
               reinterpret_cast<__half*>(p.out)[(size_t)(slot0 + col) * p.R + row] = __float2half_rn(h * 256.0f);
             }
           }
@@ -539,64 +656,105 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
     }
   } else {
     // ------------------------------------------------------------ decode producers (warps 6..13)
+    // The raw bytes of a tile travel in chunks of 4 k-blocks: 128 bytes (one cache line)
+    // of each of the tile's MROWS rows, copied by all producer threads with 16-byte
+    // cp.async (eight threads per line) into a ring of RC chunks; 16-byte granules are
+    // XOR-swizzled by row so the decode reads are free of bank conflicts.  A named
+    // barrier per chunk publishes it to all producers.  When a tile starts, its rows
+    // (contiguous bytes per matrix) are prefetched into L2 in bulk.
+    // Decode: a warp owns the TMEM lane quarter warp % 4 (32 rows).  GATEUP: warps 6..9
+    // the gate matrix, 10..13 the up matrix, a k-block's 64 elements per thread (32
+    // columns); DOWN: warps 6..9 the first 32 elements of each k-block, 10..13 the second.
+    constexpr int MROWS = Lay::MROWS;
     const int pt = threadIdx.x - 6 * 32;  // 0..255
-    // GATEUP: thread = (matrix, row), 64 elements per k-block; DOWN: thread = (row, group), 32 elements
-    const int m = (MODE == 0) ? (pt >> 7) : 0;
-    const int r = pt & 127;
-    const int g0 = (MODE == 0) ? 0 : (pt >> 7);  // first group handled
-    constexpr int NG = (MODE == 0) ? 2 : 1;      // groups per thread per k-block
+    const int qd = warp & 3;
+    const int half = (warp - 6) >> 2;
+    const int m = (MODE == 0) ? half : 0;
+    const int g0 = (MODE == 0) ? 0 : half;
+    constexpr int NG = (MODE == 0) ? 2 : 1;  // 16-byte granules (32 elements) per thread per k-block
+    const int ri = m * TM_ROWS + qd * 32 + lane;  // row of the tile (over all matrices)
     const size_t qrow = (size_t)p.K / 2, srow = (size_t)p.K / 32;
-    bool bad = false;
-    int it = 0;
-    for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x) {
-      const MxBatch* rec = p.batches + tile / mtiles;
-      const uint8_t* q = rec->w[WOFF + 2 * m];
-      const uint8_t* sc = rec->w[WOFF + 2 * m + 1];
-      const size_t row = (size_t)(tile % mtiles) * TM_ROWS + r;
-      const uint8_t* qr = q + row * qrow + g0 * 16;
-      const uint8_t* sr = sc + row * srow + g0;
-      // register double buffer: the next k-block's bytes are loaded while this one decodes
-      uint4 nq[NG];
-      uint32_t ns;
-#pragma unroll
-      for (int g = 0; g < NG; ++g) nq[g] = __ldg(reinterpret_cast<const uint4*>(qr) + g);
-      ns = (NG == 2) ? __ldg(reinterpret_cast<const uint16_t*>(sr)) : __ldg(sr);
-      for (int kb = 0; kb < kblocks; ++kb, ++it) {
-        uint4 cq[NG];
-#pragma unroll
-        for (int g = 0; g < NG; ++g) cq[g] = nq[g];
-        const uint32_t cs = ns;
-        if (kb + 1 < kblocks) {
-#pragma unroll
-          for (int g = 0; g < NG; ++g) nq[g] = __ldg(reinterpret_cast<const uint4*>(qr + (kb + 1) * 32) + g);
-          ns = (NG == 2) ? __ldg(reinterpret_cast<const uint16_t*>(sr + (kb + 1) * 2)) : __ldg(sr + (kb + 1) * 2);
-          if (kb + 8 < kblocks && (kb & 3) == 0) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(qr + (kb + 8) * 32));
+    const int kchunks = kblocks / TM_CHUNK_KB;
+    const int my_tiles = (tiles > (int)blockIdx.x) ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int nchunks = my_tiles * kchunks;
+    bool stop = false;
+    auto issue = [&](int jc) {
+      if (jc < nchunks && !stop) {
+        const int tile = blockIdx.x + (jc / kchunks) * gridDim.x, kc = jc % kchunks;
+        const MxBatch* rec = p.batches + tile / mtiles;
+        const size_t row0 = (size_t)(tile % mtiles) * TM_ROWS;
+        if (kc == 0 && pt < 2 * M) {
+          const int mm = pt >> 1;
+          if (pt & 1) l2_prefetch_bulk(rec->w[WOFF + 2 * mm + 1] + row0 * srow, (uint32_t)(TM_ROWS * srow));
+          else l2_prefetch_bulk(rec->w[WOFF + 2 * mm] + row0 * qrow, (uint32_t)(TM_ROWS * qrow));
         }
-        const int s = it % S;
-        if (!mbar_wait(empty(s), ((it / S) & 1) ^ 1, abort_flag)) break;
-        uint8_t* arow = base_ptr + s * Lay::STAGE + m * TM_A_BYTES + r * 128;
+        const uint32_t dst = raw_base + (jc % RC) * Lay::RAW_SLOT;
+#pragma unroll
+        for (int k = 0; k < MROWS * 8 / (TM_PRODUCERS * 32); ++k) {
+          const int G = k * TM_PRODUCERS * 32 + pt;  // 16-byte granule of the chunk
+          const int rr = G >> 3, gc = G & 7, mm = rr / TM_ROWS;
+          const uint8_t* src = rec->w[WOFF + 2 * mm] + (row0 + (rr % TM_ROWS)) * qrow + kc * 128 + gc * 16;
+          cp_async16(dst + rr * 128 + ((gc ^ (rr & 7)) << 4), src);
+        }
+        if (pt < MROWS) {
+          const int mm = pt / TM_ROWS;
+          cp_async8(sraw_base + (jc % RC) * Lay::SC_SLOT + pt * 8,
+                    rec->w[WOFF + 2 * mm + 1] + (row0 + (pt % TM_ROWS)) * srow + kc * 8);
+        }
+      }
+      cp_async_commit();
+    };
+    bool bad = false;
+#pragma unroll 1
+    for (int j = 0; j < RC - 1; ++j) issue(j);
+    // every producer thread runs all nchunks iterations and meets every barrier; after an
+    // abort the waits and stores are skipped
+#pragma unroll 1
+    for (int jc = 0; jc < nchunks; ++jc) {
+      cp_async_wait<RC - 2>();  // chunk jc has landed (this thread's copies)
+      producers_sync();         // ... everyone's, and everyone is done with chunk jc - 1
+      if (*abort_flag) stop = true;
+      issue(jc + RC - 1);       // into the slot chunk jc - 1 used
+      if (stop) continue;
+      const uint8_t* src = base_ptr + (raw_base - base) + (jc % RC) * Lay::RAW_SLOT + ri * 128;
+      const uint2 sc8 = *reinterpret_cast<const uint2*>(base_ptr + (sraw_base - base) + (jc % RC) * Lay::SC_SLOT + ri * 8);
+#pragma unroll 1
+      for (int kq = 0; kq < TM_CHUNK_KB; ++kq) {
+        const int i = jc * TM_CHUNK_KB + kq;
+        const uint32_t cs = ((kq < 2) ? sc8.x : sc8.y) >> (16 * (kq & 1));  // this k-block's two scale bytes
+        uint32_t a[NG * 16];
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
-          const uint32_t sc2 = ue8m0_to_f16x2((cs >> (8 * g)) & 0xFFu, bad);
-          const uint32_t w4[4] = {cq[g].x, cq[g].y, cq[g].z, cq[g].w};
+          const uint4 cq = *reinterpret_cast<const uint4*>(src + (((2 * kq + g0 + g) ^ (ri & 7)) << 4));
+          const uint32_t sc2 = ue8m0_to_f16x2((cs >> (8 * (g0 + g))) & 0xFFu, bad);
+          const uint32_t w4[4] = {cq.x, cq.y, cq.z, cq.w};
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {  // 16-byte output chunk: 8 elements = 4 packed bytes
+          for (int cc = 0; cc < 4; ++cc) {  // 8 elements = 4 packed bytes -> 4 f16x2 columns
             uint32_t h[4];
             e2m1x8_to_f16x8(w4[cc], h);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h[e]), *reinterpret_cast<const __half2*>(&sc2));
-              h[e] = *reinterpret_cast<uint32_t*>(&v);
+              a[g * 16 + cc * 4 + e] = *reinterpret_cast<uint32_t*>(&v);
             }
-            const int chunk = (g0 + g) * 4 + cc;  // 16-byte chunk of the 128-byte row
-            *reinterpret_cast<uint4*>(arow + ((chunk ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
           }
         }
-        fence_async_smem();
+        const int sa = i % SA;
+        if (!__all_sync(0xffffffffu, mbar_wait(emptyA(sa), ((i / SA) & 1) ^ 1, abort_flag))) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + Lay::A_COL0 + (sa * M + m) * 32 + g0 * 16;
+        if constexpr (MODE == 0) tmem_st32(ta, a);
+        else tmem_st16(ta, a);
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(fullA(s));
+        if (lane == 0) mbar_arrive(fullA(sa));
       }
     }
+    cp_async_wait<0>();
     if (bad) flag_status(p.status, K3MOE_DEV_SCALE_RANGE);
   }
   __syncthreads();

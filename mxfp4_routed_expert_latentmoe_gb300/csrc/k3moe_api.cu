@@ -207,6 +207,10 @@ int mx_nblk(int T) { return T <= 8 ? 1 : 2; }
 // token count from which the projections and experts run on the tcgen05 GEMMs
 // (must match the workspace layout's choice)
 constexpr int kTcMinT = 256;
+// the grouped expert GEMM moves scale bytes four k-blocks (8 bytes) at a time, so it
+// needs both expert contraction lengths to be multiples of 256; other shapes keep the
+// weight-streaming kernels at every T
+bool tc_experts(const k3moe_dims& d, int T) { return T >= kTcMinT && d.latent % 256 == 0 && d.inter % 256 == 0; }
 
 // row-major [rows, cols] f16 matrix, boxes of box_rows x 64 with the 128-byte swizzle
 bool map_f16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
@@ -470,7 +474,7 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   tp.T = T; tp.E = d.n_experts; tp.K = d.top_k; tp.H = d.hidden; tp.tau = kTieTau;
   tp.ids = at<int32_t>(ws, L.ids); tp.w = at<float>(ws, L.w); tp.ids_out = ids_out; tp.w_out = w_out;
   tp.status = status;
-  const bool tc = T >= kTcMinT;
+  const bool tc = tc_experts(d, T);
   const int nblk = mx_nblk(T);
   const int NB = tc ? TM_NB : 8 * nblk;  // tokens per expert batch
   const PermParams pp = perm_params(d, T, d.top_k, at<int32_t>(ws, L.ids), 0, NB, ws, L, experts);
