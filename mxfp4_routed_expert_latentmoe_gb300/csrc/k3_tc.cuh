@@ -368,25 +368,32 @@ namespace k3 {
 // GATEUP: two matrices (gate rows, up rows) share B; the epilogue applies SiTU-GLU,
 // rounds h to bf16 and stores it (x 2^8, f16) in slot order.  DOWN: one matrix; the
 // epilogue stores o (fp32) in slot order.
-constexpr int TM_ROWS = 128;       // weight rows per tile (MMA M)
+constexpr int TM_ROWS = 128;       // weight rows per MMA (M)
+constexpr int TM_BLOCKS = 2;       // row blocks per tile, each with its own accumulator and MMA issuer
 constexpr int TM_NB = 96;          // tokens per batch (MMA N <= 96): bounded by TMEM columns
 constexpr int TM_BK = 64;          // k-block
 constexpr int TM_PRODUCERS = 8;    // decode warps
-constexpr int TM_THREADS = (6 + TM_PRODUCERS) * 32;
+constexpr int TM_THREADS = (7 + TM_PRODUCERS) * 32;
 constexpr int TM_B_BYTES = TM_NB * TM_BK * 2;  // 12 KB
 constexpr int TM_CHUNK_KB = 4;     // k-blocks per raw chunk: 128 bytes (one cache line) of every row
 
+// Tile = 2 row blocks of 128 weight rows x one token batch.  GATEUP: block 0 = gate rows
+// 128 t .. 128 t + 127, block 1 = the same rows of the up matrix; DOWN: blocks 0 and 1 =
+// rows 256 t .. 256 t + 255 of the down matrix.  Two blocks, two accumulators and two
+// issuing threads: one thread issues a kind::f16 MMA no faster than about every 100
+// cycles at these N, two in parallel double the tensor-core rate.
 template <int MODE>
 struct TmLayout {
-  static constexpr int M = (MODE == 0) ? 2 : 1;
-  static constexpr int MROWS = M * TM_ROWS;             // weight rows per tile over all matrices
-  // TMEM columns: accumulators (2 buffers) then the A stages (32 columns per matrix per stage)
-  static constexpr int ACC = (MODE == 0) ? 2 * TM_NB : 128;  // per buffer; GATEUP: gate, then up at +TM_NB
-  static constexpr int SA = (MODE == 0) ? 2 : 4;             // A stages
+  static constexpr int MROWS = TM_BLOCKS * TM_ROWS;   // 256 weight rows per tile
+  static constexpr int TILE_ROWS = (MODE == 0) ? TM_ROWS : MROWS;  // output rows per tile
+  // TMEM columns: accumulators (2 buffers x 2 blocks x TM_NB), then the A stages
+  // (32 columns = 64 f16 per block per stage)
+  static constexpr int ACC = TM_BLOCKS * TM_NB;
+  static constexpr int SA = 2;
   static constexpr int A_COL0 = 2 * ACC;
-  static_assert(A_COL0 + SA * M * 32 <= 512, "TMEM columns");
-  static constexpr int SB = 4;                               // B stages (shared memory)
-  static constexpr int RC = 3;                               // raw chunks in flight
+  static_assert(A_COL0 + SA * TM_BLOCKS * 32 <= 512, "TMEM columns");
+  static constexpr int SB = 4;                        // B stages (shared memory)
+  static constexpr int RC = 3;                        // raw chunks in flight
   static constexpr int RAW_SLOT = MROWS * 128;
   static constexpr int SC_SLOT = MROWS * 8;
   static constexpr int SMEM = 1024 + SB * TM_B_BYTES + RC * (RAW_SLOT + SC_SLOT) + 512;
@@ -491,7 +498,7 @@ template <int MODE>
 __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_constant__ CUtensorMap mapB,
                                                                   TcMoeParams p) {
   using Lay = TmLayout<MODE>;
-  constexpr int M = Lay::M, SA = Lay::SA, SB = Lay::SB, RC = Lay::RC;
+  constexpr int SA = Lay::SA, SB = Lay::SB, RC = Lay::RC, MROWS = Lay::MROWS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -499,8 +506,8 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // B stages [SB][TM_NB rows][128 bytes]
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t raw_base = base + SB * TM_B_BYTES;           // [RC][MROWS rows][128 bytes]
-  const uint32_t sraw_base = raw_base + RC * Lay::RAW_SLOT;    // [RC][MROWS rows][8 bytes]
+  const uint32_t raw_base = base + SB * TM_B_BYTES;         // [RC][MROWS rows][128 bytes]
+  const uint32_t sraw_base = raw_base + RC * Lay::RAW_SLOT;  // [RC][MROWS rows][8 bytes]
   const uint32_t bars = sraw_base + RC * Lay::SC_SLOT;
   auto fullA = [&](int s) { return bars + 8 * s; };
   auto emptyA = [&](int s) { return bars + 8 * (SA + s); };
@@ -515,17 +522,17 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
     abort_sh = 0;
     for (int s = 0; s < SA; ++s) {
       mbar_init(fullA(s), TM_PRODUCERS);
-      mbar_init(emptyA(s), 1);
+      mbar_init(emptyA(s), TM_BLOCKS);  // one commit per issuer
     }
     for (int s = 0; s < SB; ++s) {
       mbar_init(fullB(s), 1);
-      mbar_init(emptyB(s), 1);
+      mbar_init(emptyB(s), TM_BLOCKS);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(tfull(b), 1);
+      mbar_init(tfull(b), TM_BLOCKS);
       mbar_init(tempty(b), 128);
     }
-    mbar_init(done_bar, 1);
+    mbar_init(done_bar, TM_BLOCKS);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -540,10 +547,12 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
   grid_dep_wait();
   grid_dep_launch();
 
-  const int mtiles = p.R / TM_ROWS;
+  const int mtiles = p.R / Lay::TILE_ROWS;
   const int tiles = mtiles * (*p.n_batches);
   const int kblocks = p.K / TM_BK;
-  constexpr int WOFF = (MODE == 0) ? 0 : 4;
+  // weight tensor (index into MxBatch::w) and first row of block mm of row tile tm
+  auto blk_tensor = [](int mm) { return (MODE == 0) ? 2 * mm : 4; };
+  auto blk_row0 = [](int tm, int mm) { return (MODE == 0) ? (size_t)tm * TM_ROWS : (size_t)tm * MROWS + mm * TM_ROWS; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (B)
@@ -566,9 +575,10 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp <= TM_BLOCKS) {
+    // ------------------------------------------------------------ MMA issuers (warp 1: block 0, warp 2: block 1)
     if (lane == 0) {
+      const int mm = warp - 1;
       // B descriptors differ only in their start-address field: add (offset >> 4) to the
       // stage-0 descriptor (addresses stay below 2^18, so the 14-bit field never carries)
       const uint64_t dB = sdesc_sw128(base);
@@ -580,6 +590,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
         const int b = lt & 1;
         if (!mbar_wait(tempty(b), ((lt >> 1) & 1) ^ 1, abort_flag)) break;
         tc_fence_after();
+        const uint32_t d = tmem + b * Lay::ACC + mm * TM_NB;
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int sa = it % SA, sb = it % SB;
@@ -589,13 +600,9 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
           }
           tc_fence_after();
           const uint64_t db = dB + ((uint32_t)(sb * TM_B_BYTES) >> 4);
+          const uint32_t ta = tmem + Lay::A_COL0 + (sa * TM_BLOCKS + mm) * 32;
 #pragma unroll
-          for (int k = 0; k < TM_BK / 16; ++k) {
-#pragma unroll
-            for (int m = 0; m < M; ++m)
-              tc_mma_ts(tmem + b * Lay::ACC + m * TM_NB, tmem + Lay::A_COL0 + (sa * M + m) * 32 + 8 * k, db + 2 * k,
-                        idesc, (kb | k) != 0);
-          }
+          for (int k = 0; k < TM_BK / 16; ++k) tc_mma_ts(d, ta + 8 * k, db + 2 * k, idesc, (kb | k) != 0);
           tc_commit(emptyA(sa));
           tc_commit(emptyB(sb));
         }
@@ -606,8 +613,8 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       volatile int never = 0;
       mbar_wait(done_bar, 0, &never);
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
+  } else if (warp < 3 + TM_BLOCKS + 2) {
+    // ------------------------------------------------------------ epilogue (warps 3..6)
     const int q = warp & 3;
     int lt = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
@@ -617,15 +624,15 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       tc_fence_after();
       const MxBatch* rec = p.batches + tile / mtiles;
       const int slot0 = rec->slot0, n = rec->n;
-      const int row = (tile % mtiles) * TM_ROWS + q * 32 + lane;
+      const int tm = tile % mtiles;
       const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + b * Lay::ACC;
 #pragma unroll 1
       for (int c = 0; c * 32 < n; ++c) {
-        uint32_t r0[32];
+        uint32_t r0[32], r1[32];
         tmem_ld32(tq + c * 32, r0);
+        tmem_ld32(tq + TM_NB + c * 32, r1);
         if (MODE == 0) {
-          uint32_t r1[32];
-          tmem_ld32(tq + TM_NB + c * 32, r1);
+          const int row = tm * TM_ROWS + q * 32 + lane;
           // lane j fetches column j's activation exponent p; the accumulators carry 2^p,
           // removed exactly by two power-of-two factors (p lies in [-113, 141])
           const int pw = (c * 32 + lane < n) ? __ldg(p.slot_pow + slot0 + c * 32 + lane) : 0;
@@ -642,12 +649,16 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
             }
           }
         } else {
+          const int row0 = tm * MROWS + q * 32 + lane;
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int col = c * 32 + j;
-            if (col < n)
-              reinterpret_cast<float*>(p.out)[(size_t)(slot0 + col) * p.R + row] = __uint_as_float(r0[j]) * (1.0f / 256.0f);
+            if (col < n) {
+              float* o = reinterpret_cast<float*>(p.out) + (size_t)(slot0 + col) * p.R + row0;
+              o[0] = __uint_as_float(r0[j]) * (1.0f / 256.0f);
+              o[TM_ROWS] = __uint_as_float(r1[j]) * (1.0f / 256.0f);
+            }
           }
         }
       }
@@ -655,24 +666,19 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       mbar_arrive(tempty(b));
     }
   } else {
-    // ------------------------------------------------------------ decode producers (warps 6..13)
+    // ------------------------------------------------------------ decode producers (warps 7..14)
     // The raw bytes of a tile travel in chunks of 4 k-blocks: 128 bytes (one cache line)
-    // of each of the tile's MROWS rows, copied by all producer threads with 16-byte
+    // of each of the tile's 256 rows, copied by all producer threads with 16-byte
     // cp.async (eight threads per line) into a ring of RC chunks; 16-byte granules are
     // XOR-swizzled by row so the decode reads are free of bank conflicts.  A named
     // barrier per chunk publishes it to all producers.  When a tile starts, its rows
-    // (contiguous bytes per matrix) are prefetched into L2 in bulk.
-    // Decode: a warp owns the TMEM lane quarter warp % 4 (32 rows).  GATEUP: warps 6..9
-    // the gate matrix, 10..13 the up matrix, a k-block's 64 elements per thread (32
-    // columns); DOWN: warps 6..9 the first 32 elements of each k-block, 10..13 the second.
-    constexpr int MROWS = Lay::MROWS;
-    const int pt = threadIdx.x - 6 * 32;  // 0..255
+    // (contiguous bytes per block) are prefetched into L2 in bulk.
+    // Decode: a warp owns the TMEM lane quarter warp % 4 (32 rows) of one block (warps
+    // 7..10 block 0, 11..14 block 1), a k-block's 64 elements per thread (32 columns).
+    const int pt = threadIdx.x - (3 + TM_BLOCKS + 2) * 32;  // 0..255
     const int qd = warp & 3;
-    const int half = (warp - 6) >> 2;
-    const int m = (MODE == 0) ? half : 0;
-    const int g0 = (MODE == 0) ? 0 : half;
-    constexpr int NG = (MODE == 0) ? 2 : 1;  // 16-byte granules (32 elements) per thread per k-block
-    const int ri = m * TM_ROWS + qd * 32 + lane;  // row of the tile (over all matrices)
+    const int mb = (warp - (3 + TM_BLOCKS + 2)) >> 2;
+    const int ri = mb * TM_ROWS + qd * 32 + lane;  // row of the tile (over both blocks)
     const size_t qrow = (size_t)p.K / 2, srow = (size_t)p.K / 32;
     const int kchunks = kblocks / TM_CHUNK_KB;
     const int my_tiles = (tiles > (int)blockIdx.x) ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -682,24 +688,25 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       if (jc < nchunks && !stop) {
         const int tile = blockIdx.x + (jc / kchunks) * gridDim.x, kc = jc % kchunks;
         const MxBatch* rec = p.batches + tile / mtiles;
-        const size_t row0 = (size_t)(tile % mtiles) * TM_ROWS;
-        if (kc == 0 && pt < 2 * M) {
+        const int tm = tile % mtiles;
+        if (kc == 0 && pt < 2 * TM_BLOCKS) {
           const int mm = pt >> 1;
-          if (pt & 1) l2_prefetch_bulk(rec->w[WOFF + 2 * mm + 1] + row0 * srow, (uint32_t)(TM_ROWS * srow));
-          else l2_prefetch_bulk(rec->w[WOFF + 2 * mm] + row0 * qrow, (uint32_t)(TM_ROWS * qrow));
+          const size_t r0 = blk_row0(tm, mm);
+          if (pt & 1) l2_prefetch_bulk(rec->w[blk_tensor(mm) + 1] + r0 * srow, (uint32_t)(TM_ROWS * srow));
+          else l2_prefetch_bulk(rec->w[blk_tensor(mm)] + r0 * qrow, (uint32_t)(TM_ROWS * qrow));
         }
         const uint32_t dst = raw_base + (jc % RC) * Lay::RAW_SLOT;
 #pragma unroll
         for (int k = 0; k < MROWS * 8 / (TM_PRODUCERS * 32); ++k) {
           const int G = k * TM_PRODUCERS * 32 + pt;  // 16-byte granule of the chunk
           const int rr = G >> 3, gc = G & 7, mm = rr / TM_ROWS;
-          const uint8_t* src = rec->w[WOFF + 2 * mm] + (row0 + (rr % TM_ROWS)) * qrow + kc * 128 + gc * 16;
+          const uint8_t* src = rec->w[blk_tensor(mm)] + (blk_row0(tm, mm) + (rr % TM_ROWS)) * qrow + kc * 128 + gc * 16;
           cp_async16(dst + rr * 128 + ((gc ^ (rr & 7)) << 4), src);
         }
-        if (pt < MROWS) {
+        {
           const int mm = pt / TM_ROWS;
           cp_async8(sraw_base + (jc % RC) * Lay::SC_SLOT + pt * 8,
-                    rec->w[WOFF + 2 * mm + 1] + (row0 + (pt % TM_ROWS)) * srow + kc * 8);
+                    rec->w[blk_tensor(mm) + 1] + (blk_row0(tm, mm) + (pt % TM_ROWS)) * srow + kc * 8);
         }
       }
       cp_async_commit();
@@ -722,11 +729,11 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       for (int kq = 0; kq < TM_CHUNK_KB; ++kq) {
         const int i = jc * TM_CHUNK_KB + kq;
         const uint32_t cs = ((kq < 2) ? sc8.x : sc8.y) >> (16 * (kq & 1));  // this k-block's two scale bytes
-        uint32_t a[NG * 16];
+        uint32_t a[32];
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          const uint4 cq = *reinterpret_cast<const uint4*>(src + (((2 * kq + g0 + g) ^ (ri & 7)) << 4));
-          const uint32_t sc2 = ue8m0_to_f16x2((cs >> (8 * (g0 + g))) & 0xFFu, bad);
+        for (int g = 0; g < 2; ++g) {
+          const uint4 cq = *reinterpret_cast<const uint4*>(src + (((2 * kq + g) ^ (ri & 7)) << 4));
+          const uint32_t sc2 = ue8m0_to_f16x2((cs >> (8 * g)) & 0xFFu, bad);
           const uint32_t w4[4] = {cq.x, cq.y, cq.z, cq.w};
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {  // 8 elements = 4 packed bytes -> 4 f16x2 columns
@@ -745,9 +752,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
           break;
         }
         tc_fence_after();
-        const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + Lay::A_COL0 + (sa * M + m) * 32 + g0 * 16;
-        if constexpr (MODE == 0) tmem_st32(ta, a);
-        else tmem_st16(ta, a);
+        tmem_st32(tmem + ((uint32_t)(qd * 32) << 16) + Lay::A_COL0 + (sa * TM_BLOCKS + mb) * 32, a);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
