@@ -23,6 +23,10 @@ K3_DEVI void cp_async16(uint32_t dst, const void* src) {
 K3_DEVI void cp_async8(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src));
 }
+// 4-byte copy
+K3_DEVI void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
+}
 K3_DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 K3_DEVI void cp_async_wait() {

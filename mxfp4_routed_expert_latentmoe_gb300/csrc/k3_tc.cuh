@@ -76,6 +76,37 @@ K3_DEVI bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) 
   }
 }
 
+// Non-suspending test of the phase with the given parity.
+K3_DEVI bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// As mbar_wait, but spinning on test_wait: the lowest wake-up latency, for the single
+// thread that issues MMAs (a suspended thread took hundreds of cycles to resume).
+K3_DEVI bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_test(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > (1ll << 32)) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 K3_DEVI void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
@@ -125,6 +156,16 @@ K3_DEVI void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
         "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns
+K3_DEVI void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
+      "[%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
 }
@@ -373,9 +414,10 @@ constexpr int TM_BLOCKS = 2;       // row blocks per tile, each with its own acc
 constexpr int TM_NB = 96;          // tokens per batch (MMA N <= 96): bounded by TMEM columns
 constexpr int TM_BK = 64;          // k-block
 constexpr int TM_PRODUCERS = 8;    // decode warps
-constexpr int TM_THREADS = (7 + TM_PRODUCERS) * 32;
+constexpr int TM_EPI = 8;         // epilogue warps: two per TMEM lane quarter, alternate 16-column chunks
+constexpr int TM_THREADS = (3 + TM_EPI + TM_PRODUCERS) * 32;
 constexpr int TM_B_BYTES = TM_NB * TM_BK * 2;  // 12 KB
-constexpr int TM_CHUNK_KB = 4;     // k-blocks per raw chunk: 128 bytes (one cache line) of every row
+constexpr int TM_AKB = 2;          // k-blocks per A stage (one barrier round trip per stage)
 
 // Tile = 2 row blocks of 128 weight rows x one token batch.  GATEUP: block 0 = gate rows
 // 128 t .. 128 t + 127, block 1 = the same rows of the up matrix; DOWN: blocks 0 and 1 =
@@ -386,17 +428,33 @@ template <int MODE>
 struct TmLayout {
   static constexpr int MROWS = TM_BLOCKS * TM_ROWS;   // 256 weight rows per tile
   static constexpr int TILE_ROWS = (MODE == 0) ? TM_ROWS : MROWS;  // output rows per tile
-  // TMEM columns: accumulators (2 buffers x 2 blocks x TM_NB), then the A stages
-  // (32 columns = 64 f16 per block per stage)
+  // TMEM columns: one accumulator buffer (2 blocks x TM_NB), then SA A stages of
+  // TM_AKB k-blocks (64 columns = 128 f16 per block per stage).  The epilogue empties the
+  // accumulators into shared memory (GATEUP) or global memory (DOWN) at once, so one
+  // buffer suffices and the columns go to A stages, which the MMA-completion -> decode ->
+  // MMA chain needs.
   static constexpr int ACC = TM_BLOCKS * TM_NB;
   static constexpr int SA = 2;
-  static constexpr int A_COL0 = 2 * ACC;
-  static_assert(A_COL0 + SA * TM_BLOCKS * 32 <= 512, "TMEM columns");
-  static constexpr int SB = 4;                        // B stages (shared memory)
-  static constexpr int RC = 3;                        // raw chunks in flight
-  static constexpr int RAW_SLOT = MROWS * 128;
-  static constexpr int SC_SLOT = MROWS * 8;
-  static constexpr int SMEM = 1024 + SB * TM_B_BYTES + RC * (RAW_SLOT + SC_SLOT) + 512;
+  static constexpr int A_COLS = TM_AKB * 32;          // per block per stage
+  static constexpr int A_COL0 = ACC;
+  static_assert(A_COL0 + SA * TM_BLOCKS * A_COLS <= 512, "TMEM columns");
+  // B slots (one k-block each, shared memory) in NBS groups of TM_AKB: group st % NBS
+  // holds stage st's token tiles, so TMA runs up to NBS stages ahead (NBS >= SA)
+  static constexpr int SB = (MODE == 0) ? 4 : 8;
+  static constexpr int NBS = SB / TM_AKB;
+  static_assert(SB % TM_AKB == 0 && NBS >= SA, "B slot groups");
+  // raw chunks: CKB k-blocks = CKB * 32 bytes of every row
+  static constexpr int CKB = 4;
+  static constexpr int ROWB = CKB * 32;                // raw bytes per row per chunk
+  static constexpr int GPR = ROWB / 16;                // 16-byte granules per row per chunk
+  static_assert(CKB % TM_AKB == 0, "chunks hold whole A stages");
+  static constexpr int RC = (MODE == 0) ? 2 : 3;      // raw chunks in flight
+  static constexpr int RAW_SLOT = MROWS * ROWB;
+  static constexpr int SC_SLOT = MROWS * CKB * 2;     // two scale bytes per row per k-block
+  // GATEUP staging of the accumulators: per epilogue thread up to 3 chunks x (16 g + 16 u)
+  static constexpr int STG_WORDS = (MODE == 0) ? (TM_NB / 16 / 2) * 32 : 0;
+  static constexpr int STG = STG_WORDS * TM_EPI * 32 * 4;
+  static constexpr int SMEM = 1024 + SB * TM_B_BYTES + RC * (RAW_SLOT + SC_SLOT) + STG + 512;
 };
 
 struct TcMoeParams {
@@ -418,11 +476,6 @@ K3_DEVI uint32_t ue8m0_to_f16x2(uint32_t s, bool& bad) {
   else h = 0u;
   bad |= (s < 105u || s > 142u);
   return h | (h << 16);
-}
-
-// bulk prefetch of `bytes` contiguous global bytes into L2 (16-byte aligned, multiple of 16)
-K3_DEVI void l2_prefetch_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // 2^e as f32 for e in [-126, 127]
@@ -506,31 +559,36 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // B stages [SB][TM_NB rows][128 bytes]
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t raw_base = base + SB * TM_B_BYTES;         // [RC][MROWS rows][128 bytes]
-  const uint32_t sraw_base = raw_base + RC * Lay::RAW_SLOT;  // [RC][MROWS rows][8 bytes]
-  const uint32_t bars = sraw_base + RC * Lay::SC_SLOT;
-  auto fullA = [&](int s) { return bars + 8 * s; };
-  auto emptyA = [&](int s) { return bars + 8 * (SA + s); };
-  auto fullB = [&](int s) { return bars + 8 * (2 * SA + s); };
-  auto emptyB = [&](int s) { return bars + 8 * (2 * SA + SB + s); };
-  auto tfull = [&](int b) { return bars + 8 * (2 * SA + 2 * SB + b); };
-  auto tempty = [&](int b) { return bars + 8 * (2 * SA + 2 * SB + 2 + b); };
-  const uint32_t done_bar = bars + 8 * (2 * SA + 2 * SB + 4);
+  const uint32_t raw_base = base + SB * TM_B_BYTES;         // [RC][MROWS rows][ROWB bytes]
+  const uint32_t sraw_base = raw_base + RC * Lay::RAW_SLOT;  // [RC][MROWS rows][2 CKB bytes]
+  const uint32_t stg_base = sraw_base + RC * Lay::SC_SLOT;  // [STG_WORDS][epilogue thread] f32
+  const uint32_t bars = stg_base + Lay::STG;
+  // Stage st = TM_AKB k-blocks: A in TMEM slot st % SA, B in shared-memory group st % NBS.
+  // fullA(s, m): block m's producers stored A slot s; fullB(g): TMA landed B group g;
+  // kdone(g): both issuers' MMAs of the stage in group g completed, which frees its B group
+  // and (NBS >= SA) its A slot: one commit per stage serves both rings.
+  constexpr int NBS = Lay::NBS;
+  auto fullA = [&](int s, int m) { return bars + 8 * (s * TM_BLOCKS + m); };
+  auto kdone = [&](int g) { return bars + 8 * (SA * TM_BLOCKS + g); };
+  auto fullB = [&](int g) { return bars + 8 * (SA * TM_BLOCKS + NBS + g); };
+  constexpr int NB0 = SA * TM_BLOCKS + 2 * NBS;
+  auto tfull = [&](int b) { return bars + 8 * (NB0 + b); };
+  auto tempty = [&](int b) { return bars + 8 * (NB0 + 2 + b); };
+  const uint32_t done_bar = bars + 8 * (NB0 + 4);
+  static_assert(8 * (NB0 + 5) <= 512, "barrier space");
   volatile int* abort_flag = &abort_sh;
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
-    for (int s = 0; s < SA; ++s) {
-      mbar_init(fullA(s), TM_PRODUCERS);
-      mbar_init(emptyA(s), TM_BLOCKS);  // one commit per issuer
-    }
-    for (int s = 0; s < SB; ++s) {
-      mbar_init(fullB(s), 1);
-      mbar_init(emptyB(s), TM_BLOCKS);
+    for (int s = 0; s < SA; ++s)
+      for (int m = 0; m < TM_BLOCKS; ++m) mbar_init(fullA(s, m), TM_PRODUCERS / TM_BLOCKS);
+    for (int g = 0; g < NBS; ++g) {
+      mbar_init(kdone(g), TM_BLOCKS);  // one commit per issuer
+      mbar_init(fullB(g), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull(b), TM_BLOCKS);
-      mbar_init(tempty(b), 128);
+      mbar_init(tempty(b), TM_EPI * 32);
     }
     mbar_init(done_bar, TM_BLOCKS);
     fence_barrier_init();
@@ -557,21 +615,24 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (B)
     if (lane == 0) {
-      int it = 0;
+      int bs = 0;  // stages loaded
       for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x) {
         const int slot0 = p.batches[tile / mtiles].slot0;
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const int s = it % SB;
-          if (!mbar_wait(emptyB(s), ((it / SB) & 1) ^ 1, abort_flag)) break;
-          mbar_expect_tx(fullB(s), TM_B_BYTES);
-          tma_load_2d(base + s * TM_B_BYTES, &mapB, kb * TM_BK, slot0, fullB(s));
+        for (int kb = 0; kb < kblocks; kb += TM_AKB, ++bs) {
+          // group bs % NBS last held stage bs - NBS
+          const int g = bs % NBS;
+          if (!mbar_wait(kdone(g), ((bs / NBS) & 1) ^ 1, abort_flag)) break;
+          mbar_expect_tx(fullB(g), TM_AKB * TM_B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < TM_AKB; ++kk)
+            tma_load_2d(base + (g * TM_AKB + kk) * TM_B_BYTES, &mapB, (kb + kk) * TM_BK, slot0, fullB(g));
         }
       }
-      for (int s = 0; s < SB; ++s) {  // drain issued loads
-        const int last = it - 1 - ((it - 1 - s) % SB + SB) % SB;
-        if (last >= 0 && last < it) {
+      for (int g = 0; g < NBS; ++g) {  // drain issued loads
+        const int last = bs - 1 - ((bs - 1 - g) % NBS + NBS) % NBS;
+        if (last >= 0 && last < bs) {
           volatile int never = 0;
-          mbar_wait(fullB(s), (last / SB) & 1, &never);
+          mbar_wait(fullB(g), (last / NBS) & 1, &never);
         }
       }
     }
@@ -587,73 +648,73 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
         const int n = p.batches[tile / mtiles].n;
         const int N = (n + 15) & ~15;
         const uint32_t idesc = (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(TM_ROWS >> 4) << 24);  // f16 x f16 -> f32
-        const int b = lt & 1;
-        if (!mbar_wait(tempty(b), ((lt >> 1) & 1) ^ 1, abort_flag)) break;
+        if (!mbar_wait_spin(tempty(0), (lt & 1) ^ 1, abort_flag)) break;  // accumulators emptied
         tc_fence_after();
-        const uint32_t d = tmem + b * Lay::ACC + mm * TM_NB;
+        const uint32_t d = tmem + mm * TM_NB;
         bool ok = true;
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const int sa = it % SA, sb = it % SB;
-          if (!mbar_wait(fullA(sa), (it / SA) & 1, abort_flag) || !mbar_wait(fullB(sb), (it / SB) & 1, abort_flag)) {
+        for (int kb = 0; kb < kblocks; kb += TM_AKB, it += TM_AKB) {
+          const int st = it / TM_AKB, sa = st % SA, g = st % NBS;
+          // B (loaded up to NBS stages ahead) is normally ready first: test it while A is stored
+          if (!mbar_wait_spin(fullB(g), (st / NBS) & 1, abort_flag) ||
+              !mbar_wait_spin(fullA(sa, mm), (st / SA) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t db = dB + ((uint32_t)(sb * TM_B_BYTES) >> 4);
-          const uint32_t ta = tmem + Lay::A_COL0 + (sa * TM_BLOCKS + mm) * 32;
+          const uint32_t ta = tmem + Lay::A_COL0 + (sa * TM_BLOCKS + mm) * Lay::A_COLS;
 #pragma unroll
-          for (int k = 0; k < TM_BK / 16; ++k) tc_mma_ts(d, ta + 8 * k, db + 2 * k, idesc, (kb | k) != 0);
-          tc_commit(emptyA(sa));
-          tc_commit(emptyB(sb));
+          for (int kk = 0; kk < TM_AKB; ++kk) {
+            const uint64_t db = dB + ((uint32_t)((g * TM_AKB + kk) * TM_B_BYTES) >> 4);
+#pragma unroll
+            for (int k = 0; k < TM_BK / 16; ++k)
+              tc_mma_ts(d, ta + kk * 32 + 8 * k, db + 2 * k, idesc, (kb | kk | k) != 0);
+          }
+          tc_commit(kdone(g));
         }
         if (!ok) break;
-        tc_commit(tfull(b));
+        tc_commit(tfull(0));
       }
       tc_commit(done_bar);
       volatile int never = 0;
       mbar_wait(done_bar, 0, &never);
     }
-  } else if (warp < 3 + TM_BLOCKS + 2) {
-    // ------------------------------------------------------------ epilogue (warps 3..6)
+  } else if (warp < 3 + TM_EPI) {
+    // ------------------------------------------------------------ epilogue (warps 3..10)
+    // warp w reads TMEM lane quarter w % 4 (32 weight rows) and the 16-column chunks
+    // e, e + 2, e + 4 of the batch's tokens (e = 0 for warps 3..6, 1 for 7..10).  It first
+    // empties its accumulator chunks (GATEUP: into its own shared-memory words; DOWN:
+    // straight to the output) and releases TMEM, then (GATEUP) applies SiTU-GLU while the
+    // next tile's MMAs run.
     const int q = warp & 3;
+    const int e0 = (warp - 3) >> 2;
+    const int et = threadIdx.x - 3 * 32;  // epilogue thread 0..255
+    float* stg = reinterpret_cast<float*>(base_ptr + (stg_base - base)) + et;  // word k at stg[k * 256]
     int lt = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++lt) {
-      const int b = lt & 1;
       // warp-uniform outcome: the tcgen05.ld below must be executed by all 32 lanes
-      if (!__all_sync(0xffffffffu, mbar_wait(tfull(b), (lt >> 1) & 1, abort_flag))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull(0), lt & 1, abort_flag))) break;
       tc_fence_after();
       const MxBatch* rec = p.batches + tile / mtiles;
       const int slot0 = rec->slot0, n = rec->n;
       const int tm = tile % mtiles;
-      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + b * Lay::ACC;
+      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c * 32 < n; ++c) {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tq + c * 32, r0);
-        tmem_ld32(tq + TM_NB + c * 32, r1);
+      for (int c = e0, k = 0; c * 16 < n; c += 2, ++k) {
+        uint32_t r0[16], r1[16];
+        tmem_ld16(tq + c * 16, r0);
+        tmem_ld16(tq + TM_NB + c * 16, r1);
+        tmem_ld_wait();
         if (MODE == 0) {
-          const int row = tm * TM_ROWS + q * 32 + lane;
-          // lane j fetches column j's activation exponent p; the accumulators carry 2^p,
-          // removed exactly by two power-of-two factors (p lies in [-113, 141])
-          const int pw = (c * 32 + lane < n) ? __ldg(p.slot_pow + slot0 + c * 32 + lane) : 0;
-          const float f1 = pow2f(-(pw >> 1)), f2 = pow2f((pw >> 1) - pw);
-          tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float a1 = __shfl_sync(0xffffffffu, f1, j), a2 = __shfl_sync(0xffffffffu, f2, j);
-            const int col = c * 32 + j;
-            if (col < n) {
-              const float gg = __uint_as_float(r0[j]) * a1 * a2, uu = __uint_as_float(r1[j]) * a1 * a2;
-              const float h = __uint_as_float((uint32_t)f32_to_bf16_bits(situ_fast(gg, uu)) << 16);  // bf16 rounding
-              reinterpret_cast<__half*>(p.out)[(size_t)(slot0 + col) * p.R + row] = __float2half_rn(h * 256.0f);
-            }
+          for (int j = 0; j < 16; ++j) {
+            stg[(k * 32 + j) * (TM_EPI * 32)] = __uint_as_float(r0[j]);
+            stg[(k * 32 + 16 + j) * (TM_EPI * 32)] = __uint_as_float(r1[j]);
           }
         } else {
           const int row0 = tm * MROWS + q * 32 + lane;
-          tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int col = c * 32 + j;
+          for (int j = 0; j < 16; ++j) {
+            const int col = c * 16 + j;
             if (col < n) {
               float* o = reinterpret_cast<float*>(p.out) + (size_t)(slot0 + col) * p.R + row0;
               o[0] = __uint_as_float(r0[j]) * (1.0f / 256.0f);
@@ -663,24 +724,47 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
         }
       }
       tc_fence_before();
-      mbar_arrive(tempty(b));
+      mbar_arrive(tempty(0));
+      if (MODE == 0) {
+        const int row = tm * TM_ROWS + q * 32 + lane;
+#pragma unroll 1
+        for (int c = e0, k = 0; c * 16 < n; c += 2, ++k) {
+          // lane j < 16 fetches column j's activation exponent p; the accumulators carry
+          // 2^p, removed exactly by two power-of-two factors (p lies in [-113, 141])
+          const int pw = (lane < 16 && c * 16 + lane < n) ? __ldg(p.slot_pow + slot0 + c * 16 + lane) : 0;
+          const float f1 = pow2f(-(pw >> 1)), f2 = pow2f((pw >> 1) - pw);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float a1 = __shfl_sync(0xffffffffu, f1, j), a2 = __shfl_sync(0xffffffffu, f2, j);
+            const int col = c * 16 + j;
+            if (col < n) {
+              const float gg = stg[(k * 32 + j) * (TM_EPI * 32)] * a1 * a2;
+              const float uu = stg[(k * 32 + 16 + j) * (TM_EPI * 32)] * a1 * a2;
+              const float h = __uint_as_float((uint32_t)f32_to_bf16_bits(situ_fast(gg, uu)) << 16);  // bf16 rounding
+              reinterpret_cast<__half*>(p.out)[(size_t)(slot0 + col) * p.R + row] = __float2half_rn(h * 256.0f);
+            }
+          }
+        }
+      }
     }
   } else {
-    // ------------------------------------------------------------ decode producers (warps 7..14)
-    // The raw bytes of a tile travel in chunks of 4 k-blocks: 128 bytes (one cache line)
-    // of each of the tile's 256 rows, copied by all producer threads with 16-byte
-    // cp.async (eight threads per line) into a ring of RC chunks; 16-byte granules are
-    // XOR-swizzled by row so the decode reads are free of bank conflicts.  A named
-    // barrier per chunk publishes it to all producers.  When a tile starts, its rows
-    // (contiguous bytes per block) are prefetched into L2 in bulk.
+    // ------------------------------------------------------------ decode producers (warps 11..18)
+    // The raw bytes of a tile travel in chunks of CKB k-blocks: CKB * 32 bytes of each of
+    // the tile's 256 rows, copied by all producer threads with 16-byte cp.async into a
+    // ring of RC chunks; 16-byte granules are XOR-swizzled by row so the decode reads are
+    // free of bank conflicts.  A named
+    // barrier per chunk publishes it to all producers.
     // Decode: a warp owns the TMEM lane quarter warp % 4 (32 rows) of one block (warps
-    // 7..10 block 0, 11..14 block 1), a k-block's 64 elements per thread (32 columns).
-    const int pt = threadIdx.x - (3 + TM_BLOCKS + 2) * 32;  // 0..255
+    // 11..14 block 0, 15..18 block 1), a k-block's 64 elements per thread (32 columns).
+    const int pt = threadIdx.x - (3 + TM_EPI) * 32;  // 0..255
     const int qd = warp & 3;
-    const int mb = (warp - (3 + TM_BLOCKS + 2)) >> 2;
+    const int mb = (warp - (3 + TM_EPI)) >> 2;
     const int ri = mb * TM_ROWS + qd * 32 + lane;  // row of the tile (over both blocks)
     const size_t qrow = (size_t)p.K / 2, srow = (size_t)p.K / 32;
-    const int kchunks = kblocks / TM_CHUNK_KB;
+    constexpr int CKB = Lay::CKB, ROWB = Lay::ROWB, GPR = Lay::GPR;
+    // granule c of row r sits at position c ^ swz(r): conflict-free reads of 8 consecutive rows
+    auto swz = [](int r) { return (GPR == 8) ? (r & 7) : ((r >> 1) & 3); };
+    const int kchunks = kblocks / CKB;
     const int my_tiles = (tiles > (int)blockIdx.x) ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int nchunks = my_tiles * kchunks;
     bool stop = false;
@@ -689,24 +773,20 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
         const int tile = blockIdx.x + (jc / kchunks) * gridDim.x, kc = jc % kchunks;
         const MxBatch* rec = p.batches + tile / mtiles;
         const int tm = tile % mtiles;
-        if (kc == 0 && pt < 2 * TM_BLOCKS) {
-          const int mm = pt >> 1;
-          const size_t r0 = blk_row0(tm, mm);
-          if (pt & 1) l2_prefetch_bulk(rec->w[blk_tensor(mm) + 1] + r0 * srow, (uint32_t)(TM_ROWS * srow));
-          else l2_prefetch_bulk(rec->w[blk_tensor(mm)] + r0 * qrow, (uint32_t)(TM_ROWS * qrow));
-        }
         const uint32_t dst = raw_base + (jc % RC) * Lay::RAW_SLOT;
 #pragma unroll
-        for (int k = 0; k < MROWS * 8 / (TM_PRODUCERS * 32); ++k) {
+        for (int k = 0; k < MROWS * GPR / (TM_PRODUCERS * 32); ++k) {
           const int G = k * TM_PRODUCERS * 32 + pt;  // 16-byte granule of the chunk
-          const int rr = G >> 3, gc = G & 7, mm = rr / TM_ROWS;
-          const uint8_t* src = rec->w[blk_tensor(mm)] + (blk_row0(tm, mm) + (rr % TM_ROWS)) * qrow + kc * 128 + gc * 16;
-          cp_async16(dst + rr * 128 + ((gc ^ (rr & 7)) << 4), src);
+          const int rr = G / GPR, gc = G % GPR, mm = rr / TM_ROWS;
+          const uint8_t* src = rec->w[blk_tensor(mm)] + (blk_row0(tm, mm) + (rr % TM_ROWS)) * qrow + kc * ROWB + gc * 16;
+          cp_async16(dst + rr * ROWB + ((gc ^ swz(rr)) << 4), src);
         }
         {
           const int mm = pt / TM_ROWS;
-          cp_async8(sraw_base + (jc % RC) * Lay::SC_SLOT + pt * 8,
-                    rec->w[blk_tensor(mm) + 1] + (blk_row0(tm, mm) + (pt % TM_ROWS)) * srow + kc * 8);
+          const uint8_t* ssrc = rec->w[blk_tensor(mm) + 1] + (blk_row0(tm, mm) + (pt % TM_ROWS)) * srow + kc * (2 * CKB);
+          const uint32_t sdst = sraw_base + (jc % RC) * Lay::SC_SLOT + pt * (2 * CKB);
+          if constexpr (CKB == 4) cp_async8(sdst, ssrc);
+          else cp_async4(sdst, ssrc);
         }
       }
       cp_async_commit();
@@ -723,16 +803,18 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       if (*abort_flag) stop = true;
       issue(jc + RC - 1);       // into the slot chunk jc - 1 used
       if (stop) continue;
-      const uint8_t* src = base_ptr + (raw_base - base) + (jc % RC) * Lay::RAW_SLOT + ri * 128;
-      const uint2 sc8 = *reinterpret_cast<const uint2*>(base_ptr + (sraw_base - base) + (jc % RC) * Lay::SC_SLOT + ri * 8);
-#pragma unroll 1
-      for (int kq = 0; kq < TM_CHUNK_KB; ++kq) {
-        const int i = jc * TM_CHUNK_KB + kq;
+      const uint8_t* src = base_ptr + (raw_base - base) + (jc % RC) * Lay::RAW_SLOT + ri * ROWB;
+      const uint8_t* scs = base_ptr + (sraw_base - base) + (jc % RC) * Lay::SC_SLOT + ri * (2 * CKB);
+      uint2 sc8;
+      if constexpr (CKB == 4) sc8 = *reinterpret_cast<const uint2*>(scs);
+      else sc8 = make_uint2(*reinterpret_cast<const uint32_t*>(scs), 0u);
+      // decode k-block kq of the chunk (64 elements of row ri) into a[]: f16x2 columns
+      uint32_t a[32];
+      auto decode = [&](int kq) {
         const uint32_t cs = ((kq < 2) ? sc8.x : sc8.y) >> (16 * (kq & 1));  // this k-block's two scale bytes
-        uint32_t a[32];
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
-          const uint4 cq = *reinterpret_cast<const uint4*>(src + (((2 * kq + g) ^ (ri & 7)) << 4));
+          const uint4 cq = *reinterpret_cast<const uint4*>(src + (((2 * kq + g) ^ swz(ri)) << 4));
           const uint32_t sc2 = ue8m0_to_f16x2((cs >> (8 * g)) & 0xFFu, bad);
           const uint32_t w4[4] = {cq.x, cq.y, cq.z, cq.w};
 #pragma unroll
@@ -746,17 +828,31 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
             }
           }
         }
-        const int sa = i % SA;
-        if (!__all_sync(0xffffffffu, mbar_wait(emptyA(sa), ((i / SA) & 1) ^ 1, abort_flag))) {
-          stop = true;
-          break;
+      };
+      // a tcgen05.st keeps its source registers until tcgen05.wait::st: decode, store, wait
+#pragma unroll 1
+      for (int h = 0; h < CKB / TM_AKB; ++h) {
+        const int st = jc * (CKB / TM_AKB) + h, sa = st % SA;  // A stage and its slot
+        const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + Lay::A_COL0 + (sa * TM_BLOCKS + mb) * Lay::A_COLS;
+#pragma unroll 1
+        for (int kk = 0; kk < TM_AKB; ++kk) {
+          decode(h * TM_AKB + kk);
+          if (kk == 0) {
+            // the slot's previous stage (st - SA) must have been consumed by the MMAs
+            const int j = st - SA;
+            if (j >= 0 && !__all_sync(0xffffffffu, mbar_wait(kdone(j % NBS), (j / NBS) & 1, abort_flag))) {
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+          }
+          tmem_st32(ta + kk * 32, a);
+          tmem_st_wait();
         }
-        tc_fence_after();
-        tmem_st32(tmem + ((uint32_t)(qd * 32) << 16) + Lay::A_COL0 + (sa * TM_BLOCKS + mb) * 32, a);
-        tmem_st_wait();
+        if (stop) break;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(fullA(sa));
+        if (lane == 0) mbar_arrive(fullA(sa, mb));
       }
     }
     cp_async_wait<0>();
