@@ -480,16 +480,18 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   const PermParams pp = perm_params(d, T, d.top_k, at<int32_t>(ws, L.ids), 0, NB, ws, L, experts);
   const Z16Params zp{at<uint16_t>(ws, L.z), T, d.latent, at<__half>(ws, L.z16), at<int32_t>(ws, L.zpow)};
   K3_TRY(launch_route_tail(tp, pp, zp, dev, s, pdl));
-  K3_TRY(mark(events, n_events, 2, s));
-  // experts
   const int slots = T * d.top_k;
-  if (tc) {
+  if (tc) {  // activation rows in expert-sorted slot order for the grouped GEMM (part of routing)
     const int per = d.latent / 8;
     const int gblocks = (int)(((size_t)slots * per + 255) / 256 < (size_t)sms * 8 ? ((size_t)slots * per + 255) / 256
                                                                                      : (size_t)sms * 8);
     K3_TRY(launch(k3_gather_rows_kernel, dim3(gblocks), dim3(256), 0, s, pdl, (const __half*)at<__half>(ws, L.z16),
                   (const int32_t*)at<int32_t>(ws, L.zpow), (const int32_t*)at<int32_t>(ws, L.slot_tok), slots,
                   (int)d.latent, at<__half>(ws, L.z16p), at<int32_t>(ws, L.spow)));
+  }
+  K3_TRY(mark(events, n_events, 2, s));
+  // experts
+  if (tc) {
     TcMoeParams gp{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.inter, d.latent,
                    at<int32_t>(ws, L.spow), at<void>(ws, L.h16), status};
     K3_TRY(launch_tc_moe<0>(at<__half>(ws, L.z16p), slots, gp, dev, sms, s, pdl));
