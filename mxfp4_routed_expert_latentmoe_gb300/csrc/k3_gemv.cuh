@@ -42,6 +42,7 @@ struct MxGemvParams {
   const __half* act;         // GATEUP: z16 [T, K]; DOWN: h16 [slots, K]
   const int32_t* act_pow;    // GATEUP: per-token exponent p (z16 = z * 2^p)
   void* out;                 // GATEUP: h16 [slots, R] (h * 2^8); DOWN: o f32 [slots, R]
+  uint32_t* status;          // device status word (bounded waits of the bulk-copy kernel)
 };
 
 template <int M, int STAGES>

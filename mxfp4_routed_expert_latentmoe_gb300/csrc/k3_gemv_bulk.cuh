@@ -1,0 +1,312 @@
+// k3_gemv_bulk.cuh -- MXFP4 weight-streaming GEMV with bulk (TMA engine) copies, for
+// small token counts per expert (decode, chunked prefill) when K is a multiple of 256.
+//
+// Same arithmetic as k3_mx_gemv_kernel (k3_gemv.cuh): item = 16 rows of one matrix
+// (gate and up together for GATEUP) x one batch of up to 8 * NBLK tokens; K split into
+// 256-element slices, one per compute warp; each 32-element scale group is decoded with
+// cvt.rn.f16x2.e2m1x2, multiplied on the tensor core (m16n8k16, f16 in, fp32 out) and
+// folded into the fp32 accumulator with the group's power-of-two scale.
+//
+// What differs is how bytes move and how partial sums meet:
+//   warp 0       producer: the item's 16 rows are contiguous in each matrix; lanes
+//                0..7 (and 8..15 for the up matrix) each issue one cp.async.bulk of a
+//                pair of rows into shared memory, pairs padded by 16 bytes (the fragment
+//                reads of 8 rows then meet at most 2-way bank conflicts), plus one bulk
+//                copy of the 16 rows' scale bytes per matrix; completion is counted in
+//                bytes on the stage's mbarrier.  The copies run on the TMA engine, so the
+//                bytes in flight are not limited by per-warp load queues; the engine takes
+//                about one copy instruction per ~100 cycles, hence pairs of rows (measured
+//                per item: 34 single-row copies took ~3300 cycles);
+//   warp 1       reducer: adds the compute warps' partial sums in warp order
+//                (deterministic), applies the epilogue (SiTU-GLU for GATEUP) and stores;
+//   warps 2..    compute: one 256-element K slice each.
+// Stages (STAGES deep), partial-sum buffers (2) and their hand-offs are mbarriers; no
+// block-wide barrier is taken per item.  Every wait is bounded (about 2^32 cycles, with a
+// per-CTA abort flag): a wait that runs out sets K3MOE_DEV_TIMEOUT and all roles drain
+// their issued copies and return.
+#pragma once
+
+#include "k3_common.cuh"
+#include "k3_gemv.cuh"
+#include "k3_tc.cuh"
+
+namespace k3 {
+
+constexpr int MXB_MAX_WARPS = 14;  // compute warps: K <= 3584 (larger K uses k3_mx_gemv_kernel)
+
+K3_DEVI void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+template <int MODE>
+struct MxbLayout {
+  static constexpr int M = (MODE == MX_GATEUP) ? 2 : 1;
+  // per stage: M x (8 padded row pairs + 16 rows of scale bytes), then the 128-byte batch record
+  __host__ __device__ static constexpr int pair_stride(int K) { return K + 16; }
+  __host__ __device__ static constexpr int mat_bytes(int K) { return (MX_ROWS / 2) * pair_stride(K) + MX_ROWS * (K / 32); }
+  __host__ __device__ static constexpr int stage_bytes(int K) { return M * mat_bytes(K) + 128; }
+  __host__ __device__ static constexpr int red_floats(int W, int nblk) { return W * M * nblk * 128; }
+  static constexpr int META = 48;  // ints per partial-sum buffer: slot0, n, row0, tok[16], pow[16]
+  __host__ __device__ static constexpr int smem_bytes(int K, int stages, int nblk) {
+    return 128 + stages * stage_bytes(K) + 2 * red_floats(K / 256, nblk) * 4 + 2 * META * 4 + 256;
+  }
+};
+
+// PRE: the first stages' weight copies are issued before waiting for the previous kernel
+// (programmatic dependent launch); valid when the batch records were written at least
+// two kernels earlier.
+template <int MODE, int NBLK, int STAGES, bool PRE>
+__global__ void __launch_bounds__((2 + MXB_MAX_WARPS) * 32) k3_mxb_gemv_kernel(MxGemvParams p) {
+  using Lay = MxbLayout<MODE>;
+  constexpr int M = Lay::M;
+  constexpr int RED = M * NBLK * 128;  // floats of one warp's partial sums
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ int abort_sh;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int W = (int)(blockDim.x >> 5) - 2;  // compute warps (K / 256)
+  const int K = p.K, PS = Lay::pair_stride(K), MB = Lay::mat_bytes(K), SB = Lay::stage_bytes(K);
+  const uint32_t base = (smem_u32(smem_raw) + 127u) & ~127u;
+  uint8_t* base_ptr = smem_raw + (base - smem_u32(smem_raw));
+  const uint32_t red_s = base + STAGES * SB;  // [2][W][RED] f32
+  float* red = reinterpret_cast<float*>(base_ptr + STAGES * SB);
+  int* meta = reinterpret_cast<int*>(base_ptr + STAGES * SB + 2 * W * RED * 4);  // [2][META]
+  const uint32_t bars = red_s + 2 * W * RED * 4 + 2 * Lay::META * 4;
+  auto full = [&](int s) { return bars + 8 * s; };
+  auto empty = [&](int s) { return bars + 8 * (STAGES + s); };
+  auto rfull = [&](int b) { return bars + 8 * (2 * STAGES + b); };
+  auto rempty = [&](int b) { return bars + 8 * (2 * STAGES + 2 + b); };
+  volatile int* abort_flag = &abort_sh;
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), W);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(rfull(b), W);
+      mbar_init(rempty(b), 1);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const int tiles = p.R / MX_ROWS;
+  const size_t qrow = (size_t)K / 2, srow = (size_t)K / 32;
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (!PRE) grid_dep_wait();
+    const int total = tiles * (*p.n_batches);
+    const int n_mine = (total > (int)blockIdx.x) ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    constexpr int WOFF = (MODE == MX_GATEUP) ? 0 : 4;
+    // lanes 0..5 hold the six tensor pointers of the item's batch record, loaded one
+    // item ahead so the copies are not held up by the record's latency
+    auto rec_word = [&](int s2) -> uint64_t {
+      if (s2 >= n_mine || lane >= 6) return 0ull;
+      return reinterpret_cast<const uint64_t*>(p.batches + (blockIdx.x + s2 * gridDim.x) / tiles)[lane];
+    };
+    uint64_t wnext = rec_word(0);
+    int s = 0;
+    for (; s < n_mine; ++s) {
+      if (PRE && s == STAGES) grid_dep_wait();
+      const int st = s % STAGES;
+      const uint64_t wcur = wnext;
+      wnext = rec_word(s + 1);
+      if (!__all_sync(0xffffffffu, mbar_wait(empty(st), ((s / STAGES) & 1) ^ 1, abort_flag))) break;
+      const int i = blockIdx.x + s * gridDim.x;
+      const MxBatch* rec = p.batches + i / tiles;
+      const size_t row0 = (size_t)(i % tiles) * MX_ROWS;
+      const uint32_t sbase = base + st * SB;
+      if (lane == 0) mbar_expect_tx(full(st), (uint32_t)(M * MX_ROWS * (qrow + srow) + 128));
+      __syncwarp();
+      const int mq = (lane < 8 * M) ? (lane >> 3) : ((lane >= 16 && lane < 16 + M) ? lane - 16 : 0);
+      const uint8_t* qptr = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, wcur, WOFF + 2 * mq));
+      const uint8_t* sptr = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, wcur, WOFF + 2 * mq + 1));
+      if (lane < 8 * M) {  // row pair lane & 7 of matrix lane >> 3
+        const int pr = lane & 7;
+        bulk_g2s(sbase + mq * MB + pr * PS, qptr + (row0 + 2 * pr) * qrow, (uint32_t)(2 * qrow), full(st));
+      } else if (lane >= 16 && lane < 16 + M) {  // scale bytes of matrix lane - 16
+        bulk_g2s(sbase + mq * MB + (MX_ROWS / 2) * PS, sptr + row0 * srow, (uint32_t)(MX_ROWS * srow), full(st));
+      }
+      if (lane == 31) bulk_g2s(sbase + M * MB, rec, 128, full(st));
+    }
+    if (PRE && s < STAGES) grid_dep_wait();
+    grid_dep_launch();
+    // drain: every issued stage must land before the CTA exits
+    for (int t = (s > STAGES ? s - STAGES : 0); t < s; ++t) {
+      volatile int never = 0;
+      mbar_wait(full(t % STAGES), (t / STAGES) & 1, &never);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ reducer + epilogue
+    grid_dep_wait();
+    grid_dep_launch();
+    const int total = tiles * (*p.n_batches);
+    const int n_mine = (total > (int)blockIdx.x) ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    for (int s = 0; s < n_mine; ++s) {
+      const int b = s & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(rfull(b), (s >> 1) & 1, abort_flag))) break;
+      const int* mt = meta + b * Lay::META;
+      const int slot0 = mt[0], n = mt[1], row0 = mt[2];
+      const float* rs = red + b * W * RED;
+      for (int idx = lane; idx < MX_ROWS * n; idx += 32) {
+        const int row = idx & 15, col = idx >> 4, nb = col >> 3, cc = col & 7;
+        float v[M];
+#pragma unroll
+        for (int mm = 0; mm < M; ++mm) {
+          float sum = 0.f;
+#pragma unroll 6
+          for (int w = 0; w < W; ++w) sum += rs[w * RED + (mm * NBLK + nb) * 128 + row * 8 + cc];
+          v[mm] = sum;
+        }
+        const int slot = slot0 + col;
+        if (MODE == MX_GATEUP) {
+          const int pw = mt[19 + col];
+          const float f1 = pow2f(-(pw >> 1)), f2 = pow2f((pw >> 1) - pw);  // exact 2^-p
+          const float gg = v[0] * f1 * f2, uu = v[M - 1] * f1 * f2;
+          const float h = __uint_as_float((uint32_t)f32_to_bf16_bits(situ_fast(gg, uu)) << 16);  // bf16 rounding
+          reinterpret_cast<__half*>(p.out)[(size_t)slot * p.R + row0 + row] = __float2half_rn(h * 256.0f);
+        } else {
+          reinterpret_cast<float*>(p.out)[(size_t)slot * p.R + row0 + row] = v[0] * (1.0f / 256.0f);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rempty(b));
+    }
+  } else {
+    // ------------------------------------------------------------ compute warps
+    const int c = warp - 2;  // K slice
+    const int g = lane >> 2, t = lane & 3;
+    grid_dep_wait();
+    grid_dep_launch();
+    const int total = tiles * (*p.n_batches);
+    const int n_mine = (total > (int)blockIdx.x) ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    // single-token batches keep this warp's activation fragments in registers while
+    // consecutive items use the same activation row (GATEUP: the same token; DOWN: the
+    // same slot, i.e. the same batch)
+    constexpr bool CACHE_B = (NBLK == 1);
+    uint4 bcache[CACHE_B ? MX_GPW : 1];
+    int bkey = -1;
+    for (int s = 0; s < n_mine; ++s) {
+      const int st = s % STAGES;
+      if (!__all_sync(0xffffffffu, mbar_wait(full(st), (s / STAGES) & 1, abort_flag))) break;
+      const uint8_t* stp = base_ptr + st * SB;
+      const MxBatch* rec = reinterpret_cast<const MxBatch*>(stp + M * MB);
+      const int slot0 = rec->slot0, n = rec->n;
+      // warp 0 passes the item's bookkeeping to the reducer (fetched now, stored with the
+      // partial sums): token ids and, for GATEUP, their activation exponents
+      int my_tok = 0, my_pow = 0;
+      if (c == 0 && lane < n) {
+        my_tok = rec->tok[lane];
+        if (MODE == MX_GATEUP) my_pow = p.act_pow[my_tok];
+      }
+
+      float acc[M][NBLK][4];
+#pragma unroll
+      for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int nb = 0; nb < NBLK; ++nb)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[m][nb][q] = 0.f;
+      // activation row of this lane's token column in every 8-token block (columns past
+      // the batch repeat its last token: their results are never stored)
+      const __half* bptr[NBLK];
+#pragma unroll
+      for (int nb = 0; nb < NBLK; ++nb) {
+        const int col = min(nb * 8 + g, n - 1);
+        const int row = (MODE == MX_GATEUP) ? rec->tok[col] : slot0 + col;
+        bptr[nb] = p.act + (size_t)row * K + c * 256 + 8 * t;
+      }
+      if (CACHE_B) {
+        const int key = (n == 1) ? ((MODE == MX_GATEUP) ? rec->tok[0] : slot0) : -1;
+        if (key < 0 || key != bkey) {
+#pragma unroll
+          for (int j = 0; j < MX_GPW; ++j) bcache[CACHE_B ? j : 0] = ldg128(bptr[0] + 32 * j);
+          bkey = key;
+        }
+      }
+      uint2 sc_lo[M], sc_hi[M];
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const uint8_t* ss = stp + m * MB + (MX_ROWS / 2) * PS + c * MX_GPW;
+        sc_lo[m] = *reinterpret_cast<const uint2*>(ss + g * srow);
+        sc_hi[m] = *reinterpret_cast<const uint2*>(ss + (g + 8) * srow);
+      }
+#pragma unroll
+      for (int j = 0; j < MX_GPW; ++j) {
+        uint32_t a0[M][4], a1[M][4];
+        float slo[M], shi[M];
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          // row r sits at pair r / 2, half r % 2
+          const uint8_t* sq = stp + m * MB + c * 128 + j * 16 + 4 * t + (g >> 1) * PS + (g & 1) * (K / 2);
+          const uint32_t wlo = *reinterpret_cast<const uint32_t*>(sq);
+          const uint32_t whi = *reinterpret_cast<const uint32_t*>(sq + 4 * PS);
+          uint32_t plo[4], phi[4];
+          e2m1x8_to_f16x8(wlo, plo);
+          e2m1x8_to_f16x8(whi, phi);
+          // K order inside the group: this thread's 8 elements 8t..8t+7 feed MMA 0 slots
+          // {2t,2t+1 | 2t+8,2t+9} = elements {8t,8t+1 | 8t+2,8t+3} and MMA 1 the same
+          // slots with elements {8t+4,8t+5 | 8t+6,8t+7}
+          a0[m][0] = plo[0]; a0[m][1] = phi[0]; a0[m][2] = plo[1]; a0[m][3] = phi[1];
+          a1[m][0] = plo[2]; a1[m][1] = phi[2]; a1[m][2] = plo[3]; a1[m][3] = phi[3];
+          const uint32_t blo = (j < 4) ? sc_lo[m].x : sc_lo[m].y;
+          const uint32_t bhi = (j < 4) ? sc_hi[m].x : sc_hi[m].y;
+          if ((j & 3) == 0) { slo[m] = ue8m0_byte_to_f32<0>(blo); shi[m] = ue8m0_byte_to_f32<0>(bhi); }
+          if ((j & 3) == 1) { slo[m] = ue8m0_byte_to_f32<1>(blo); shi[m] = ue8m0_byte_to_f32<1>(bhi); }
+          if ((j & 3) == 2) { slo[m] = ue8m0_byte_to_f32<2>(blo); shi[m] = ue8m0_byte_to_f32<2>(bhi); }
+          if ((j & 3) == 3) { slo[m] = ue8m0_byte_to_f32<3>(blo); shi[m] = ue8m0_byte_to_f32<3>(bhi); }
+        }
+#pragma unroll
+        for (int nb = 0; nb < NBLK; ++nb) {
+          if (NBLK == 1 || nb * 8 < n) {
+            const uint4 bv = CACHE_B ? bcache[CACHE_B ? j : 0] : ldg128(bptr[nb] + 32 * j);
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+              const float z4[4] = {0.f, 0.f, 0.f, 0.f};
+              float d[4];
+              mma_f16(d, a0[m], bv.x, bv.y, z4);
+              mma_f16(d, a1[m], bv.z, bv.w, d);
+              ffma2(acc[m][nb][0], acc[m][nb][1], d[0], d[1], slo[m], acc[m][nb][0], acc[m][nb][1]);
+              ffma2(acc[m][nb][2], acc[m][nb][3], d[2], d[3], shi[m], acc[m][nb][2], acc[m][nb][3]);
+            }
+          }
+        }
+      }
+      // the stage's bytes are consumed: hand it back to the producer
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(st));
+      // partial sums -> red[s & 1][c][m][nb][row 16][col 8] once the reducer released it
+      const int b = s & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(rempty(b), ((s >> 1) & 1) ^ 1, abort_flag))) break;
+      float* rb = red + (b * W + c) * RED;
+      if (c == 0) {
+        int* mt = meta + b * Lay::META;
+        if (lane == 0) {
+          mt[0] = slot0;
+          mt[1] = n;
+          mt[2] = ((blockIdx.x + s * gridDim.x) % tiles) * MX_ROWS;
+        }
+        if (lane < n) {
+          mt[3 + lane] = my_tok;
+          mt[19 + lane] = my_pow;
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int nb = 0; nb < NBLK; ++nb) {
+          float* r = rb + (m * NBLK + nb) * 128;
+          *reinterpret_cast<float2*>(r + g * 8 + 2 * t) = make_float2(acc[m][nb][0], acc[m][nb][1]);
+          *reinterpret_cast<float2*>(r + (g + 8) * 8 + 2 * t) = make_float2(acc[m][nb][2], acc[m][nb][3]);
+        }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rfull(b));
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) flag_status(p.status, K3MOE_DEV_TIMEOUT);
+}
+
+}  // namespace k3

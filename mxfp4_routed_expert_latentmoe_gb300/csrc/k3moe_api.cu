@@ -7,6 +7,7 @@
 
 #include "k3_common.cuh"
 #include "k3_gemv.cuh"
+#include "k3_gemv_bulk.cuh"
 #include "k3_route.cuh"
 #include "k3_tc.cuh"
 
@@ -283,8 +284,31 @@ cudaError_t launch_mx_t(const MxGemvParams& p, int dev, int sms, cudaStream_t st
   return cudaErrorInvalidValue;
 }
 
+// bulk-copy GEMV: one CTA per SM, K / 256 compute warps + producer + reducer
+template <int MODE, int NBLK, int STAGES>
+cudaError_t launch_mxb(const MxGemvParams& p, int dev, int sms, cudaStream_t st, bool pdl) {
+  constexpr bool PRE = MODE == MX_DOWN;  // its batches were written two kernels earlier
+  const int smem = MxbLayout<MODE>::smem_bytes(p.K, STAGES, NBLK);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  if (!set_smem<k3_mxb_gemv_kernel<MODE, NBLK, STAGES, PRE>>(dev, smem)) return cudaErrorInvalidValue;
+  // two CTAs per SM where shared memory and registers allow (more warps to hide the
+  // per-item latency of the compute warps)
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, k3_mxb_gemv_kernel<MODE, NBLK, STAGES, PRE>) != cudaSuccess) return cudaErrorInvalidValue;
+  const int threads = (2 + p.K / 256) * 32;
+  const bool two = 2 * (smem + 2048) <= 228 * 1024 && 2 * threads * fa.numRegs <= 65536;
+  return launch(k3_mxb_gemv_kernel<MODE, NBLK, STAGES, PRE>, dim3(two ? 2 * sms : sms), dim3(threads), smem, st, pdl,
+                p);
+}
+
 template <int MODE>
 cudaError_t launch_mx(const MxGemvParams& p, int nblk, int dev, int sms, cudaStream_t st, bool pdl) {
+  if (p.K % 256 == 0 && p.K / 256 <= MXB_MAX_WARPS) {
+    if constexpr (MODE == MX_GATEUP)
+      return nblk == 1 ? launch_mxb<MODE, 1, 3>(p, dev, sms, st, pdl) : launch_mxb<MODE, 2, 2>(p, dev, sms, st, pdl);
+    else
+      return nblk == 1 ? launch_mxb<MODE, 1, 3>(p, dev, sms, st, pdl) : launch_mxb<MODE, 2, 6>(p, dev, sms, st, pdl);
+  }
   return nblk == 1 ? launch_mx_t<MODE, 1>(p, dev, sms, st, pdl) : launch_mx_t<MODE, 2>(p, dev, sms, st, pdl);
 }
 
@@ -366,6 +390,7 @@ PermParams perm_params(const k3moe_dims& d, int T, int K, const int32_t* ids, in
 
 MxGemvParams mx_params(const k3moe_dims& d, const WsLayout& L, void* ws, int mode, const __half* act, void* out) {
   MxGemvParams p{};
+  p.status = at<uint32_t>(ws, L.status);
   if (mode == MX_GATEUP) {
     p.R = d.inter;
     p.K = d.latent;
