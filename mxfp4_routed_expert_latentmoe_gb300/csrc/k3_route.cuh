@@ -9,7 +9,8 @@ namespace k3 {
 // ============================================================================ top-k
 // One warp per token.  Sigmoid scores and biased scores in fp32 from fp32 logits;
 // the K + REFINE_EXTRA best candidates by biased score are picked (ties to the lower
-// id); every candidate whose biased score lies within `tau` of a neighbour, in a
+// id) by a bitwise search for the threshold key (one warp-wide count per bit), ballot
+// compaction and a warp sort; every candidate whose biased score lies within `tau` of a neighbour, in a
 // near-tie cluster that reaches the top K + 1, gets its logit recomputed exactly in
 // fp64 from the bf16 inputs; candidates are then ranked on the refined values.
 // The ranking compares 64-bit integer images of the (exact) double values: the fp64
@@ -63,76 +64,140 @@ K3_DEVI long long order_key(uint64_t bits) { return (long long)(bits ^ ((uint64_
 // e = lane + 32 i in registers; a tournament over the lanes' heads (warp argmax by
 // shuffles) picks the next candidate, the winning lane pops its head, and rescans
 // its experts only when its three are used up.
-K3_DEVI bool topk_better(float va, int ia, float vb, int ib) { return va > vb || (va == vb && ia < ib); }
+// monotone map of a float onto uint32 (larger float -> larger key), and back
+K3_DEVI uint32_t f32_order(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+K3_DEVI float f32_from_order(uint32_t k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k); }
 
-K3_DEVI void topk_lane_top3(const float* sb, int E, int lane, float (&v)[3], int (&id)[3]) {
+// candidate selection with each lane's keys in registers (E <= 32 KPL): every load is
+// issued before any arithmetic, and the per-bit counts run on registers
+template <int KPL>
+K3_DEVI void topk_select(const TopkParams& p, int t, TopkScratch& S, int lane, int P) {
+  // keys of the biased scores (NaN ranks last, as -inf; -0 counts as +0); all loads first
+  float lg[KPL], bs[KPL];
 #pragma unroll
-  for (int k = 0; k < 3; ++k) {
-    v[k] = -INFINITY;
-    id[k] = 0x7fffffff;
+  for (int j = 0; j < KPL; ++j) {
+    const int e = lane + 32 * j;
+    lg[j] = (e < p.E) ? __ldg(p.logits + (size_t)t * p.E + e) : 0.f;
+    bs[j] = (e < p.E) ? __ldg(p.bias + e) : 0.f;
   }
-  for (int e = lane; e < E; e += 32) {
-    const float x = sb[e];
-    if (x != x) continue;  // taken
-    if (topk_better(x, e, v[2], id[2])) {
-      if (topk_better(x, e, v[1], id[1])) {
-        v[2] = v[1]; id[2] = id[1];
-        if (topk_better(x, e, v[0], id[0])) {
-          v[1] = v[0]; id[1] = id[0];
-          v[0] = x; id[0] = e;
-        } else {
-          v[1] = x; id[1] = e;
-        }
-      } else {
-        v[2] = x; id[2] = e;
-      }
+  uint32_t kr[KPL];
+  uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
+#pragma unroll
+  for (int j = 0; j < KPL; ++j) {
+    const float v = sigmoidf_(lg[j]) + bs[j];
+    kr[j] = (lane + 32 * j < p.E) ? f32_order((v == v) ? v + 0.0f : -INFINITY) : 0u;  // 0: below every key
+    if (lane + 32 * j < p.E) {
+      kmax = max(kmax, kr[j]);
+      kmin = min(kmin, kr[j]);
+    }
+  }
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  // the P-th largest key, bit by bit from the most significant bit in which keys differ
+  // (one warp-wide count per bit)
+  const uint32_t diff = kmax ^ kmin;
+  uint32_t thr = diff ? (kmax & ~((2u << (31 - __clz(diff))) - 1u)) : kmax;
+  for (int bit = diff ? 31 - __clz(diff) : -1; bit >= 0; --bit) {
+    const uint32_t cand = thr | (1u << bit);
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) c += (kr[j] >= cand) ? 1 : 0;
+    if ((int)__reduce_add_sync(0xffffffffu, (uint32_t)c) >= P) thr = cand;
+  }
+  // candidates: every key above the threshold, then keys equal to it in id order until P
+  // (equal keys rank by lower id), compacted with ballots in id order
+  int nsel = 0;
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll
+    for (int j = 0; j < KPL; ++j) {
+      const int e = lane + 32 * j;
+      const bool q = (e < p.E) && (pass == 0 ? (kr[j] > thr) : (kr[j] == thr));
+      const unsigned m = __ballot_sync(0xffffffffu, q);
+      const int pos = nsel + __popc(m & ((1u << lane) - 1u));
+      if (q && pos < P) S.key[pos] = (long long)(((uint64_t)kr[j] << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e));
+      nsel = min(P, nsel + __popc(m));
+    }
+  }
+}
+
+// the same selection for E > 1024, keys kept in shared memory (kh: E words)
+K3_DEVI void topk_select_smem(const TopkParams& p, int t, uint32_t* kh, TopkScratch& S, int lane, int P) {
+  uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
+  for (int e = lane; e < p.E; e += 32) {
+    const float v = sigmoidf_(__ldg(p.logits + (size_t)t * p.E + e)) + __ldg(p.bias + e);
+    const uint32_t k = f32_order((v == v) ? v + 0.0f : -INFINITY);
+    kh[e] = k;
+    kmax = max(kmax, k);
+    kmin = min(kmin, k);
+  }
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  __syncwarp();
+  const uint32_t diff = kmax ^ kmin;
+  uint32_t thr = diff ? (kmax & ~((2u << (31 - __clz(diff))) - 1u)) : kmax;
+  for (int bit = diff ? 31 - __clz(diff) : -1; bit >= 0; --bit) {
+    const uint32_t cand = thr | (1u << bit);
+    int c = 0;
+    for (int e = lane; e < p.E; e += 32) c += (kh[e] >= cand) ? 1 : 0;
+    if ((int)__reduce_add_sync(0xffffffffu, (uint32_t)c) >= P) thr = cand;
+  }
+  int nsel = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int e0 = 0; e0 < p.E && nsel < P; e0 += 32) {
+      const int e = e0 + lane;
+      const uint32_t k = (e < p.E) ? kh[e] : 0u;
+      const bool q = (e < p.E) && (pass == 0 ? (k > thr) : (k == thr));
+      const unsigned m = __ballot_sync(0xffffffffu, q);
+      const int pos = nsel + __popc(m & ((1u << lane) - 1u));
+      if (q && pos < P) S.key[pos] = (long long)(((uint64_t)k << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e));
+      nsel = min(P, nsel + __popc(m));
     }
   }
 }
 
 K3_DEVI void topk_token(const TopkParams& p, int t, float* sb, float* sr, TopkScratch& S, int lane) {
-  // sb: NaN marks an expert already taken; a NaN score ranks last (-inf)
-  for (int e = lane; e < p.E; e += 32) {
-    const float s = sigmoidf_(p.logits[(size_t)t * p.E + e]);
-    const float v = s + p.bias[e];
-    sr[e] = s;
-    sb[e] = (v == v) ? v : -INFINITY;
+  (void)sr;
+  const int P = min(p.E, p.K + REFINE_EXTRA);
+  if (p.E <= 1024) topk_select<32>(p, t, S, lane, P);
+  else topk_select_smem(p, t, reinterpret_cast<uint32_t*>(sb), S, lane, P);
+  __syncwarp();
+  // order the P candidates by (score desc, id asc) = key desc: bitonic sort in the warp
+  // for P <= 32, else a selection sort by lane 0 (top-k above 24 only)
+  if (P <= 32) {
+    uint64_t v = (lane < P) ? (uint64_t)S.key[lane] : 0ull;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const uint64_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+        const bool desc = ((lane & size) == 0);
+        const bool lower = ((lane & stride) == 0);
+        const bool take = (lower == desc) ? (o > v) : (o < v);
+        if (take) v = o;
+      }
+    }
+    if (lane < P) S.key[lane] = (long long)v;
+  } else if (lane == 0) {
+    for (int a2 = 0; a2 < P; ++a2) {
+      int b2 = a2;
+      for (int c2 = a2 + 1; c2 < P; ++c2)
+        if ((uint64_t)S.key[c2] > (uint64_t)S.key[b2]) b2 = c2;
+      const long long tk = S.key[a2]; S.key[a2] = S.key[b2]; S.key[b2] = tk;
+    }
   }
   __syncwarp();
-  const int P = min(p.E, p.K + REFINE_EXTRA);
-  float hv[3];
-  int hi[3];
-  topk_lane_top3(sb, p.E, lane, hv, hi);
-  int used = 0;  // entries of this lane's top-3 already taken
-  for (int k = 0; k < P; ++k) {
-    float best = hv[0];
-    int bid = hi[0];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, best, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bid, off);
-      if (topk_better(ov, oi, best, bid)) {
-        best = ov;
-        bid = oi;
-      }
-    }
-    if (lane == 0) {
-      S.cv[k] = best;
-      S.ci[k] = bid;
-      S.cs[k] = sr[bid];
-    }
-    if (hi[0] == bid) {  // this lane owned the winner: pop it
-      sb[bid] = __int_as_float(0x7fc00000);
-      hv[0] = hv[1]; hi[0] = hi[1];
-      hv[1] = hv[2]; hi[1] = hi[2];
-      hv[2] = -INFINITY; hi[2] = 0x7fffffff;
-      if (++used == 3) {
-        topk_lane_top3(sb, p.E, lane, hv, hi);
-        used = 0;
-      }
-    }
-    __syncwarp();
+  for (int k = lane; k < P; k += 32) {
+    const uint64_t key = (uint64_t)S.key[k];
+    const int id = (int)(0xFFFFFFFFu - (uint32_t)key);
+    S.cv[k] = f32_from_order((uint32_t)(key >> 32));
+    S.ci[k] = id;
+    S.cs[k] = sigmoidf_(__ldg(p.logits + (size_t)t * p.E + id));
   }
+  __syncwarp();
   // near-tie clusters: consecutive candidates closer than tau are linked; a cluster
   // is refined when it starts at or before position K (it can change the top K or
   // their order)
