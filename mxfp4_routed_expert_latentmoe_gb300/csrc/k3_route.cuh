@@ -87,7 +87,8 @@ K3_DEVI void topk_select(const TopkParams& p, int t, TopkScratch& S, int lane, i
   uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
 #pragma unroll
   for (int j = 0; j < KPL; ++j) {
-    const float v = sigmoidf_(lg[j]) + bs[j];
+    // ranking keys only: a few-ulp sigmoid (near ties below tau are re-ranked in fp64)
+    const float v = __fdividef(1.0f, 1.0f + __expf(-lg[j])) + bs[j];
     kr[j] = (lane + 32 * j < p.E) ? f32_order((v == v) ? v + 0.0f : -INFINITY) : 0u;  // 0: below every key
     if (lane + 32 * j < p.E) {
       kmax = max(kmax, kr[j]);
@@ -102,10 +103,10 @@ K3_DEVI void topk_select(const TopkParams& p, int t, TopkScratch& S, int lane, i
   uint32_t thr = diff ? (kmax & ~((2u << (31 - __clz(diff))) - 1u)) : kmax;
   for (int bit = diff ? 31 - __clz(diff) : -1; bit >= 0; --bit) {
     const uint32_t cand = thr | (1u << bit);
-    int c = 0;
+    int c[4] = {0, 0, 0, 0};  // independent partial counts (short dependency chains)
 #pragma unroll
-    for (int j = 0; j < KPL; ++j) c += (kr[j] >= cand) ? 1 : 0;
-    if ((int)__reduce_add_sync(0xffffffffu, (uint32_t)c) >= P) thr = cand;
+    for (int j = 0; j < KPL; ++j) c[j & 3] += (kr[j] >= cand) ? 1 : 0;
+    if ((int)__reduce_add_sync(0xffffffffu, (uint32_t)(c[0] + c[1] + c[2] + c[3])) >= P) thr = cand;
   }
   // candidates: every key above the threshold, then keys equal to it in id order until P
   // (equal keys rank by lower id), compacted with ballots in id order
@@ -159,6 +160,75 @@ K3_DEVI void topk_select_smem(const TopkParams& p, int t, uint32_t* kh, TopkScra
   }
 }
 
+// Everything after the candidate sort, for P <= 32, with candidate k in lane k's
+// registers: near-tie clusters (neighbours by shuffles), fp64 refinement of the flagged
+// candidates, re-ranking when any was refined, weights, stores.
+K3_DEVI void topk_finish_warp(const TopkParams& p, int t, uint64_t key, int lane, int P) {
+  const bool in = lane < P;
+  int id = in ? (int)(0xFFFFFFFFu - (uint32_t)key) : 0x7fffffff;
+  const float cv = f32_from_order((uint32_t)(key >> 32));
+  float cs = in ? sigmoidf_(__ldg(p.logits + (size_t)t * p.E + id)) : 0.f;  // the weight's score
+  const float cv_prev = __shfl_up_sync(0xffffffffu, cv, 1);
+  const float cv_next = __shfl_down_sync(0xffffffffu, cv, 1);
+  const bool linked_prev = in && lane > 0 && (cv_prev - cv) < p.tau;
+  const bool linked_next = in && lane + 1 < P && (cv - cv_next) < p.tau;
+  // a cluster starts at an unlinked position; it is refined when it starts at or before K
+  const unsigned unl = __ballot_sync(0xffffffffu, in && !linked_prev);
+  const unsigned le = unl & ((2u << lane) - 1u);
+  const int start = le ? 31 - __clz(le) : 0;
+  const unsigned rmask = __ballot_sync(0xffffffffu, in && (linked_prev || linked_next) && start <= p.K);
+  if (lane == 0 && P < p.E && ((rmask >> (P - 1)) & 1u)) flag_status(p.status, K3MOE_DEV_TIE_WINDOW);
+  if (rmask) {
+    long long rkey = in ? order_key(f32_as_f64_bits(cv)) : LLONG_MIN;
+    for (unsigned m = rmask; m; m &= m - 1u) {
+      const int k = __ffs(m) - 1;
+      const int e = __shfl_sync(0xffffffffu, id, k);
+      double acc = 0.0;
+      const uint16_t* xr = p.x + (size_t)t * p.H;
+      const uint16_t* wrr = p.wr + (size_t)e * p.H;
+      for (int h = lane; h < p.H; h += 32)
+        acc = fma((double)bf16_bits_to_f32(xr[h]), (double)bf16_bits_to_f32(wrr[h]), acc);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (lane == k) {
+        const double s = 1.0 / (1.0 + exp(-acc));
+        cs = (float)s;
+        rkey = order_key((uint64_t)__double_as_longlong(s + (double)p.bias[e]));
+      }
+    }
+    // re-rank by (refined key desc, id asc): bitonic network carrying the score
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const long long ok = __shfl_xor_sync(0xffffffffu, rkey, stride);
+        const int oi = __shfl_xor_sync(0xffffffffu, id, stride);
+        const float os = __shfl_xor_sync(0xffffffffu, cs, stride);
+        const bool o_better = ok > rkey || (ok == rkey && oi < id);
+        const bool desc = ((lane & size) == 0);
+        const bool lower = ((lane & stride) == 0);
+        if ((lower == desc) ? o_better : !o_better) {
+          rkey = ok;
+          id = oi;
+          cs = os;
+        }
+      }
+    }
+  }
+  // weights of the first K: a fixed butterfly sum (the same on every lane), then w = s / sum
+  float sum = (lane < p.K) ? cs : 0.f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane < p.K) {
+    const float wk = cs / sum;
+    p.ids[(size_t)t * p.K + lane] = id;
+    p.w[(size_t)t * p.K + lane] = wk;
+    if (p.ids_out) p.ids_out[(size_t)t * p.K + lane] = id;
+    if (p.w_out) p.w_out[(size_t)t * p.K + lane] = wk;
+  }
+  __syncwarp();
+}
+
 K3_DEVI void topk_token(const TopkParams& p, int t, float* sb, float* sr, TopkScratch& S, int lane) {
   (void)sr;
   const int P = min(p.E, p.K + REFINE_EXTRA);
@@ -180,7 +250,8 @@ K3_DEVI void topk_token(const TopkParams& p, int t, float* sb, float* sr, TopkSc
         if (take) v = o;
       }
     }
-    if (lane < P) S.key[lane] = (long long)v;
+    topk_finish_warp(p, t, v, lane, P);
+    return;
   } else if (lane == 0) {
     for (int a2 = 0; a2 < P; ++a2) {
       int b2 = a2;
