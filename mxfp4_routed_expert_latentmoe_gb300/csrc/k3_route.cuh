@@ -11,8 +11,8 @@ namespace k3 {
 // the K + REFINE_EXTRA best candidates by biased score are picked (ties to the lower
 // id) by a bitwise search for the threshold key (one warp-wide count per bit), ballot
 // compaction and a warp sort; every candidate whose biased score lies within `tau` of a neighbour, in a
-// near-tie cluster that reaches the top K + 1, gets its logit recomputed exactly in
-// fp64 from the bf16 inputs; candidates are then ranked on the refined values.
+// near-tie cluster that reaches the top K + 1, gets its logit recomputed from the bf16
+// inputs in double-f32 (about 48 significant bits); candidates are then ranked on the refined values.
 // The ranking compares 64-bit integer images of the (exact) double values: the fp64
 // unit is used only for the rare refinements.
 constexpr int REFINE_EXTRA = 8;
@@ -160,6 +160,37 @@ K3_DEVI void topk_select_smem(const TopkParams& p, int t, uint32_t* kh, TopkScra
   }
 }
 
+// Logit of token t for expert e, refined: every bf16 x bf16 product is exact in f32; the
+// products are summed in double-f32 (error-free two-sum per lane, then a two-sum
+// butterfly), about 48 significant bits -- far below the tie window, on the f32 pipes
+// (this GPU's fp64 rate is a small fraction of its f32 rate).  Same value on every lane.
+K3_DEVI void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bp = s - a;
+  e = (a - (s - bp)) + (b - bp);
+}
+K3_DEVI double refine_logit(const TopkParams& p, int t, int e, int lane) {
+  const uint16_t* xr = p.x + (size_t)t * p.H;
+  const uint16_t* wrr = p.wr + (size_t)e * p.H;
+  float hi = 0.f, lo = 0.f;
+  for (int h = lane; h < p.H; h += 32) {
+    const float pr = bf16_bits_to_f32(__ldg(xr + h)) * bf16_bits_to_f32(__ldg(wrr + h));
+    float s, er;
+    two_sum(hi, pr, s, er);
+    hi = s;
+    lo += er;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ohi = __shfl_xor_sync(0xffffffffu, hi, off), olo = __shfl_xor_sync(0xffffffffu, lo, off);
+    float s, er;
+    two_sum(hi, ohi, s, er);
+    hi = s;
+    lo = lo + olo + er;
+  }
+  return (double)hi + (double)lo;
+}
+
 // Everything after the candidate sort, for P <= 32, with candidate k in lane k's
 // registers: near-tie clusters (neighbours by shuffles), fp64 refinement of the flagged
 // candidates, re-ranking when any was refined, weights, stores.
@@ -183,13 +214,7 @@ K3_DEVI void topk_finish_warp(const TopkParams& p, int t, uint64_t key, int lane
     for (unsigned m = rmask; m; m &= m - 1u) {
       const int k = __ffs(m) - 1;
       const int e = __shfl_sync(0xffffffffu, id, k);
-      double acc = 0.0;
-      const uint16_t* xr = p.x + (size_t)t * p.H;
-      const uint16_t* wrr = p.wr + (size_t)e * p.H;
-      for (int h = lane; h < p.H; h += 32)
-        acc = fma((double)bf16_bits_to_f32(xr[h]), (double)bf16_bits_to_f32(wrr[h]), acc);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      const double acc = refine_logit(p, t, e, lane);
       if (lane == k) {
         const double s = 1.0 / (1.0 + exp(-acc));
         cs = (float)s;
@@ -297,13 +322,7 @@ K3_DEVI void topk_token(const TopkParams& p, int t, float* sb, float* sr, TopkSc
   for (int k = 0; k < P; ++k) {
     if (!S.rf[k]) continue;  // warp-uniform
     const int e = S.ci[k];
-    double acc = 0.0;
-    const uint16_t* xr = p.x + (size_t)t * p.H;
-    const uint16_t* wrr = p.wr + (size_t)e * p.H;
-    for (int h = lane; h < p.H; h += 32)
-      acc = fma((double)bf16_bits_to_f32(xr[h]), (double)bf16_bits_to_f32(wrr[h]), acc);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const double acc = refine_logit(p, t, e, lane);
     if (lane == 0) {
       const double s = 1.0 / (1.0 + exp(-acc));
       S.cs[k] = (float)s;
@@ -383,6 +402,8 @@ struct PermParams {
   MxBatch* batches;    // [nb_prefix[n_uniq]] token batches
   int32_t* n_batches;  // [1]
   uint32_t* status;
+  int32_t* cta_cnt;    // multi-CTA path: [ceil(T*K / PERM_SPAN)][E] per-CTA expert counts
+  int32_t* cta_base;   // ... and each CTA's first sorted position per expert
 };
 
 // exclusive scan of 4 values per thread over a PERM_WARPS-warp block (values in order
@@ -633,6 +654,184 @@ __global__ void __launch_bounds__(PERM_WARPS * 32) k3_permute_kernel(PermParams 
   grid_dep_wait();
   grid_dep_launch();
   permute_block(p, reinterpret_cast<int32_t*>(smem), wsum);
+}
+
+// ============================================================================ multi-CTA permutation
+// The same stable counting sort for many slots, across CTAs of PERM_SPAN slots each
+// (PERM_WARPS warps x 128 slots, in slot order):
+//   1. k3_perm_hist_kernel     per-CTA expert counts            -> cta_cnt[c][e]
+//   2. k3_perm_scan_kernel     one CTA: per expert, running sums over CTAs -> cta_base,
+//                              counts; expert offsets; unique experts; batch prefix
+//   3. k3_perm_scatter_kernel  per CTA: per-warp counts again, warp-major running
+//                              offsets from cta_base, stable placement as permute_block
+//   4. k3_perm_records_kernel  one thread per token-batch record
+// Equal to permute_block: within an expert, slots keep increasing flat index.
+constexpr int PERM_SPAN = PERM_WARPS * 128;
+
+// per-warp expert histogram of this CTA's slots into hist[PERM_WARPS][E]; returns the
+// warp's slot range [b0, b1)
+K3_DEVI void perm_warp_hist(const PermParams& p, int32_t* hist, int& b0, int& b1, bool flag_bad) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n = p.T * p.K;
+  b0 = min(n, (int)blockIdx.x * PERM_SPAN + warp * 128);
+  b1 = min(n, b0 + 128);
+  for (int i = threadIdx.x; i < PERM_WARPS * p.E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  for (int i = b0 + lane; i < b1; i += 32) {
+    int e = p.ids ? p.ids[i] : p.fixed_expert;
+    if (e < 0 || e >= p.E) {
+      if (flag_bad) flag_status(p.status, K3MOE_DEV_BAD_ID);
+      e = min(max(e, 0), p.E - 1);
+    }
+    atomicAdd(&hist[warp * p.E + e], 1);
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(PERM_WARPS * 32) k3_perm_hist_kernel(PermParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  int32_t* hist = reinterpret_cast<int32_t*>(smem);
+  grid_dep_wait();
+  grid_dep_launch();
+  int b0, b1;
+  perm_warp_hist(p, hist, b0, b1, true);
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < PERM_WARPS; ++w) c += hist[w * p.E + e];
+    p.cta_cnt[(size_t)blockIdx.x * p.E + e] = c;
+  }
+}
+
+__global__ void __launch_bounds__(PERM_WARPS * 32) k3_perm_scan_kernel(PermParams p, int nct) {
+  __shared__ int wsum[PERM_WARPS + 1];
+  grid_dep_wait();
+  grid_dep_launch();
+  int cnt[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e = threadIdx.x * 4 + q;
+    int run = 0;
+    if (e < p.E) {
+      for (int c = 0; c < nct; ++c) {
+        const int v = p.cta_cnt[(size_t)c * p.E + e];
+        p.cta_base[(size_t)c * p.E + e] = run;
+        run += v;
+      }
+      p.counts[e] = run;
+    }
+    cnt[q] = run;
+  }
+  int off[4] = {cnt[0], cnt[1], cnt[2], cnt[3]};
+  const int tot = block_scan4(off, wsum);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e = threadIdx.x * 4 + q;
+    if (e < p.E) {
+      p.offsets[e] = off[q];
+      for (int c = 0; c < nct; ++c) p.cta_base[(size_t)c * p.E + e] += off[q];
+    }
+  }
+  if (threadIdx.x == 0) p.offsets[p.E] = tot;
+  // unique experts (ascending) and their token-batch prefix
+  int flag[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) flag[q] = cnt[q] > 0 ? 1 : 0;
+  const int nu = block_scan4(flag, wsum);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e = threadIdx.x * 4 + q;
+    if (e < p.E && cnt[q] > 0) p.uniq[flag[q]] = e;
+  }
+  if (threadIdx.x == 0) *p.n_uniq = nu;
+  __syncthreads();
+  int nbv[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int u = threadIdx.x * 4 + q;
+    nbv[q] = (u < nu) ? (p.counts[p.uniq[u]] + p.NB - 1) / p.NB : 0;
+  }
+  int nbx[4] = {nbv[0], nbv[1], nbv[2], nbv[3]};
+  const int nbt = block_scan4(nbx, wsum);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int u = threadIdx.x * 4 + q;
+    if (u < nu) p.nb_prefix[u] = nbx[q];
+  }
+  if (threadIdx.x == 0) {
+    p.nb_prefix[nu] = nbt;
+    *p.n_batches = nbt;
+  }
+}
+
+__global__ void __launch_bounds__(PERM_WARPS * 32) k3_perm_scatter_kernel(PermParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  int32_t* hist = reinterpret_cast<int32_t*>(smem);
+  grid_dep_wait();
+  grid_dep_launch();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int b0, b1;
+  perm_warp_hist(p, hist, b0, b1, false);
+  // warp-major running offsets, starting at this CTA's first position per expert
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+    int run = p.cta_base[(size_t)blockIdx.x * p.E + e];
+    for (int w = 0; w < PERM_WARPS; ++w) {
+      const int c = hist[w * p.E + e];
+      hist[w * p.E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int base = b0; base < b1; base += 32) {
+    const int i = base + lane;
+    const bool valid = i < b1;
+    int e = -1;
+    if (valid) {
+      e = p.ids ? p.ids[i] : p.fixed_expert;
+      e = min(max(e, 0), p.E - 1);
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int leader = __ffs(peers) - 1;
+    if (valid) {
+      const int pos = hist[warp * p.E + e] + rank;
+      p.slot_of[pos] = i;
+      p.slot_tok[pos] = i / p.K;
+      p.inv[i] = pos;
+    }
+    __syncwarp();
+    if (valid && lane == leader) hist[warp * p.E + e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// one thread per token-batch record: the unique expert is found by binary search of the
+// batch prefix
+__global__ void __launch_bounds__(256) k3_perm_records_kernel(PermParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int nu = *p.n_uniq, nbt = *p.n_batches;
+  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < nbt; r += gridDim.x * blockDim.x) {
+    int lo = 0, hi = nu - 1;  // largest u with nb_prefix[u] <= r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.nb_prefix[mid] <= r) lo = mid;
+      else hi = mid - 1;
+    }
+    const int u = lo, e = p.uniq[u], b = r - p.nb_prefix[u];
+    const int cntu = p.counts[e], offu = p.offsets[e];
+    MxBatch* rec = p.batches + r;
+    rec->w[0] = p.ex.gate_q[e];
+    rec->w[1] = p.ex.gate_s[e];
+    rec->w[2] = p.ex.up_q[e];
+    rec->w[3] = p.ex.up_s[e];
+    rec->w[4] = p.ex.down_q[e];
+    rec->w[5] = p.ex.down_s[e];
+    const int s0 = offu + b * p.NB, nn = min(p.NB, cntu - b * p.NB);
+    rec->slot0 = s0;
+    rec->n = nn;
+    for (int j = 0; j < MX_MAX_NB; ++j) rec->tok[j] = (j < nn) ? p.slot_tok[s0 + j] : 0;
+    rec->pad[0] = rec->pad[1] = 0;
+  }
 }
 
 // ============================================================================ activation prep

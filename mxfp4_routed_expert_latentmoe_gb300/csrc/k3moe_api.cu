@@ -22,7 +22,7 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 struct WsLayout {
   size_t status, logits, ids, w, zmax, zpow, counts, offsets, slot_of, slot_tok, inv, uniq, n_uniq, nb_prefix,
-      n_batches, batches, z, z16, h16, o, y, yhat, cpart, ccount, z16p, spow, total;
+      n_batches, cta_cnt, cta_base, batches, z, z16, h16, o, y, yhat, cpart, ccount, z16p, spow, total;
 };
 
 WsLayout ws_layout(const k3moe_dims& d, int T) {
@@ -51,6 +51,10 @@ WsLayout ws_layout(const k3moe_dims& d, int T) {
   L.n_uniq = take(4);
   L.nb_prefix = take((E + 1) * 4);
   L.n_batches = take(4);
+  // multi-CTA permutation: per-CTA expert counts and first positions
+  const size_t nct = (slots + PERM_SPAN - 1) / PERM_SPAN;
+  L.cta_cnt = take(nct * E * 4);
+  L.cta_base = take(nct * E * 4);
   // token batches of at least 8 tokens: at most ceil(slots / 8) + min(E, slots) of them
   L.batches = take((slots / 8 + 1 + (E < slots ? E : slots)) * sizeof(MxBatch));
   L.z = take(Tz * Lt * 2);
@@ -320,8 +324,23 @@ cudaError_t launch_topk(const TopkParams& p, int dev, cudaStream_t st, bool pdl)
 
 cudaError_t launch_permute(const PermParams& p, int dev, cudaStream_t st, bool pdl) {
   const int smem = PERM_WARPS * p.E * 4;
-  if (!set_smem<k3_permute_kernel>(dev, smem)) return cudaErrorInvalidValue;
-  return launch(k3_permute_kernel, dim3(1), dim3(PERM_WARPS * 32), smem, st, pdl, p);
+  const int n = p.T * p.K;
+  if (n <= 2 * PERM_SPAN) {  // one CTA
+    if (!set_smem<k3_permute_kernel>(dev, smem)) return cudaErrorInvalidValue;
+    return launch(k3_permute_kernel, dim3(1), dim3(PERM_WARPS * 32), smem, st, pdl, p);
+  }
+  const int nct = (n + PERM_SPAN - 1) / PERM_SPAN;
+  if (!set_smem<k3_perm_hist_kernel>(dev, smem) || !set_smem<k3_perm_scatter_kernel>(dev, smem))
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch(k3_perm_hist_kernel, dim3(nct), dim3(PERM_WARPS * 32), smem, st, pdl, p);
+  if (e == cudaSuccess) e = launch(k3_perm_scan_kernel, dim3(1), dim3(PERM_WARPS * 32), 0, st, pdl, p, nct);
+  if (e == cudaSuccess) e = launch(k3_perm_scatter_kernel, dim3(nct), dim3(PERM_WARPS * 32), smem, st, pdl, p);
+  if (e == cudaSuccess && p.ex.gate_q) {
+    const int bound = n / 8 + 1 + (p.E < n ? p.E : n);  // records capacity of the workspace
+    const int blocks = (bound + 255) / 256;
+    e = launch(k3_perm_records_kernel, dim3(blocks < 1024 ? blocks : 1024), dim3(256), 0, st, pdl, p);
+  }
+  return e;
 }
 
 cudaError_t launch_z16(const Z16Params& p, cudaStream_t st, bool pdl) {
@@ -385,6 +404,8 @@ PermParams perm_params(const k3moe_dims& d, int T, int K, const int32_t* ids, in
   pp.n_uniq = at<int32_t>(ws, L.n_uniq);
   pp.nb_prefix = at<int32_t>(ws, L.nb_prefix);
   pp.status = at<uint32_t>(ws, L.status);
+  pp.cta_cnt = at<int32_t>(ws, L.cta_cnt);
+  pp.cta_base = at<int32_t>(ws, L.cta_base);
   return pp;
 }
 
