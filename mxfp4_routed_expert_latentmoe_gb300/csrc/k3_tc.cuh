@@ -544,8 +544,6 @@ K3_DEVI void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_
       : "memory");
 }
 
-// named barrier over the producer warps
-K3_DEVI void producers_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(TM_PRODUCERS * 32) : "memory"); }
 
 template <int MODE>
 __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_constant__ CUtensorMap mapB,
@@ -750,13 +748,12 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
   } else {
     // ------------------------------------------------------------ decode producers (warps 11..18)
     // The raw bytes of a tile travel in chunks of CKB k-blocks: CKB * 32 bytes of each of
-    // the tile's 256 rows, copied by all producer threads with 16-byte cp.async into a
-    // ring of RC chunks; 16-byte granules are XOR-swizzled by row so the decode reads are
-    // free of bank conflicts.  A named
-    // barrier per chunk publishes it to all producers.
+    // the tile's 256 rows.  Each producer warp copies the 32 rows it decodes (full
+    // 128-byte lines, eight lanes per line, 16-byte cp.async) into a ring of RC chunks and
+    // waits on its own copy groups, so the warps never wait for one another; 16-byte
+    // granules are XOR-swizzled by row so the decode reads are free of bank conflicts.
     // Decode: a warp owns the TMEM lane quarter warp % 4 (32 rows) of one block (warps
     // 11..14 block 0, 15..18 block 1), a k-block's 64 elements per thread (32 columns).
-    const int pt = threadIdx.x - (3 + TM_EPI) * 32;  // 0..255
     const int qd = warp & 3;
     const int mb = (warp - (3 + TM_EPI)) >> 2;
     const int ri = mb * TM_ROWS + qd * 32 + lane;  // row of the tile (over both blocks)
@@ -768,41 +765,35 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
     const int my_tiles = (tiles > (int)blockIdx.x) ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int nchunks = my_tiles * kchunks;
     bool stop = false;
+    const int wr0 = mb * TM_ROWS + qd * 32;  // this warp's first row of the tile
     auto issue = [&](int jc) {
       if (jc < nchunks && !stop) {
         const int tile = blockIdx.x + (jc / kchunks) * gridDim.x, kc = jc % kchunks;
         const MxBatch* rec = p.batches + tile / mtiles;
         const int tm = tile % mtiles;
+        const uint8_t* q = rec->w[blk_tensor(mb)] + (blk_row0(tm, mb) + qd * 32) * qrow + kc * ROWB;
         const uint32_t dst = raw_base + (jc % RC) * Lay::RAW_SLOT;
 #pragma unroll
-        for (int k = 0; k < MROWS * GPR / (TM_PRODUCERS * 32); ++k) {
-          const int G = k * TM_PRODUCERS * 32 + pt;  // 16-byte granule of the chunk
-          const int rr = G / GPR, gc = G % GPR, mm = rr / TM_ROWS;
-          const uint8_t* src = rec->w[blk_tensor(mm)] + (blk_row0(tm, mm) + (rr % TM_ROWS)) * qrow + kc * ROWB + gc * 16;
-          cp_async16(dst + rr * ROWB + ((gc ^ swz(rr)) << 4), src);
+        for (int k = 0; k < 32 * GPR / 32; ++k) {
+          const int G = k * 32 + lane;  // 16-byte granule of this warp's 32 rows
+          const int r = G / GPR, gc = G % GPR, rr = wr0 + r;
+          cp_async16(dst + rr * ROWB + ((gc ^ swz(rr)) << 4), q + r * qrow + gc * 16);
         }
-        {
-          const int mm = pt / TM_ROWS;
-          const uint8_t* ssrc = rec->w[blk_tensor(mm) + 1] + (blk_row0(tm, mm) + (pt % TM_ROWS)) * srow + kc * (2 * CKB);
-          const uint32_t sdst = sraw_base + (jc % RC) * Lay::SC_SLOT + pt * (2 * CKB);
-          if constexpr (CKB == 4) cp_async8(sdst, ssrc);
-          else cp_async4(sdst, ssrc);
-        }
+        const uint8_t* ssrc = rec->w[blk_tensor(mb) + 1] + (blk_row0(tm, mb) + qd * 32 + lane) * srow + kc * (2 * CKB);
+        const uint32_t sdst = sraw_base + (jc % RC) * Lay::SC_SLOT + (wr0 + lane) * (2 * CKB);
+        if constexpr (CKB == 4) cp_async8(sdst, ssrc);
+        else cp_async4(sdst, ssrc);
       }
       cp_async_commit();
     };
     bool bad = false;
 #pragma unroll 1
     for (int j = 0; j < RC - 1; ++j) issue(j);
-    // every producer thread runs all nchunks iterations and meets every barrier; after an
-    // abort the waits and stores are skipped
 #pragma unroll 1
-    for (int jc = 0; jc < nchunks; ++jc) {
+    for (int jc = 0; jc < nchunks && !stop; ++jc) {
       cp_async_wait<RC - 2>();  // chunk jc has landed (this thread's copies)
-      producers_sync();         // ... everyone's, and everyone is done with chunk jc - 1
-      if (*abort_flag) stop = true;
+      __syncwarp();             // ... the whole warp's, and the warp is done with chunk jc - 1
       issue(jc + RC - 1);       // into the slot chunk jc - 1 used
-      if (stop) continue;
       const uint8_t* src = base_ptr + (raw_base - base) + (jc % RC) * Lay::RAW_SLOT + ri * ROWB;
       const uint8_t* scs = base_ptr + (sraw_base - base) + (jc % RC) * Lay::SC_SLOT + ri * (2 * CKB);
       uint2 sc8;
