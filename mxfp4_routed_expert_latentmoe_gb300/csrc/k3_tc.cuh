@@ -766,12 +766,23 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
     const int nchunks = my_tiles * kchunks;
     bool stop = false;
     const int wr0 = mb * TM_ROWS + qd * 32;  // this warp's first row of the tile
+    // this warp's rows of the current tile: packed-byte and scale base pointers, loaded
+    // from the batch record once per tile (reloading them at every chunk put an L2 round
+    // trip in front of each chunk's copies)
+    int cur_tile = -1;
+    const uint8_t* qtile = nullptr;
+    const uint8_t* stile = nullptr;
     auto issue = [&](int jc) {
       if (jc < nchunks && !stop) {
         const int tile = blockIdx.x + (jc / kchunks) * gridDim.x, kc = jc % kchunks;
-        const MxBatch* rec = p.batches + tile / mtiles;
-        const int tm = tile % mtiles;
-        const uint8_t* q = rec->w[blk_tensor(mb)] + (blk_row0(tm, mb) + qd * 32) * qrow + kc * ROWB;
+        if (tile != cur_tile) {
+          const MxBatch* rec = p.batches + tile / mtiles;
+          const size_t r0 = blk_row0(tile % mtiles, mb) + qd * 32;
+          qtile = rec->w[blk_tensor(mb)] + r0 * qrow;
+          stile = rec->w[blk_tensor(mb) + 1] + r0 * srow;
+          cur_tile = tile;
+        }
+        const uint8_t* q = qtile + kc * ROWB;
         const uint32_t dst = raw_base + (jc % RC) * Lay::RAW_SLOT;
 #pragma unroll
         for (int k = 0; k < 32 * GPR / 32; ++k) {
@@ -779,7 +790,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
           const int r = G / GPR, gc = G % GPR, rr = wr0 + r;
           cp_async16(dst + rr * ROWB + ((gc ^ swz(rr)) << 4), q + r * qrow + gc * 16);
         }
-        const uint8_t* ssrc = rec->w[blk_tensor(mb) + 1] + (blk_row0(tm, mb) + qd * 32 + lane) * srow + kc * (2 * CKB);
+        const uint8_t* ssrc = stile + lane * srow + kc * (2 * CKB);
         const uint32_t sdst = sraw_base + (jc % RC) * Lay::SC_SLOT + (wr0 + lane) * (2 * CKB);
         if constexpr (CKB == 4) cp_async8(sdst, ssrc);
         else cp_async4(sdst, ssrc);
