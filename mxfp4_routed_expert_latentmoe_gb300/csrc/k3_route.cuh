@@ -173,12 +173,39 @@ K3_DEVI double refine_logit(const TopkParams& p, int t, int e, int lane) {
   const uint16_t* xr = p.x + (size_t)t * p.H;
   const uint16_t* wrr = p.wr + (size_t)e * p.H;
   float hi = 0.f, lo = 0.f;
-  for (int h = lane; h < p.H; h += 32) {
-    const float pr = bf16_bits_to_f32(__ldg(xr + h)) * bf16_bits_to_f32(__ldg(wrr + h));
+  auto acc = [&](float pr) {
     float s, er;
     two_sum(hi, pr, s, er);
     hi = s;
     lo += er;
+  };
+  if ((p.H & 7) == 0 && ((reinterpret_cast<uintptr_t>(p.x) | reinterpret_cast<uintptr_t>(p.wr)) & 15u) == 0) {
+    // 16-byte loads, eight per operand in flight per lane (a refinement is latency-bound:
+    // one row pair is read once)
+    const uint4* xv = reinterpret_cast<const uint4*>(xr);
+    const uint4* wv = reinterpret_cast<const uint4*>(wrr);
+    const int nv = p.H >> 3;
+    for (int v0 = lane; v0 < nv; v0 += 32 * 8) {
+      uint4 a[8], b[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + 32 * u;
+        a[u] = (v < nv) ? __ldg(xv + v) : make_uint4(0u, 0u, 0u, 0u);
+        b[u] = (v < nv) ? __ldg(wv + v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t aw[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+        const uint32_t bw[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc(__uint_as_float(aw[j] << 16) * __uint_as_float(bw[j] << 16));
+          acc(__uint_as_float(aw[j] & 0xFFFF0000u) * __uint_as_float(bw[j] & 0xFFFF0000u));
+        }
+      }
+    }
+  } else {
+    for (int h = lane; h < p.H; h += 32) acc(bf16_bits_to_f32(__ldg(xr + h)) * bf16_bits_to_f32(__ldg(wrr + h)));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -946,6 +973,73 @@ struct CombineParams {
 
 constexpr int COMB_THREADS = 256;
 constexpr int COMB_MAX_SPLIT = 32;
+
+// grid T, for L <= 8 * 4 * COMB_THREADS: one CTA per token; thread i combines the float4
+// columns i + j * blockDim.x (j < CPT) in k order, the K expert rows read with independent
+// loads, and keeps them in registers; the row's sum of squares is reduced in the CTA
+// (warp partials added in warp order) and y and yhat are written from registers.
+template <int CPT>
+__global__ void __launch_bounds__(COMB_THREADS) k3_combine_row_kernel(CombineParams p) {
+  __shared__ float wpart[COMB_THREADS / 32];
+  __shared__ const float* rows[64];
+  __shared__ float wk[64];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int t = blockIdx.x;
+  if ((int)threadIdx.x < p.K) {
+    rows[threadIdx.x] = p.o + (size_t)p.inv[(size_t)t * p.K + threadIdx.x] * p.L;
+    wk[threadIdx.x] = p.w[(size_t)t * p.K + threadIdx.x];
+  }
+  __syncthreads();
+  const int L4 = p.L >> 2;
+  float4 y[CPT];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const int c4 = threadIdx.x + j * blockDim.x;
+    y[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c4 < L4) {
+      for (int k0 = 0; k0 < p.K; k0 += 16) {
+        float4 v[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          if (k0 + q < p.K) v[q] = reinterpret_cast<const float4*>(rows[k0 + q])[c4];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          if (k0 + q < p.K) {
+            const float wq = wk[k0 + q];
+            y[j].x = fmaf(wq, v[q].x, y[j].x);
+            y[j].y = fmaf(wq, v[q].y, y[j].y);
+            y[j].z = fmaf(wq, v[q].z, y[j].z);
+            y[j].w = fmaf(wq, v[q].w, y[j].w);
+          }
+        }
+      }
+      ss = fmaf(y[j].x, y[j].x, ss);
+      ss = fmaf(y[j].y, y[j].y, ss);
+      ss = fmaf(y[j].z, y[j].z, ss);
+      ss = fmaf(y[j].w, y[j].w, ss);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) wpart[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += wpart[w];
+  const float r = 1.0f / sqrtf(tot / (float)p.L + p.eps);
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const int c4 = threadIdx.x + j * blockDim.x;
+    if (c4 < L4) {
+      reinterpret_cast<float4*>(p.y + (size_t)t * p.L)[c4] = y[j];
+      const float4 g = __ldg(reinterpret_cast<const float4*>(p.gamma) + c4);
+      const uint32_t lo = f32_to_bf16_bits(g.x * (y[j].x * r)) | (f32_to_bf16_bits(g.y * (y[j].y * r)) << 16);
+      const uint32_t hi = f32_to_bf16_bits(g.z * (y[j].z * r)) | (f32_to_bf16_bits(g.w * (y[j].w * r)) << 16);
+      reinterpret_cast<uint2*>(p.yhat + (size_t)t * p.L)[c4] = make_uint2(lo, hi);
+    }
+  }
+}
 
 // grid (T, split): CTA sp of token t combines float4 columns [sp*256, sp*256+256) in k
 // order -- one column per thread, the K expert rows read with independent loads --,

@@ -367,6 +367,20 @@ cudaError_t launch_route_tail(const TopkParams& tp, const PermParams& pp, const 
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
+  // one CTA per token while a thread holds at most 8 float4 columns and there are enough
+  // tokens to fill the GPU (few tokens: a row is split over several CTAs for more loads
+  // in flight)
+  const int L4 = p.L / 4;
+  if (p.T >= kTcMinT && L4 <= 8 * COMB_THREADS && (reinterpret_cast<uintptr_t>(p.gamma) & 15u) == 0) {
+    const int cpt = L4 <= COMB_THREADS ? 1 : L4 <= 2 * COMB_THREADS ? 2 : L4 <= 4 * COMB_THREADS ? 4 : 8;
+    const int threads = ((L4 + cpt - 1) / cpt + 31) / 32 * 32;
+    switch (cpt) {
+      case 1: return launch(k3_combine_row_kernel<1>, dim3(p.T), dim3(threads), 0, st, pdl, p);
+      case 2: return launch(k3_combine_row_kernel<2>, dim3(p.T), dim3(threads), 0, st, pdl, p);
+      case 4: return launch(k3_combine_row_kernel<4>, dim3(p.T), dim3(threads), 0, st, pdl, p);
+      default: return launch(k3_combine_row_kernel<8>, dim3(p.T), dim3(threads), 0, st, pdl, p);
+    }
+  }
   const int split = (p.L / 4 + COMB_THREADS - 1) / COMB_THREADS;  // one float4 column per thread
   if (split > COMB_MAX_SPLIT) return cudaErrorInvalidValue;
   return launch(k3_combine_norm_kernel, dim3(p.T, split), dim3(COMB_THREADS), 0, st, pdl, p);
