@@ -562,14 +562,15 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
   const uint32_t stg_base = sraw_base + RC * Lay::SC_SLOT;  // [STG_WORDS][epilogue thread] f32
   const uint32_t bars = stg_base + Lay::STG;
   // Stage st = TM_AKB k-blocks: A in TMEM slot st % SA, B in shared-memory group st % NBS.
-  // fullA(s, m): block m's producers stored A slot s; fullB(g): TMA landed B group g;
-  // kdone(g): both issuers' MMAs of the stage in group g completed, which frees its B group
-  // and (NBS >= SA) its A slot: one commit per stage serves both rings.
+  // full(g): the stage in group g is ready -- all producer warps stored their A rows
+  // (one arrival each) and the TMA landed its B tiles (the TMA thread's arrival with the
+  // byte count) -- so an issuer tests one barrier per stage; kdone(g): both issuers' MMAs
+  // of the stage in group g completed, which frees its B group and (NBS >= SA) its A slot:
+  // one commit per stage serves both rings.
   constexpr int NBS = Lay::NBS;
-  auto fullA = [&](int s, int m) { return bars + 8 * (s * TM_BLOCKS + m); };
-  auto kdone = [&](int g) { return bars + 8 * (SA * TM_BLOCKS + g); };
-  auto fullB = [&](int g) { return bars + 8 * (SA * TM_BLOCKS + NBS + g); };
-  constexpr int NB0 = SA * TM_BLOCKS + 2 * NBS;
+  auto full = [&](int g) { return bars + 8 * g; };
+  auto kdone = [&](int g) { return bars + 8 * (NBS + g); };
+  constexpr int NB0 = 2 * NBS;
   auto tfull = [&](int b) { return bars + 8 * (NB0 + b); };
   auto tempty = [&](int b) { return bars + 8 * (NB0 + 2 + b); };
   const uint32_t done_bar = bars + 8 * (NB0 + 4);
@@ -578,11 +579,9 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
-    for (int s = 0; s < SA; ++s)
-      for (int m = 0; m < TM_BLOCKS; ++m) mbar_init(fullA(s, m), TM_PRODUCERS / TM_BLOCKS);
     for (int g = 0; g < NBS; ++g) {
-      mbar_init(kdone(g), TM_BLOCKS);  // one commit per issuer
-      mbar_init(fullB(g), 1);
+      mbar_init(full(g), TM_PRODUCERS + 1);  // producer warps + the TMA thread
+      mbar_init(kdone(g), TM_BLOCKS);        // one commit per issuer
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull(b), TM_BLOCKS);
@@ -620,17 +619,27 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
           // group bs % NBS last held stage bs - NBS
           const int g = bs % NBS;
           if (!mbar_wait(kdone(g), ((bs / NBS) & 1) ^ 1, abort_flag)) break;
-          mbar_expect_tx(fullB(g), TM_AKB * TM_B_BYTES);
+          mbar_expect_tx(full(g), TM_AKB * TM_B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < TM_AKB; ++kk)
-            tma_load_2d(base + (g * TM_AKB + kk) * TM_B_BYTES, &mapB, (kb + kk) * TM_BK, slot0, fullB(g));
+            tma_load_2d(base + (g * TM_AKB + kk) * TM_B_BYTES, &mapB, (kb + kk) * TM_BK, slot0, full(g));
         }
       }
-      for (int g = 0; g < NBS; ++g) {  // drain issued loads
+      // drain issued loads: the stage's phase completes once its bytes landed (and the
+      // producers arrived).  After an abort the producers may never arrive: wait a bounded
+      // time, far beyond a copy's latency, instead.
+      const bool aborted = *abort_flag != 0;
+      for (int g = 0; g < NBS; ++g) {
         const int last = bs - 1 - ((bs - 1 - g) % NBS + NBS) % NBS;
         if (last >= 0 && last < bs) {
-          volatile int never = 0;
-          mbar_wait(fullB(g), (last / NBS) & 1, &never);
+          if (!aborted) {
+            volatile int never = 0;
+            mbar_wait(full(g), (last / NBS) & 1, &never);
+          } else {
+            const long long t0 = clock64();
+            while (!mbar_test(full(g), (last / NBS) & 1) && clock64() - t0 < (1ll << 21)) {
+            }
+          }
         }
       }
     }
@@ -652,9 +661,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
         bool ok = true;
         for (int kb = 0; kb < kblocks; kb += TM_AKB, it += TM_AKB) {
           const int st = it / TM_AKB, sa = st % SA, g = st % NBS;
-          // B (loaded up to NBS stages ahead) is normally ready first: test it while A is stored
-          if (!mbar_wait_spin(fullB(g), (st / NBS) & 1, abort_flag) ||
-              !mbar_wait_spin(fullA(sa, mm), (st / SA) & 1, abort_flag)) {
+          if (!mbar_wait_spin(full(g), (st / NBS) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -854,7 +861,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
         if (stop) break;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(fullA(sa, mb));
+        if (lane == 0) mbar_arrive(full(st % NBS));
       }
     }
     cp_async_wait<0>();
