@@ -824,7 +824,11 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           const uint4 cq = *reinterpret_cast<const uint4*>(src + (((2 * kq + g) ^ swz(ri)) << 4));
-          const uint32_t sc2 = ue8m0_to_f16x2((cs >> (8 * g)) & 0xFFu, bad);
+          // scale byte s in 113..142: 2^(s-127) is a normal f16, exponent field s - 112, in
+          // both halves -- two integer multiply-adds; other bytes take the general decode
+          const uint32_t sb = (cs >> (8 * g)) & 0xFFu;
+          uint32_t sc2 = (sb * 1024u - 114688u) * 0x10001u;
+          if (sb - 113u > 29u) sc2 = ue8m0_to_f16x2(sb, bad);
           const uint32_t w4[4] = {cq.x, cq.y, cq.z, cq.w};
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {  // 8 elements = 4 packed bytes -> 4 f16x2 columns
