@@ -77,6 +77,9 @@ typedef enum {
 #define K3MOE_DEV_SCALE_RANGE 0x8u /* the tensor-core expert path (T >= 256) met a scale byte
                                       outside 105..142, where its f16 weight decode is not
                                       exact; the affected outputs are approximate */
+#define K3MOE_DEV_ALIGN 0x10u      /* the tensor-core expert path (T >= 256) met an expert weight
+                                      tensor that is not 16-byte aligned; the call was abandoned
+                                      and its outputs are invalid */
 
 /* The six vendor tensors of every expert, as DEVICE arrays of n_experts DEVICE
  * pointers (the pointer tables themselves live in device memory):

@@ -27,7 +27,7 @@ NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", 
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "pointer not 16-byte aligned",
           4: "workspace too small", 5: "current device is not compute capability 10.3", 6: "CUDA launch or copy failed"}
-DEV_TIE_WINDOW, DEV_TIMEOUT, DEV_BAD_ID = 0x1, 0x2, 0x4
+DEV_TIE_WINDOW, DEV_TIMEOUT, DEV_BAD_ID, DEV_SCALE_RANGE, DEV_ALIGN = 0x1, 0x2, 0x4, 0x8, 0x10
 
 
 class K3MoEError(RuntimeError):

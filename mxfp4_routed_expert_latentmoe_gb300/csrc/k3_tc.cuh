@@ -117,6 +117,29 @@ K3_DEVI void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, u
 K3_DEVI void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(map) : "memory");
 }
+// Tensor maps rewritten on the device: the global address of a map held in shared memory,
+// the warp-wide copy of that map to global memory with a release fence for the tensor-map
+// proxy, and the acquire fence before a copy uses the global map.
+K3_DEVI void tmap_replace_addr(uint32_t smem_map, const void* gaddr) {
+  asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;\n" ::"r"(smem_map), "l"(gaddr)
+               : "memory");
+}
+K3_DEVI void tmap_store_release(void* gmem_map, uint32_t smem_map) {
+  asm volatile(
+      "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned [%0], [%1], 128;\n" ::"l"(
+          gmem_map),
+      "r"(smem_map)
+      : "memory");
+}
+K3_DEVI void tmap_acquire(const void* gmem_map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;\n" ::"l"(gmem_map) : "memory");
+}
+K3_DEVI void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+// arrival on the barrier once all of this thread's earlier cp.async copies have landed (the
+// barrier's expected count includes it)
+K3_DEVI void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
 
 K3_DEVI void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst_smem), "r"(ncols)
@@ -415,7 +438,8 @@ constexpr int TM_NB = 96;          // tokens per batch (MMA N <= 96): bounded by
 constexpr int TM_BK = 64;          // k-block
 constexpr int TM_PRODUCERS = 8;    // decode warps
 constexpr int TM_EPI = 8;         // epilogue warps: two per TMEM lane quarter, alternate 16-column chunks
-constexpr int TM_THREADS = (3 + TM_EPI + TM_PRODUCERS) * 32;
+constexpr int TM_COPY_WARP = 3 + TM_EPI + TM_PRODUCERS;  // packed-weight TMA copies
+constexpr int TM_THREADS = (TM_COPY_WARP + 1) * 32;
 constexpr int TM_B_BYTES = TM_NB * TM_BK * 2;  // 12 KB
 constexpr int TM_AKB = 2;          // k-blocks per A stage (one barrier round trip per stage)
 
@@ -454,8 +478,12 @@ struct TmLayout {
   // GATEUP staging of the accumulators: per epilogue thread up to 3 chunks x (16 g + 16 u)
   static constexpr int STG_WORDS = (MODE == 0) ? (TM_NB / 16 / 2) * 32 : 0;
   static constexpr int STG = STG_WORDS * TM_EPI * 32 * 4;
-  static constexpr int SMEM = 1024 + SB * TM_B_BYTES + RC * (RAW_SLOT + SC_SLOT) + STG + 512;
+  // barriers (512 bytes), then a shared-memory copy of each block's packed-weight tensor map
+  static constexpr int SMEM = 1024 + SB * TM_B_BYTES + RC * (RAW_SLOT + SC_SLOT) + STG + 512 + TM_BLOCKS * 128;
 };
+
+// CTAs of one grouped-GEMM launch at most (sizes the per-warp tensor-map workspace)
+constexpr int TM_MAX_CTAS = 256;
 
 struct TcMoeParams {
   const MxBatch* batches;    // token batches of up to TM_NB tokens (one expert each)
@@ -465,6 +493,7 @@ struct TcMoeParams {
   const int32_t* slot_pow;   // GATEUP: per-slot exponent p of its activation row (act = value * 2^p)
   void* out;                 // GATEUP: h16 [slots, R]; DOWN: o f32 [slots, R]
   uint32_t* status;
+  void* tmaps;               // packed-weight tensor maps, [TM_MAX_CTAS][TM_BLOCKS][2] x 128 bytes
 };
 
 // E8M0 scale byte -> f16x2 of 2^(s-127) in both halves (0 when not representable);
@@ -547,6 +576,7 @@ K3_DEVI void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_
 
 template <int MODE>
 __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_constant__ CUtensorMap mapB,
+                                                                  const __grid_constant__ CUtensorMap mapA,
                                                                   TcMoeParams p) {
   using Lay = TmLayout<MODE>;
   constexpr int SA = Lay::SA, SB = Lay::SB, RC = Lay::RC, MROWS = Lay::MROWS;
@@ -561,6 +591,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
   const uint32_t sraw_base = raw_base + RC * Lay::RAW_SLOT;  // [RC][MROWS rows][2 CKB bytes]
   const uint32_t stg_base = sraw_base + RC * Lay::SC_SLOT;  // [STG_WORDS][epilogue thread] f32
   const uint32_t bars = stg_base + Lay::STG;
+  const uint32_t smaps = bars + 512;  // [TM_BLOCKS][128 bytes] tensor maps
   // Stage st = TM_AKB k-blocks: A in TMEM slot st % SA, B in shared-memory group st % NBS.
   // full(g): the stage in group g is ready -- all producer warps stored their A rows
   // (one arrival each) and the TMA landed its B tiles (the TMA thread's arrival with the
@@ -574,7 +605,12 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
   auto tfull = [&](int b) { return bars + 8 * (NB0 + b); };
   auto tempty = [&](int b) { return bars + 8 * (NB0 + 2 + b); };
   const uint32_t done_bar = bars + 8 * (NB0 + 4);
-  static_assert(8 * (NB0 + 5) <= 512, "barrier space");
+  // raw_full(s): the packed and scale bytes of the chunk in slot s landed (the copy warp's
+  // lane 0 arrives with the TMA byte count, each of its lanes once its scale copies land);
+  // raw_empty(s): every producer warp is done with the slot's chunk
+  auto raw_full = [&](int s) { return bars + 8 * (NB0 + 5 + s); };
+  auto raw_empty = [&](int s) { return bars + 8 * (NB0 + 5 + RC + s); };
+  static_assert(8 * (NB0 + 5 + 2 * RC) <= 512, "barrier space");
   volatile int* abort_flag = &abort_sh;
 
   if (threadIdx.x == 0) {
@@ -588,6 +624,10 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       mbar_init(tempty(b), TM_EPI * 32);
     }
     mbar_init(done_bar, TM_BLOCKS);
+    for (int r = 0; r < RC; ++r) {
+      mbar_init(raw_full(r), 1 + 32);
+      mbar_init(raw_empty(r), TM_PRODUCERS);
+    }
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -752,19 +792,102 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
         }
       }
     }
+  } else if (warp == TM_COPY_WARP) {
+    // ------------------------------------------------------------ packed-weight copies (warp 19)
+    // The packed bytes of a tile travel in chunks of CKB k-blocks (ROWB bytes of each of its
+    // 256 rows) through a ring of RC slots: per chunk one TMA copy per block (128 rows x
+    // ROWB bytes; the 128-byte swizzle puts 16-byte granule c of row r at c ^ (r & 7), the
+    // layout the decode reads), issued once all producer warps are done with the slot.
+    // The tensor maps take the tile's expert tensors as global addresses, rewritten on the
+    // device when the tile changes; two per block in global memory, used by alternate tiles,
+    // so a map is rewritten only after every copy of the tile before last has landed.
+    constexpr int CKB = Lay::CKB, ROWB = Lay::ROWB;
+    static_assert(ROWB == 128, "the TMA 128-byte swizzle matches the granule layout for 128-byte rows");
+    const int kchunks = kblocks / CKB;
+    const int my_tiles = (tiles > (int)blockIdx.x) ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int nchunks = my_tiles * kchunks;
+    uint8_t* gmaps = reinterpret_cast<uint8_t*>(p.tmaps) + (size_t)blockIdx.x * (TM_BLOCKS * 2 * 128);
+    auto gmap = [&](int b, int par) { return gmaps + (b * 2 + par) * 128; };
+#pragma unroll
+    for (int b = 0; b < TM_BLOCKS; ++b)
+      reinterpret_cast<uint32_t*>(base_ptr + (smaps + b * 128 - base))[lane] = reinterpret_cast<const uint32_t*>(&mapA)[lane];
+    __syncwarp();
+    const size_t srow = (size_t)p.K / 32;
+    const uint8_t* sc_t[TM_BLOCKS] = {nullptr, nullptr};  // the tile's scale tensors, at its first row
+    int cur_tile = -1, par = 1, tm = 0, n_issued = 0;
+#pragma unroll 1
+    for (int jc = 0; jc < nchunks && !*abort_flag; ++jc) {
+      const int slot = jc % RC;
+      // the slot's previous chunk (jc - RC) has been decoded by every producer warp
+      if (jc >= RC && !__all_sync(0xffffffffu, mbar_wait(raw_empty(slot), ((jc / RC) - 1) & 1, abort_flag))) break;
+      const int tile = blockIdx.x + (jc / kchunks) * gridDim.x, kc = jc % kchunks;
+      if (tile != cur_tile) {  // warp-uniform
+        const MxBatch* rec = p.batches + tile / mtiles;
+        const uint8_t* q0 = rec->w[blk_tensor(0)];
+        const uint8_t* q1 = rec->w[blk_tensor(1)];
+        if (((reinterpret_cast<uintptr_t>(q0) | reinterpret_cast<uintptr_t>(q1)) & 15u) != 0) {
+          // a TMA source must be 16-byte aligned: abandon the call
+          if (lane == 0) flag_status(p.status, K3MOE_DEV_ALIGN);
+          *abort_flag = 1;
+          break;
+        }
+        par ^= 1;
+        if (lane == 0) {
+          tmap_replace_addr(smaps, q0);
+          tmap_replace_addr(smaps + 128, q1);
+        }
+        __syncwarp();
+        tmap_store_release(gmap(0, par), smaps);
+        tmap_store_release(gmap(1, par), smaps + 128);
+        if (lane == 0) {
+          tmap_acquire(gmap(0, par));
+          tmap_acquire(gmap(1, par));
+        }
+        cur_tile = tile;
+        tm = tile % mtiles;
+#pragma unroll
+        for (int b = 0; b < TM_BLOCKS; ++b) sc_t[b] = rec->w[blk_tensor(b) + 1] + blk_row0(tm, b) * srow;
+      }
+      // scale bytes: 2 CKB per row, rows lane + 32 i of the slot's 256, by cp.async; each
+      // lane's arrival on raw_full fires once they land
+#pragma unroll
+      for (int i = 0; i < MROWS / 32; ++i) {
+        const int r = lane + 32 * i, b = r / TM_ROWS;
+        const uint8_t* ssrc = sc_t[b] + (size_t)(r % TM_ROWS) * srow + kc * (2 * CKB);
+        const uint32_t sdst = sraw_base + slot * Lay::SC_SLOT + r * (2 * CKB);
+        if constexpr (CKB == 4) cp_async8(sdst, ssrc);
+        else cp_async4(sdst, ssrc);
+      }
+      cp_async_mbar_arrive(raw_full(slot));
+      if (lane == 0) {
+        mbar_expect_tx(raw_full(slot), TM_BLOCKS * TM_ROWS * ROWB);
+#pragma unroll
+        for (int b = 0; b < TM_BLOCKS; ++b)
+          tma_load_2d(raw_base + slot * Lay::RAW_SLOT + b * TM_ROWS * ROWB, reinterpret_cast<const CUtensorMap*>(gmap(b, par)),
+                      kc * ROWB, (int)blk_row0(tm, b), raw_full(slot));
+      }
+      n_issued = jc + 1;
+    }
+    // let every issued copy land before the CTA exits (after an abort some are never
+    // consumed): the lanes' cp.async, then bounded waits on the last RC chunks
+    cp_async_wait<0>();
+    if (lane == 0) {
+      for (int j = (n_issued > RC ? n_issued - RC : 0); j < n_issued; ++j) {
+        const long long t0 = clock64();
+        while (!mbar_test(raw_full(j % RC), (j / RC) & 1) && clock64() - t0 < (1ll << 21)) {
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ decode producers (warps 11..18)
-    // The raw bytes of a tile travel in chunks of CKB k-blocks: CKB * 32 bytes of each of
-    // the tile's 256 rows.  Each producer warp copies the 32 rows it decodes (full
-    // 128-byte lines, eight lanes per line, 16-byte cp.async) into a ring of RC chunks and
-    // waits on its own copy groups, so the warps never wait for one another; 16-byte
-    // granules are XOR-swizzled by row so the decode reads are free of bank conflicts.
+    // A chunk's packed and scale bytes come from the copy warp (raw_full / raw_empty);
+    // 16-byte granules are XOR-swizzled by row so the decode reads are free of bank
+    // conflicts.
     // Decode: a warp owns the TMEM lane quarter warp % 4 (32 rows) of one block (warps
     // 11..14 block 0, 15..18 block 1), a k-block's 64 elements per thread (32 columns).
     const int qd = warp & 3;
     const int mb = (warp - (3 + TM_EPI)) >> 2;
     const int ri = mb * TM_ROWS + qd * 32 + lane;  // row of the tile (over both blocks)
-    const size_t qrow = (size_t)p.K / 2, srow = (size_t)p.K / 32;
     constexpr int CKB = Lay::CKB, ROWB = Lay::ROWB, GPR = Lay::GPR;
     // granule c of row r sits at position c ^ swz(r): conflict-free reads of 8 consecutive rows
     auto swz = [](int r) { return (GPR == 8) ? (r & 7) : ((r >> 1) & 3); };
@@ -772,46 +895,14 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
     const int my_tiles = (tiles > (int)blockIdx.x) ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int nchunks = my_tiles * kchunks;
     bool stop = false;
-    const int wr0 = mb * TM_ROWS + qd * 32;  // this warp's first row of the tile
-    // this warp's rows of the current tile: packed-byte and scale base pointers, loaded
-    // from the batch record once per tile (reloading them at every chunk put an L2 round
-    // trip in front of each chunk's copies)
-    int cur_tile = -1;
-    const uint8_t* qtile = nullptr;
-    const uint8_t* stile = nullptr;
-    auto issue = [&](int jc) {
-      if (jc < nchunks && !stop) {
-        const int tile = blockIdx.x + (jc / kchunks) * gridDim.x, kc = jc % kchunks;
-        if (tile != cur_tile) {
-          const MxBatch* rec = p.batches + tile / mtiles;
-          const size_t r0 = blk_row0(tile % mtiles, mb) + qd * 32;
-          qtile = rec->w[blk_tensor(mb)] + r0 * qrow;
-          stile = rec->w[blk_tensor(mb) + 1] + r0 * srow;
-          cur_tile = tile;
-        }
-        const uint8_t* q = qtile + kc * ROWB;
-        const uint32_t dst = raw_base + (jc % RC) * Lay::RAW_SLOT;
-#pragma unroll
-        for (int k = 0; k < 32 * GPR / 32; ++k) {
-          const int G = k * 32 + lane;  // 16-byte granule of this warp's 32 rows
-          const int r = G / GPR, gc = G % GPR, rr = wr0 + r;
-          cp_async16(dst + rr * ROWB + ((gc ^ swz(rr)) << 4), q + r * qrow + gc * 16);
-        }
-        const uint8_t* ssrc = stile + lane * srow + kc * (2 * CKB);
-        const uint32_t sdst = sraw_base + (jc % RC) * Lay::SC_SLOT + (wr0 + lane) * (2 * CKB);
-        if constexpr (CKB == 4) cp_async8(sdst, ssrc);
-        else cp_async4(sdst, ssrc);
-      }
-      cp_async_commit();
-    };
     bool bad = false;
 #pragma unroll 1
-    for (int j = 0; j < RC - 1; ++j) issue(j);
-#pragma unroll 1
     for (int jc = 0; jc < nchunks && !stop; ++jc) {
-      cp_async_wait<RC - 2>();  // chunk jc has landed (this thread's copies)
-      __syncwarp();             // ... the whole warp's, and the warp is done with chunk jc - 1
-      issue(jc + RC - 1);       // into the slot chunk jc - 1 used
+      // chunk jc's packed and scale bytes (the copy warp's) have landed
+      if (!__all_sync(0xffffffffu, mbar_wait(raw_full(jc % RC), (jc / RC) & 1, abort_flag))) {
+        stop = true;
+        break;
+      }
       const uint8_t* src = base_ptr + (raw_base - base) + (jc % RC) * Lay::RAW_SLOT + ri * ROWB;
       const uint8_t* scs = base_ptr + (sraw_base - base) + (jc % RC) * Lay::SC_SLOT + ri * (2 * CKB);
       uint2 sc8;
@@ -867,8 +958,10 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
         __syncwarp();
         if (lane == 0) mbar_arrive(full(st % NBS));
       }
+      // the warp's reads of this chunk's packed bytes are done (its last decode came before
+      // the TMEM store and the arrival above): the slot may be refilled
+      if (!stop && lane == 0) mbar_arrive(raw_empty(jc % RC));
     }
-    cp_async_wait<0>();
     if (bad) flag_status(p.status, K3MOE_DEV_SCALE_RANGE);
   }
   __syncthreads();

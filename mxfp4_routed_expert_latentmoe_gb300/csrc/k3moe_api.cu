@@ -22,7 +22,7 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 struct WsLayout {
   size_t status, logits, ids, w, zmax, zpow, counts, offsets, slot_of, slot_tok, inv, uniq, n_uniq, nb_prefix,
-      n_batches, cta_cnt, cta_base, batches, z, z16, h16, o, y, yhat, cpart, ccount, z16p, spow, total;
+      n_batches, cta_cnt, cta_base, batches, z, z16, h16, o, y, yhat, cpart, ccount, z16p, spow, tmaps, total;
 };
 
 WsLayout ws_layout(const k3moe_dims& d, int T) {
@@ -69,6 +69,7 @@ WsLayout ws_layout(const k3moe_dims& d, int T) {
   const bool tc = T >= 256;
   L.z16p = take(tc ? slots * Lt * 2 : 0);
   L.spow = take(tc ? slots * 4 : 0);
+  L.tmaps = take(tc ? (size_t)TM_MAX_CTAS * TM_BLOCKS * 2 * 128 : 0);  // packed-weight tensor maps
   L.total = off;
   return L;
 }
@@ -162,6 +163,19 @@ bool map_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// row-major [rows, cols] byte matrix, boxes of box_rows x 128 bytes with the 128-byte swizzle
+bool map_u8(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------------------- launch helpers
 // Launch with programmatic stream serialization: the kernel may start while its
 // predecessor finishes; it waits (griddepcontrol.wait) before reading its inputs.
@@ -233,11 +247,15 @@ bool map_f16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint
 // grouped MXFP4 expert GEMM on tcgen05; act [slots, K] f16 in slot order
 template <int MODE>
 cudaError_t launch_tc_moe(const __half* act, int slots, TcMoeParams p, int dev, int sms, cudaStream_t st, bool pdl) {
-  CUtensorMap mb;
+  CUtensorMap mb, ma;
   if (!map_f16(&mb, act, slots, p.K, TM_NB)) return cudaErrorInvalidValue;
+  // template of the packed-weight maps ([R, K/2] bytes, 128-row boxes): the kernel writes
+  // each expert tensor's address into its copies; the workspace stands in until then
+  if (!map_u8(&ma, p.tmaps, (uint64_t)p.R, (uint64_t)p.K / 2, TM_ROWS)) return cudaErrorInvalidValue;
   constexpr int smem = TmLayout<MODE>::SMEM;
   if (!set_smem<k3_tc_moe_kernel<MODE>>(dev, smem)) return cudaErrorInvalidValue;
-  return launch(k3_tc_moe_kernel<MODE>, dim3(sms), dim3(TM_THREADS), smem, st, pdl, mb, p);
+  const int grid = sms < TM_MAX_CTAS ? sms : TM_MAX_CTAS;
+  return launch(k3_tc_moe_kernel<MODE>, dim3(grid), dim3(TM_THREADS), smem, st, pdl, mb, ma, p);
 }
 
 // D[M, N0 (+N1)] = A[M, K] . [B0; B1]^T on tcgen05 (A, B bf16 row-major)
@@ -553,11 +571,11 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   // experts
   if (tc) {
     TcMoeParams gp{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.inter, d.latent,
-                   at<int32_t>(ws, L.spow), at<void>(ws, L.h16), status};
+                   at<int32_t>(ws, L.spow), at<void>(ws, L.h16), status, at<void>(ws, L.tmaps)};
     K3_TRY(launch_tc_moe<0>(at<__half>(ws, L.z16p), slots, gp, dev, sms, s, pdl));
     K3_TRY(mark(events, n_events, 3, s));
     TcMoeParams dp2{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.latent, d.inter, nullptr,
-                    at<void>(ws, L.o), status};
+                    at<void>(ws, L.o), status, at<void>(ws, L.tmaps)};
     K3_TRY(launch_tc_moe<1>(at<__half>(ws, L.h16), slots, dp2, dev, sms, s, pdl));
   } else {
     K3_TRY(launch_mx<MX_GATEUP>(mx_params(d, L, ws, MX_GATEUP, at<__half>(ws, L.z16), at<void>(ws, L.h16)), nblk,
