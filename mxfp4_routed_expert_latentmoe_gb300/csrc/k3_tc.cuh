@@ -551,6 +551,14 @@ K3_DEVI void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// An empty statement reading 32 registers: keeps the source of an in-flight tcgen05.st
+// allocated (the compiler does not know the store reads them until tcgen05.wait::st)
+K3_DEVI void keep_regs32(const uint32_t (&r)[32]) {
+  asm volatile("" ::"r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+               "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+               "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+               "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
+}
 K3_DEVI void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -909,8 +917,8 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       if constexpr (CKB == 4) sc8 = *reinterpret_cast<const uint2*>(scs);
       else sc8 = make_uint2(*reinterpret_cast<const uint32_t*>(scs), 0u);
       // decode k-block kq of the chunk (64 elements of row ri) into a[]: f16x2 columns
-      uint32_t a[32];
-      auto decode = [&](int kq) {
+      uint32_t a[32], a2[32];
+      auto decode = [&](int kq, uint32_t (&out)[32]) {
         const uint32_t cs = ((kq < 2) ? sc8.x : sc8.y) >> (16 * (kq & 1));  // this k-block's two scale bytes
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
@@ -928,32 +936,31 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h[e]), *reinterpret_cast<const __half2*>(&sc2));
-              a[g * 16 + cc * 4 + e] = *reinterpret_cast<uint32_t*>(&v);
+              out[g * 16 + cc * 4 + e] = *reinterpret_cast<uint32_t*>(&v);
             }
           }
         }
       };
-      // a tcgen05.st keeps its source registers until tcgen05.wait::st: decode, store, wait
+      // a tcgen05.st keeps its source registers until tcgen05.wait::st: the stage's second
+      // k-block is decoded into other registers while the first one's store is in flight
+      static_assert(TM_AKB == 2, "two k-blocks per A stage");
 #pragma unroll 1
       for (int h = 0; h < CKB / TM_AKB; ++h) {
         const int st = jc * (CKB / TM_AKB) + h, sa = st % SA;  // A stage and its slot
         const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + Lay::A_COL0 + (sa * TM_BLOCKS + mb) * Lay::A_COLS;
-#pragma unroll 1
-        for (int kk = 0; kk < TM_AKB; ++kk) {
-          decode(h * TM_AKB + kk);
-          if (kk == 0) {
-            // the slot's previous stage (st - SA) must have been consumed by the MMAs
-            const int j = st - SA;
-            if (j >= 0 && !__all_sync(0xffffffffu, mbar_wait(kdone(j % NBS), (j / NBS) & 1, abort_flag))) {
-              stop = true;
-              break;
-            }
-            tc_fence_after();
-          }
-          tmem_st32(ta + kk * 32, a);
-          tmem_st_wait();
+        decode(h * TM_AKB, a);
+        // the slot's previous stage (st - SA) must have been consumed by the MMAs
+        const int j = st - SA;
+        if (j >= 0 && !__all_sync(0xffffffffu, mbar_wait(kdone(j % NBS), (j / NBS) & 1, abort_flag))) {
+          stop = true;
+          break;
         }
-        if (stop) break;
+        tc_fence_after();
+        tmem_st32(ta, a);
+        decode(h * TM_AKB + 1, a2);
+        tmem_st32(ta + 32, a2);
+        tmem_st_wait();
+        keep_regs32(a);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(full(st % NBS));
