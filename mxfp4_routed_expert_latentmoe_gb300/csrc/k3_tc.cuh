@@ -423,6 +423,9 @@ namespace k3 {
 //       cvt.rn.f16x2.e2m1x2 gives the exact E2M1 values in f16 and one f16x2 multiply
 //       applies the power-of-two scale; exact for scale bytes 105..142 (the value set
 //       e2m1 * 2^k, k in [-23, 15]); other scale bytes set K3MOE_DEV_SCALE_RANGE;
+//       the vendor bytes reach shared memory through a chunk ring filled by a copy warp
+//       (TMA for the packed bytes, through tensor maps whose global address is set to
+//       the tile's expert tensor on the device; cp.async for the scale bytes);
 //   B = the batch's activation rows in slot order (f16, exactly prescaled by a power
 //       of two per token) loaded by TMA into shared memory (128-byte swizzle);
 //   fp32 accumulation in TMEM (kind::f16, M 128, N = tokens rounded up to 16).
