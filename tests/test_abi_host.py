@@ -40,6 +40,28 @@ def test_workspace_bytes_is_monotone_and_rejects_bad_dims():
     assert L.k3moe_workspace_bytes(ctypes.byref(d), -1) == 0
 
 
+def test_workspace_holds_the_tensor_core_path_buffers_from_256_tokens():
+    # from 256 tokens the grouped expert GEMM needs the slot-ordered f16 activations, their
+    # per-slot exponents and the weight tensor maps (256 CTAs x 2 blocks x 2 x 128 bytes);
+    # below that the workspace grows by the per-token buffers only
+    L = k3.lib()
+    d = _d()
+    ws = {T: L.k3moe_workspace_bytes(ctypes.byref(d), T) for T in (254, 255, 256)}
+    per_token = ws[255] - ws[254]
+    slots = 256 * 16
+    tc_bytes = slots * 3584 * 2 + slots * 4 + 256 * 2 * 2 * 128
+    assert ws[256] - ws[255] >= tc_bytes
+    assert ws[256] - ws[255] <= tc_bytes + 2 * per_token + 3 * 256
+
+
+def test_device_status_bits_match_the_header():
+    import re
+    text = open(k3._HEADER).read()
+    bits = {m.group(1): int(m.group(2), 16) for m in re.finditer(r"#define K3MOE_DEV_(\w+) (0x[0-9a-fA-F]+)u", text)}
+    assert bits == {"TIE_WINDOW": k3.DEV_TIE_WINDOW, "TIMEOUT": k3.DEV_TIMEOUT, "BAD_ID": k3.DEV_BAD_ID,
+                    "SCALE_RANGE": k3.DEV_SCALE_RANGE, "ALIGN": k3.DEV_ALIGN}
+
+
 def _route(d, T, x=16, wr=16, bias=16, ids=16, w=16, ws=16, ws_bytes=None):
     L = k3.lib()
     nb = ws_bytes if ws_bytes is not None else L.k3moe_workspace_bytes(ctypes.byref(d), T)
