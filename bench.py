@@ -59,6 +59,18 @@ def workload_cfg(name):
     return {"decode": C.DECODE, "chunk": C.CHUNK, "prefill": C.PREFILL}[name]
 
 
+def kernels_per_step(cfg, tc: bool) -> int:
+    """Kernel launches of one forward (the memsets are not kernels): up to 64 tokens the
+    routing runs as one fused kernel (6 in all); beyond, top-k, the permutation (four
+    kernels past 2 x 2048 routed slots, else one), the f16 activation prep and, on the
+    grouped-GEMM path, the slot-order gather, around the two projections, the two expert
+    kernels and the combine."""
+    if cfg.T <= 64:
+        return 6
+    perm = 4 if cfg.T * cfg.top_k > 2 * 2048 else 1
+    return 7 + perm + (1 if tc else 0)
+
+
 def uses_grouped_gemm(cfg) -> bool:
     """The library runs the experts on the grouped tcgen05 GEMM from 256 tokens on when both
     contraction lengths are multiples of 256; smaller batches stream the weights through
@@ -443,7 +455,7 @@ def run_ours(a, cfg, rank, world, local_rank):
             "expert_phase": {"us": expert_us, "GB_s": exp_bytes / (expert_us / 1e6) / 1e9,
                              "frac_hbm": exp_bytes / (expert_us / 1e6) / 1e9 / peaks["hbm_gbs"]},
             "phases": phases, "profiled_ms_per_step": profiled_ms, "clocks": clocks, "e2e": e2e,
-            "gpu_launches": (6 if cfg.T <= 64 else (9 if tc else 8)) * a.steps, "device_status": status}
+            "gpu_launches": kernels_per_step(cfg, tc) * a.steps, "device_status": status}
     if not a.no_cpu_baseline:
         v, cores, sample, el = oracle_sample(cfg, a.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample,
