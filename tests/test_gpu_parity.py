@@ -277,6 +277,21 @@ def test_forward_tensor_core_path_ragged_tokens(k3, prefill):
     assert rel_l2(got[rows], ref["out"]) <= REL_L2_BAR
 
 
+def test_misaligned_expert_tensor_sets_the_align_status(k3, prefill):
+    """From 256 tokens the grouped GEMM writes expert tensor addresses into its weight
+    tensor maps on the device.  Gate tensors 8 bytes off the 16-byte alignment the ABI
+    requires are refused by the kernel's own check before any copy: the status word gets
+    K3MOE_DEV_ALIGN and the call is abandoned (its outputs are invalid)."""
+    cfg = C.PREFILL.with_tokens(256, x_seed=11)
+    L = prefill.with_tokens(k3, cfg)
+    bases = L.pool.data_ptr() + torch.arange(L.pool.numel() // L.eb, dtype=torch.int64) * L.eb
+    bad = k3.ExpertTables(bases, L.offs, device="cuda")
+    bad.tables[0] += 8  # every expert's gate_q, 8 bytes into its own tensor
+    L.tables = bad
+    _, _, _, ws = L.forward(k3)
+    assert k3.device_status(ws) & k3.DEV_ALIGN
+
+
 def test_forward_prefill_sampled(k3, prefill):
     cfg = C.PREFILL
     L = prefill
