@@ -87,7 +87,10 @@ typedef enum {
  *   up_q[e]   [I, L/2], up_s[e]   [I, L/32]    up projection
  *   down_q[e] [L, I/2], down_s[e] [L, I/32]    down projection
  * A checkpoint that stores gate and up as one fused [2I, L] matrix (gate rows first)
- * passes up_q[e] = gate_q[e] + I*L/2 and up_s[e] = gate_s[e] + I*L/32. */
+ * passes up_q[e] = gate_q[e] + I*L/2 and up_s[e] = gate_s[e] + I*L/32.
+ * Every pointer in the tables must be 16-byte aligned like any other tensor; the host
+ * cannot see them, so the tensor-core path (T >= 256) checks the packed tensors on the
+ * device, reports K3MOE_DEV_ALIGN and abandons the call when one is not. */
 typedef struct {
   const uint8_t* const* gate_q;
   const uint8_t* const* gate_s;
