@@ -88,7 +88,20 @@ def unit_of(cfg):
     return ("tokens/s", True) if cfg.name == "prefill" else ("µs/token", False)
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest replica's time (the job ends when its last rank does): an all-reduce
+    MAX over the default process group (NCCL tensors on `device`, or CPU for gloo)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def metric_value(cfg, ms_per_step, world):
+    """Whole-job value of N replicas that each process cfg.T tokens per step."""
     if cfg.name == "prefill":
         return cfg.T * world / (ms_per_step / 1e3)
     return ms_per_step * 1e3 / (cfg.T * world)
@@ -376,11 +389,7 @@ def run_ours(a, cfg, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     w1 = time.time()
-    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev), world, dev)
     clocks = sampler.summary(w0, w1)
     # timed region 2: per-kernel durations, events recorded by the library between phases
     nph = len(k3.PHASES)
@@ -412,11 +421,7 @@ def run_ours(a, cfg, rank, world, local_rank):
             e1.synchronize()
             if s >= a.warmup:
                 ms_e2e.append(e0.elapsed_time(e1))
-        me = statistics.mean(ms_e2e)
-        if world > 1:
-            tt = torch.tensor([me], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            me = float(tt.item())
+        me = max_over_ranks(statistics.mean(ms_e2e), world, dev)
         e2e = {"value": metric_value(cfg, me, world), "unit": unit, "h2d_bytes_per_step": xh.numel() * 2,
                "d2h_bytes_per_step": oh.numel() * 4}
     sampler.stop()
