@@ -1,13 +1,18 @@
 #!/usr/bin/env python3
 """Benchmark of the K3-shape MXFP4 Stable LatentMoE routed-expert layer.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|chunk|prefill]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|decode|chunk|prefill]
                 [--impl ours|reference]
 
 One step = one k3moe_forward over one batch of synthetic tokens (router, top-k,
 permutation, latent down, expert gate/up + SiTU-GLU, expert down, combine, RMSNorm,
 latent up), inputs resident in HBM.  L2 is flushed (256 MiB write) before every timed
 step, outside the timed events.  Prints one JSON line (rank 0).
+
+The default (--workload all) times the three K3-shape workloads one after another:
+decode (1 token; the line's `value`, µs/token), then the 32-token chunk and the
+4096-token prefill (`chunk` and `prefill` objects of the same line, with their own
+value, roofline, phases, end-to-end time and oracle baseline).
 
 --impl reference times the fp64 oracle on the host cores (the only reference this
 method has), on a bounded sample of the same workload.
@@ -20,6 +25,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -32,24 +38,27 @@ if ROOT not in sys.path:
 
 METRIC = "K3-shape MXFP4 LatentMoE layer: decode µs/token (HBM GB/s), prefill tokens/s"
 FLUSH_BYTES = 256 << 20
+WORKLOADS = ("decode", "chunk", "prefill")
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", choices=("decode", "chunk", "prefill"), default="decode")
+    ap.add_argument("--workload", choices=("all",) + WORKLOADS, default="all")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU work of the oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+                    help="target CPU work of the oracle baseline, per workload and thread count")
     ap.add_argument("--no-graph", action="store_true", help="launch the forward eagerly instead of replaying a graph")
     ap.add_argument("--n-experts", type=int, default=None,
                     help="profiling case: a smaller expert pool with the same per-expert shapes and top-k")
     ap.add_argument("--tokens", type=int, default=None,
                     help="profiling case: this many tokens instead of the workload's")
-    a = ap.parse_args()
+    ap.add_argument("--oracle-sample", choices=WORKLOADS, default=None, help=argparse.SUPPRESS)
+    a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
     return a
 
@@ -59,16 +68,31 @@ def workload_cfg(name):
     return {"decode": C.DECODE, "chunk": C.CHUNK, "prefill": C.PREFILL}[name]
 
 
+def selected_cfgs(a):
+    """(name, config) of every workload this run times; the first one is the line's headline."""
+    import dataclasses
+    names = WORKLOADS if a.workload == "all" else (a.workload,)
+    out = []
+    for n in names:
+        cfg = workload_cfg(n)
+        if a.n_experts:
+            cfg = dataclasses.replace(cfg, n_experts=a.n_experts, name=cfg.name)
+        if a.tokens:
+            cfg = cfg.with_tokens(a.tokens, x_seed=cfg.x_seed)
+        out.append((n, cfg))
+    return out
+
+
 def kernels_per_step(cfg, tc: bool) -> int:
     """Kernel launches of one forward (the memsets are not kernels): up to 64 tokens the
     routing runs as one fused kernel (6 in all); beyond, top-k, the permutation (four
-    kernels past 2 x 2048 routed slots, else one), the f16 activation prep and, on the
-    grouped-GEMM path, the slot-order gather, around the two projections, the two expert
-    kernels and the combine."""
+    kernels past 2 x 2048 routed slots, else one) and the activation prep (the f16 copy
+    of z for the weight-streaming kernels, or on the grouped-GEMM path the slot-order
+    gather), around the two projections, the two expert kernels and the combine."""
     if cfg.T <= 64:
         return 6
     perm = 4 if cfg.T * cfg.top_k > 2 * 2048 else 1
-    return 7 + perm + (1 if tc else 0)
+    return 7 + perm
 
 
 def uses_grouped_gemm(cfg) -> bool:
@@ -126,6 +150,19 @@ def algorithmic(cfg, n_unique):
     }
 
 
+def step_flops(cfg):
+    """Algorithmic flops of one forward: router + latent down, experts, latent up."""
+    T, H, L, E, K, I = cfg.T, cfg.hidden, cfg.latent, cfg.n_experts, cfg.top_k, cfg.inter
+    return 2 * T * (E * H + 2 * L * H + K * (2 * I * L + L * I))
+
+
+def step_bytes(cfg, n_unique):
+    """Algorithmic HBM bytes of one forward: dense weights once, the selected experts once."""
+    gu, dn = expert_bytes(cfg)
+    T, H, L, E = cfg.T, cfg.hidden, cfg.latent, cfg.n_experts
+    return (E * H + 2 * L * H) * 2 + n_unique * (gu + dn) + T * H * (2 + 4)
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -144,9 +181,9 @@ def csrc_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_phase, workload):
-    """dram bytes per launch recorded by an ncu capture under profiles/, if the kernel
-    sources are unchanged since the capture."""
+def profiled(kernel_phase, workload):
+    """Figures recorded by an ncu capture under profiles/ (key: value lines), if the kernel
+    sources are unchanged since the capture; else None."""
     path = os.path.join(ROOT, "profiles", f"{kernel_phase}_{workload}.md")
     try:
         kv = {}
@@ -156,9 +193,34 @@ def profiled_traffic(kernel_phase, workload):
                 kv[k.strip()] = v.strip()
         if kv.get("source_sha256_16") != csrc_hash():
             return None
-        return int(kv["dram_bytes_per_launch"])
+        return kv
     except Exception:
         return None
+
+
+def profiled_traffic(kernel_phase, workload):
+    kv = profiled(kernel_phase, workload)
+    try:
+        return int(kv["dram_bytes_per_launch"]) if kv else None
+    except (KeyError, ValueError):
+        return None
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
 
 
 # ------------------------------------------------------------------------------ raw CUDA events
@@ -220,12 +282,13 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self, t0, t1):
+    def summary(self, windows):
+        """Clock summary over the samples inside the given (t0, t1) windows."""
         if not self.samples:
             return None
-        win = [p for (t, p) in self.samples if t0 <= t <= t1]
-        if not win:  # timed region shorter than the sampling period: nearest samples
-            win = [min(self.samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))[1]]
+        win = [p for (t, p) in self.samples if any(t0 <= t <= t1 for (t0, t1) in windows)]
+        if not win:  # timed regions shorter than the sampling period: nearest samples
+            win = [min(self.samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))[1] for (t0, t1) in windows]
 
         def num(x):
             try:
@@ -235,13 +298,14 @@ class ClockSampler:
 
         sm = [num(p[1]) for p in win if num(p[1]) is not None]
         mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        pw = [num(p[3]) for p in win if num(p[3]) is not None]
         reasons = set()
         for p in win:
             for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), p[5:9]):
                 if v.strip().lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(win)}
+                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons), "samples": len(win)}
 
 
 # ------------------------------------------------------------------------------ oracle timing
@@ -271,7 +335,26 @@ def oracle_sample(cfg, seconds_target: float, min_tokens=1, max_tokens=64):
     rows = list(range(n)) if n <= T else [i % T for i in range(n)]
     el = run(rows)
     val = (n / el) if cfg.name == "prefill" else (el / n * 1e6)
-    return val, oracle.threads_used(), f"{n} token(s) of the {cfg.name} workload, token at a time", el
+    return val, oracle.threads_used(), f"the first {n} token(s) of the {cfg.name} workload, token at a time", el
+
+
+def oracle_baseline(cfg, unit, seconds):
+    """The oracle on all host cores (in this process) and on one core (a child process
+    with OMP_NUM_THREADS=1), each on a bounded token sample."""
+    v, cores, sample, el = oracle_sample(cfg, seconds)
+    out = {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample, "seconds": el,
+           "cpu": cpu_model()}
+    try:
+        env = dict(os.environ, OMP_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", cfg.name,
+                            "--cpu-seconds", str(seconds)], capture_output=True, text=True, env=env,
+                           timeout=20 * seconds + 120)
+        one = json.loads(r.stdout.strip().splitlines()[-1])
+        out["single_thread"] = {"value": one["value"], "unit": unit, "cores": one["cores"], "sample": one["sample"],
+                                "seconds": one["seconds"]}
+    except Exception as e:  # the all-core figure stands on its own
+        out["single_thread"] = {"error": f"{type(e).__name__}: {e}"[:200]}
+    return out
 
 
 # ------------------------------------------------------------------------------ reference arm
@@ -311,29 +394,28 @@ def run_reference(a, cfg, rank, world):
             "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": hib, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
             "config": {"workload": describe(cfg), "sample_tokens_per_step": per_step},
-            "cpu_baseline": {"value": val, "unit": unit, "cores": cores, "kind": "oracle",
+            "cpu_baseline": {"value": val, "unit": unit, "cores": cores, "kind": "oracle", "cpu": cpu_model(),
                              "sample": f"{per_step} token(s) per step of the {cfg.name} workload"},
             "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------------------ our arm
-def run_ours(a, cfg, rank, world, local_rank):
+def measure(a, cfg, k3, dev, world, pools, sampler):
+    """Times one workload: the forward replayed from a CUDA graph (the figure), the same
+    forward with per-phase events, and the end-to-end call with host buffers."""
     import numpy as np
     import torch
     import torch.distributed as dist
-
-    import __graft_entry__ as g
-    g.build()
-    import mxfp4_routed_expert_latentmoe_gb300 as k3
     from datagen import device as D
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
     unit, hib = unit_of(cfg)
     d = k3.dims(**cfg.dims)
     t = D.layer_tensors(cfg, dev)
-    pool, eb, offs = D.expert_pool(cfg, dev)
+    key = (cfg.seed, cfg.scale_lo, cfg.scale_hi, cfg.n_experts, cfg.latent, cfg.inter)
+    if key not in pools:
+        pools[key] = D.expert_pool(cfg, dev)
+    pool, eb, offs = pools[key]
     tables = k3.ExpertTables.from_pool(pool, eb, offs)
     T = cfg.T
     out = torch.empty(T, cfg.hidden, dtype=torch.float32, device=dev)
@@ -354,7 +436,7 @@ def run_ours(a, cfg, rank, world, local_rank):
     status = k3.device_status(ws)
     n_unique = int(np.unique(ids.cpu().numpy()).size)
 
-    # the headline step: one k3moe_forward captured into a CUDA graph (its kernels and
+    # the timed step: one k3moe_forward captured into a CUDA graph (its kernels and
     # memsets, chained with programmatic dependent launch) and replayed
     step = lambda: k3.forward(*args, ids_out=ids, w_out=wts)
     graph = None
@@ -372,11 +454,7 @@ def run_ours(a, cfg, rank, world, local_rank):
             flush.zero_()
             step()
         torch.cuda.synchronize()
-    gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
-    sampler = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}")
-    time.sleep(0.3)
-    # timed region 1: the headline number, plain k3moe_forward (kernels chained with
-    # programmatic dependent launch), one event pair per step
+    time.sleep(0.05)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
     barrier()
     torch.cuda.synchronize()
@@ -390,8 +468,7 @@ def run_ours(a, cfg, rank, world, local_rank):
     barrier()
     w1 = time.time()
     ms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev), world, dev)
-    clocks = sampler.summary(w0, w1)
-    # timed region 2: per-kernel durations, events recorded by the library between phases
+    # per-kernel durations: events recorded by the library between phases, on its stream
     nph = len(k3.PHASES)
     pev = [RawEvents(nph + 1) for _ in range(a.steps)]
     torch.cuda.synchronize()
@@ -402,7 +479,7 @@ def run_ours(a, cfg, rank, world, local_rank):
     phase_ms = {name: statistics.mean(pev[s].ms(i, i + 1) for s in range(a.steps)) for i, name in enumerate(k3.PHASES)}
     profiled_ms = statistics.mean(pev[s].ms(0, nph) for s in range(a.steps))
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: H2D of x, the forward, D2H of out
     e2e = None
     if not a.no_e2e:
         xh = t["x"].cpu().pin_memory()
@@ -423,26 +500,29 @@ def run_ours(a, cfg, rank, world, local_rank):
                 ms_e2e.append(e0.elapsed_time(e1))
         me = max_over_ranks(statistics.mean(ms_e2e), world, dev)
         e2e = {"value": metric_value(cfg, me, world), "unit": unit, "h2d_bytes_per_step": xh.numel() * 2,
-               "d2h_bytes_per_step": oh.numel() * 4}
-    sampler.stop()
+               "d2h_bytes_per_step": oh.numel() * 4, "ms_per_step": me}
+    del ws, flush
+    torch.cuda.empty_cache()
 
-    if rank != 0:
-        return
     peaks, peak_kind = measured_peaks()
     alg = algorithmic(cfg, n_unique)
     dom = "gateup"
     tc = uses_grouped_gemm(cfg)
     if tc:
+        # the grouped GEMM runs for milliseconds inside a step of a few milliseconds: the
+        # burst bf16 peak is its denominator
         achieved = alg[dom]["flops"] / (phase_ms[dom] / 1e3) / 1e12
-        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+        peak = peaks["bf16_tflops"]
+        kv = profiled(dom, cfg.name) or {}
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": profiled_traffic(dom, cfg.name), "kernel": "k3_tc_moe_kernel<0> (gate/up)",
-                "peak_kind": f"{peak_kind} bf16 sustained"}
+                "peak_kind": f"{peak_kind} bf16 burst",
+                "tensor_pipe_active_pct": float(kv["tensor_pipe_active_pct"]) if "tensor_pipe_active_pct" in kv else None}
     else:
         achieved = alg[dom]["bytes"] / (phase_ms[dom] / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(dom, cfg.name), "kernel": "k3_mx_gemv_kernel<gate/up>",
+                "traffic": profiled_traffic(dom, cfg.name), "kernel": "k3_mxb_gemv_kernel<gate/up>",
                 "peak_kind": f"{peak_kind} HBM copy"}
     phases = {k: {"us": v * 1e3,
                   "GB_s": (alg[k]["bytes"] / (v / 1e3) / 1e9) if k in alg else None,
@@ -450,37 +530,86 @@ def run_ours(a, cfg, rank, world, local_rank):
               for k, v in phase_ms.items()}
     expert_us = (phase_ms["gateup"] + phase_ms["down"]) * 1e3
     exp_bytes = alg["gateup"]["bytes"] + alg["down"]["bytes"]
-    line = {"metric": METRIC, "value": metric_value(cfg, ms, world), "unit": unit, "n_gpus": world,
-            "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": hib, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": describe(cfg), "global_batch": cfg.T * world, "seq_len": cfg.T,
-                       "parallelism": f"replicas x{world}", "l2": "flushed by a 256 MiB write before every timed step",
-                       "unique_experts": n_unique, "cuda_graph": graph is not None},
-            "roofline": roof,
-            "expert_phase": {"us": expert_us, "GB_s": exp_bytes / (expert_us / 1e6) / 1e9,
-                             "frac_hbm": exp_bytes / (expert_us / 1e6) / 1e9 / peaks["hbm_gbs"]},
-            "phases": phases, "profiled_ms_per_step": profiled_ms, "clocks": clocks, "e2e": e2e,
-            "gpu_launches": kernels_per_step(cfg, tc) * a.steps, "device_status": status}
+    res = {"value": metric_value(cfg, ms, world), "unit": unit, "higher_is_better": hib, "ms_per_step": ms,
+           "config": {"workload": describe(cfg), "global_batch": cfg.T * world, "seq_len": cfg.T,
+                      "parallelism": f"replicas x{world}", "l2": "flushed by a 256 MiB write before every timed step",
+                      "unique_experts": n_unique, "cuda_graph": graph is not None},
+           "roofline": roof,
+           "layer": {"GB_s": step_bytes(cfg, n_unique) / (ms / 1e3) / 1e9,
+                     "frac_hbm": step_bytes(cfg, n_unique) / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                     "TFLOP_s": step_flops(cfg) / (ms / 1e3) / 1e12,
+                     "frac_bf16_burst": step_flops(cfg) / (ms / 1e3) / 1e12 / peaks["bf16_tflops"]},
+           "expert_phase": {"us": expert_us, "GB_s": exp_bytes / (expert_us / 1e6) / 1e9,
+                            "frac_hbm": exp_bytes / (expert_us / 1e6) / 1e9 / peaks["hbm_gbs"]},
+           "phases": phases, "profiled_ms_per_step": profiled_ms, "e2e": e2e,
+           "gpu_launches": kernels_per_step(cfg, tc) * a.steps, "device_status": status,
+           "_window": (w0, w1)}
+    return res
+
+
+def run_ours(a, cfgs, rank, world, local_rank):
+    import torch
+
+    import __graft_entry__ as g
+    g.build()
+    import mxfp4_routed_expert_latentmoe_gb300 as k3
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(gpu_uuid if gpu_uuid.startswith("GPU-") else f"GPU-{gpu_uuid}")
+    time.sleep(0.3)
+    pools = {}
+    results = {}
+    for name, cfg in cfgs:
+        results[name] = measure(a, cfg, k3, dev, world, pools, sampler)
+    time.sleep(0.1)
+    sampler.stop()
+    for r in results.values():
+        r["clocks"] = sampler.summary([r.pop("_window")])
+    per = [v["clocks"] for v in results.values()]
+    if rank != 0:
+        return
     if not a.no_cpu_baseline:
-        v, cores, sample, el = oracle_sample(cfg, a.cpu_seconds)
-        line["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample,
-                                "seconds": el}
+        for name, cfg in cfgs:
+            results[name]["cpu_baseline"] = oracle_baseline(cfg, results[name]["unit"], a.cpu_seconds)
+    head_name, head_cfg = cfgs[0]
+    head = results[head_name]
+    # the line's clocks: every timed region of the run
+    reasons = sorted({x for c in per if c for x in c["reasons"]})
+    sm = [c["sm_mhz"] for c in per if c and c["sm_mhz"] is not None]
+    clocks = {"sm_mhz": statistics.median(sm) if sm else None,
+              "sm_max_mhz": max((c["sm_max_mhz"] for c in per if c and c["sm_max_mhz"]), default=None),
+              "reasons": reasons, "per_workload": {n: results[n]["clocks"] for n, _ in cfgs}}
+    line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": head["higher_is_better"],
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(head["config"], timed_workloads=[n for n, _ in cfgs]),
+            "roofline": head["roofline"], "layer": head["layer"], "expert_phase": head["expert_phase"],
+            "phases": head["phases"], "profiled_ms_per_step": head["profiled_ms_per_step"], "clocks": clocks,
+            "e2e": head["e2e"], "gpu_launches": sum(results[n]["gpu_launches"] for n, _ in cfgs),
+            "device_status": head["device_status"]}
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    for name, _cfg in cfgs[1:]:
+        r = dict(results[name])
+        line[name] = r
     print(json.dumps(line), flush=True)
 
 
 def main():
     a = parse()
+    if a.oracle_sample:  # child of oracle_baseline: one oracle sample, one JSON line
+        cfg = workload_cfg(a.oracle_sample)
+        v, cores, sample, el = oracle_sample(cfg, a.cpu_seconds)
+        print(json.dumps({"value": v, "cores": cores, "sample": sample, "seconds": el}), flush=True)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    cfg = workload_cfg(a.workload)
-    if a.n_experts:
-        import dataclasses
-        cfg = dataclasses.replace(cfg, n_experts=a.n_experts, name=cfg.name)
-    if a.tokens:
-        cfg = cfg.with_tokens(a.tokens, x_seed=cfg.x_seed)
+    cfgs = selected_cfgs(a)
     if a.impl == "reference":
-        run_reference(a, cfg, rank, world)
+        run_reference(a, cfgs[0][1], rank, world)
         return
     if world > 1:
         import torch
@@ -488,7 +617,7 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
-        run_ours(a, cfg, rank, world, local_rank)
+        run_ours(a, cfgs, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

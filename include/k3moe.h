@@ -74,9 +74,8 @@ typedef enum {
                                      exact ranking for that token */
 #define K3MOE_DEV_TIMEOUT 0x2u    /* a device-side bounded wait ran out; outputs are invalid */
 #define K3MOE_DEV_BAD_ID 0x4u     /* an expert id outside [0, E) reached the permutation */
-#define K3MOE_DEV_SCALE_RANGE 0x8u /* the tensor-core expert path (T >= 256) met a scale byte
-                                      outside 105..142, where its f16 weight decode is not
-                                      exact; the affected outputs are approximate */
+#define K3MOE_DEV_SCALE_RANGE 0x8u /* never set: every path decodes every scale byte exactly
+                                      (the value is kept so that the bit stays reserved) */
 #define K3MOE_DEV_ALIGN 0x10u      /* the tensor-core expert path (T >= 256) met an expert weight
                                       tensor that is not 16-byte aligned; the call was abandoned
                                       and its outputs are invalid */
@@ -111,8 +110,10 @@ size_t k3moe_workspace_bytes(const k3moe_dims* dims, int32_t T);
  *   ids   [T, K] int32   out: selected experts, descending biased score
  *   w     [T, K] f32     out: renormalised raw scores
  * Logits are accumulated in fp32; candidates whose biased scores lie within 3e-5
- * of a neighbour among the top K+1 are re-ranked from fp64 logits, so the ids
- * equal an exact-arithmetic ranking unless a gap is below fp64 resolution.
+ * of a neighbour in a cluster reaching the top K+1 get their logits recomputed from
+ * the bf16 inputs in double-f32 arithmetic (error-free sums, about 48 significant
+ * bits) and are re-ranked, so the ids equal an exact-arithmetic ranking unless two
+ * biased scores differ by less than about 1e-12.
  * T = 0 is a valid no-op.  `stream` is a cudaStream_t (NULL = legacy default). */
 k3moe_status k3moe_route(const k3moe_dims* dims, int32_t T, const uint16_t* x, const uint16_t* wr,
                          const float* bias, int32_t* ids, float* w, void* ws, size_t ws_bytes, void* stream);
@@ -145,23 +146,29 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
                                     float* w_out, void* ws, size_t ws_bytes, void* stream, void* const* events,
                                     int32_t n_events);
 
+/* Size in bytes of the fixed device scratch array that k3moe_forward_noalloc uses. */
+#define K3MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+
 /* k3moe_forward for callers that cannot allocate device memory: no workspace
  * argument, and no cudaMalloc / cudaFree or allocating library call inside.  This
  * suits code that runs where the allocator is off limits, e.g. a plugin inside a
  * host framework that owns every device allocation, or a path that must not touch
  * the allocator once it is set up.  The pages have no counterpart to this entry
  * point; it is a packaging variant of k3moe_forward.
- *  - Scratch lives in one fixed 4 MiB array in device memory that every GPU which
- *    loads the library holds until the process exits; that is enough for K3 shapes
- *    (H 7168, L 3584, E 896, K 16, I 3072) up to 8 tokens per call.  A call whose
- *    dims and T need more scratch than that (k3moe_workspace_bytes) returns
- *    K3MOE_ERR_WORKSPACE and launches nothing.
+ *  - Scratch lives in one fixed array of K3MOE_NOALLOC_SCRATCH_BYTES (4 MiB) in device
+ *    memory that every GPU which loads the library holds until the process exits.  A
+ *    call fits when k3moe_workspace_bytes(dims, T) is at most that size: at K3 shapes
+ *    (H 7168, L 3584, E 896, K 16, I 3072) that is up to 11 tokens per call.  A call
+ *    that needs more returns K3MOE_ERR_WORKSPACE and launches nothing.
  *  - The first call on a device looks up the array's device address with
  *    cudaGetSymbolAddress (with that device current); make that first call before
- *    any stream capture.
+ *    any stream capture.  The lookup is repeated only if the device's context has
+ *    changed since (e.g. after cudaDeviceReset).
  *  - Every call shares the array and leaves its contents behind (the call clears
  *    what must start at zero).  Calls that overlap on the GPU, on any stream, race
  *    on the array: serialise them.
+ *  - Conditions that only the device sees go to the status word at the start of the
+ *    array: read it with k3moe_device_status(NULL, ...).
  * Arguments, results and other errors are those of k3moe_forward. */
 k3moe_status k3moe_forward_noalloc(const k3moe_dims* dims, int32_t T, const uint16_t* x, const uint16_t* wr,
                                    const float* bias, const uint16_t* w_down, const uint16_t* w_up,
@@ -193,7 +200,8 @@ k3moe_status k3moe_permute(const k3moe_dims* dims, int32_t T, const int32_t* ids
                            size_t ws_bytes, void* stream);
 
 /* Reads the device status word of the last call that used `ws` (K3MOE_DEV_* bits)
- * into *host_out.  Synchronises `stream`. */
+ * into *host_out.  ws = NULL reads the status word of the last
+ * k3moe_forward_noalloc call on the current device.  Synchronises `stream`. */
 k3moe_status k3moe_device_status(const void* ws, uint32_t* host_out, void* stream);
 
 /* Intermediate tensors of the last k3moe_forward that used `ws`, for inspection:

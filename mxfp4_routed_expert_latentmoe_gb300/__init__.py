@@ -22,6 +22,8 @@ _HEADER = os.path.join(_ROOT, "include", "k3moe.h")
 _lock = threading.Lock()
 _lib = None
 
+NOALLOC_SCRATCH_BYTES = 4 << 20  # K3MOE_NOALLOC_SCRATCH_BYTES
+
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-shared"]
 
@@ -209,6 +211,8 @@ def permute(d: Dims, ids, counts, offsets, slot_of, uniq, n_uniq, ws, stream=Non
 
 
 def device_status(ws, stream=None) -> int:
+    """K3MOE_DEV_* bits of the last call that used workspace `ws`; ws=None reads the
+    status of the last k3moe_forward_noalloc call on the current device."""
     v = ctypes.c_uint32(0)
     _check(lib().k3moe_device_status(_ptr(ws), ctypes.byref(v), _stream(stream)), "k3moe_device_status")
     return int(v.value)

@@ -115,6 +115,43 @@ K3_DEVI float sigmoidf_(float a) { return 1.0f / (1.0f + expf(-a)); }
 // SiTU-GLU, 4 tanh(g/4) sigmoid(g) * 25 tanh(u/25)
 K3_DEVI float situf(float g, float u) { return 4.0f * tanhf(g * 0.25f) * sigmoidf_(g) * (25.0f * tanhf(u / 25.0f)); }
 
+// e^x - 1 to a few ulp without cancellation near 0: the Taylor series through x^9 for
+// |x| < 1/2 (truncation below 1e-9 relative), expf(x) - 1 elsewhere.
+K3_DEVI float expm1_k3(float x) {
+  float t = 1.0f / 362880.0f;
+  t = fmaf(t, x, 1.0f / 40320.0f);
+  t = fmaf(t, x, 1.0f / 5040.0f);
+  t = fmaf(t, x, 1.0f / 720.0f);
+  t = fmaf(t, x, 1.0f / 120.0f);
+  t = fmaf(t, x, 1.0f / 24.0f);
+  t = fmaf(t, x, 1.0f / 6.0f);
+  t = fmaf(t, x, 0.5f);
+  t = fmaf(t, x, 1.0f);
+  const float small = t * x;
+  return (fabsf(x) < 0.5f) ? small : expf(x) - 1.0f;
+}
+// SiTU-GLU from two exponentials per element pair:  with P = e^(g/2), A = P - 1 and
+// B = e^(2u/25) - 1,
+//   tanh(g/4) = A / (A + 2),  sigmoid(g) = P^2 / (P^2 + 1),  tanh(u/25) = B / (B + 2),
+// so h = 100 * A/(A+2) * P^2/(P^2+1) * B/(B+2).  A comes from the series near g = 0 (no
+// cancellation in e^(g/2) - 1) and P from expf elsewhere (no cancellation in A + 1 for
+// negative g, where sigmoid(g) is tiny): a few f32 ulp everywhere until P^2 underflows
+// (g < -87, |h| < 1e-36).  g is clamped to 80 and u/25 to [-40, 40], where every factor
+// is already 1 (or -1) in f32; NaN passes through.
+K3_DEVI float situ_fast(float g, float u) {
+  g = (g > 80.0f) ? 80.0f : g;
+  float v = u * 0.08f;  // 2u/25
+  v = (v > 80.0f) ? 80.0f : ((v < -80.0f) ? -80.0f : v);
+  const float x = 0.5f * g;
+  const float A = expm1_k3(x), B = expm1_k3(v);
+  const float P = (fabsf(x) < 0.5f) ? A + 1.0f : expf(x);
+  const float P2 = P * P;
+  return 100.0f * __fdividef(A, A + 2.0f) * __fdividef(P2, P2 + 1.0f) * __fdividef(B, B + 2.0f);
+}
+
+// 2^e as f32 for e in [-126, 127]
+K3_DEVI float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
 K3_DEVI uint16_t f32_to_bf16_bits(float v) {
   __nv_bfloat16 b = __float2bfloat16_rn(v);
   return *reinterpret_cast<uint16_t*>(&b);

@@ -914,19 +914,21 @@ __global__ void k3_z16_kernel(Z16Params p) {
 }
 
 // ============================================================================ slot-order activation rows
-// act16_perm[s] = z16[slot_tok[s]] and slot_pow[s] = pow2[slot_tok[s]] for every routed
-// slot (the B operand rows of the tensor-core expert GEMM, one expert's tokens contiguous)
-__global__ void k3_gather_rows_kernel(const __half* z16, const int32_t* pow2, const int32_t* slot_tok, int slots, int L,
-                                      __half* out, int32_t* slot_pow) {
+// act[s] = z[slot_tok[s]] for every routed slot: the B operand rows of the tensor-core
+// expert GEMM (one expert's tokens contiguous), bf16, each group of 8 elements stored in
+// the interleaved order 0, 4, 1, 5, 2, 6, 3, 7 that the GEMM's weight decode produces.
+__global__ void k3_gather_rows_kernel(const uint16_t* z, const int32_t* slot_tok, int slots, int L, uint16_t* out) {
   grid_dep_wait();
   grid_dep_launch();
-  const int per = L / 8;  // 16-byte chunks per row
+  const int per = L / 8;  // 16-byte chunks (8 elements) per row
   const size_t total = (size_t)slots * per;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const int s = (int)(i / per), c = (int)(i - (size_t)s * per);
     const int t = __ldg(slot_tok + s);
-    reinterpret_cast<uint4*>(out + (size_t)s * L)[c] = __ldg(reinterpret_cast<const uint4*>(z16 + (size_t)t * L) + c);
-    if (c == 0) slot_pow[s] = __ldg(pow2 + t);
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(z + (size_t)t * L) + c);  // [e0 e1] [e2 e3] [e4 e5] [e6 e7]
+    reinterpret_cast<uint4*>(out + (size_t)s * L)[c] =
+        make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632), __byte_perm(v.y, v.w, 0x5410),
+                   __byte_perm(v.y, v.w, 0x7632));
   }
 }
 

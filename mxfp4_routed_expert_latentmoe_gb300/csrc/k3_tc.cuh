@@ -419,22 +419,31 @@ namespace k3 {
 // Per token batch (up to TM_NB tokens of one expert) and 128-row tile of the expert's
 // weight matrix:  D[rows, tokens] = W[rows, K] . Act[tokens, K]^T  with
 //   A = W decoded by producer warps from the vendor MXFP4 bytes into TENSOR MEMORY
-//       (tcgen05.st; row i in lane i, two f16 per 32-bit column, K along columns):
-//       cvt.rn.f16x2.e2m1x2 gives the exact E2M1 values in f16 and one f16x2 multiply
-//       applies the power-of-two scale; exact for scale bytes 105..142 (the value set
-//       e2m1 * 2^k, k in [-23, 15]); other scale bytes set K3MOE_DEV_SCALE_RANGE;
+//       (tcgen05.st; row i in lane i, two bf16 per 32-bit column, K along columns):
+//       integer operations place each E2M1 code's sign, exponent and mantissa bits in
+//       a bf16 word (the value v * 2^-126, exact, subnormal for the code 0.5), and one
+//       bf16x2 multiply by a power of two (two when the scale byte exceeds 128) gives
+//       v * 2^(s-127), exact in bf16 for every scale byte 0..252 (every e2m1 value
+//       times 2^k with k in [-127, 125] is a bf16 number);
 //       the vendor bytes reach shared memory through a chunk ring filled by a copy warp
 //       (TMA for the packed bytes, through tensor maps whose global address is set to
 //       the tile's expert tensor on the device; cp.async for the scale bytes);
-//   B = the batch's activation rows in slot order (f16, exactly prescaled by a power
-//       of two per token) loaded by TMA into shared memory (128-byte swizzle);
-//   fp32 accumulation in TMEM (kind::f16, M 128, N = tokens rounded up to 16).
+//   B = the batch's activation rows in slot order (the bf16 values themselves) loaded
+//       by TMA into shared memory (128-byte swizzle);
+//   fp32 accumulation in TMEM (kind::f16 with bf16 A and B, M 128, N = tokens rounded
+//   up to 16).
+// Both operands hold the K dimension in the same interleaved order: within every group
+// of 8 consecutive elements, positions 0..7 hold elements 0, 4, 1, 5, 2, 6, 3, 7 (the
+// order in which one 32-bit word of packed codes decodes into four bf16 pairs with
+// the same shifts in both halves).  A dot product does not depend on the order of its
+// terms' positions, so the products are those of the natural order; the activation
+// rows are written in this order by the gather (z) and by the gate/up epilogue (h).
 // Keeping A out of shared memory leaves shared-memory bandwidth to B and the raw bytes
 // (with A in shared memory the decoded tile is written and then read again by the
 // tensor core, which made the kernel shared-memory bound at these small N).
 // GATEUP: two matrices (gate rows, up rows) share B; the epilogue applies SiTU-GLU,
-// rounds h to bf16 and stores it (x 2^8, f16) in slot order.  DOWN: one matrix; the
-// epilogue stores o (fp32) in slot order.
+// rounds h to bf16 and stores it in slot order (interleaved K order, for the down
+// GEMM).  DOWN: one matrix; the epilogue stores o (fp32) in slot order.
 constexpr int TM_ROWS = 128;       // weight rows per MMA (M)
 constexpr int TM_BLOCKS = 2;       // row blocks per tile, each with its own accumulator and MMA issuer
 constexpr int TM_NB = 96;          // tokens per batch (MMA N <= 96): bounded by TMEM columns
@@ -493,54 +502,38 @@ struct TcMoeParams {
   const int32_t* n_batches;
   int R;                     // rows per matrix (I for gate/up, L for down)
   int K;                     // reduction length (L or I)
-  const int32_t* slot_pow;   // GATEUP: per-slot exponent p of its activation row (act = value * 2^p)
-  void* out;                 // GATEUP: h16 [slots, R]; DOWN: o f32 [slots, R]
+  void* out;                 // GATEUP: h [slots, R] bf16 (interleaved K order); DOWN: o f32 [slots, R]
   uint32_t* status;
   void* tmaps;               // packed-weight tensor maps, [TM_MAX_CTAS][TM_BLOCKS][2] x 128 bytes
 };
 
-// E8M0 scale byte -> f16x2 of 2^(s-127) in both halves (0 when not representable);
-// *bad is set when the byte is outside the exact range 105..142
-K3_DEVI uint32_t ue8m0_to_f16x2(uint32_t s, bool& bad) {
-  uint32_t h;
-  if (s >= 113u && s <= 142u) h = (s - 112u) << 10;  // normal f16
-  else if (s >= 103u && s < 113u) h = 1u << (s - 103u);  // subnormal f16
-  else h = 0u;
-  bad |= (s < 105u || s > 142u);
-  return h | (h << 16);
+// Eight E2M1 codes (one 32-bit word of packed bytes, low nibble first: codes c0..c7 of
+// eight consecutive elements) -> four bf16x2 words holding v * 2^-126 for the code
+// pairs [c0 c4] [c1 c5] [c2 c6] [c3 c7] (low half first).  A code s e1 e0 m shifted
+// into bits 15 (sign) and 8..6 (exponent bits 1..0, mantissa bit 6) is the bf16 number
+// v * 2^-126: for e > 0 the exponent field e gives 2^(e-127) (1 + m/2) = 2^(e-1) (1 + m/2)
+// * 2^-126, and for e = 0 the subnormal m * 2^-127 = (m/2) * 2^-126.  The multiply by
+// 0x1040 (or 0x104 for a high nibble) copies the masked nibble of both halves to bit
+// offsets +6 and +12 at once (no carries between the copies); the mask keeps the sign
+// from the second copy and the magnitude from the first.
+K3_DEVI void e2m1x8_to_bf16x8_il(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t w8 = w >> 8;
+  o[0] = ((w & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
+  o[1] = ((w & 0x00F000F0u) * 0x104u) & 0x81C081C0u;
+  o[2] = ((w8 & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
+  o[3] = ((w8 & 0x00F000F0u) * 0x104u) & 0x81C081C0u;
 }
 
-// 2^e as f32 for e in [-126, 127]
-K3_DEVI float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
-
-// e^x - 1 to a few ulp without cancellation near 0: the Taylor series through x^9 for
-// |x| < 1/2 (truncation below 1e-9 relative), expf(x) - 1 elsewhere.
-K3_DEVI float expm1_k3(float x) {
-  float t = 1.0f / 362880.0f;
-  t = fmaf(t, x, 1.0f / 40320.0f);
-  t = fmaf(t, x, 1.0f / 5040.0f);
-  t = fmaf(t, x, 1.0f / 720.0f);
-  t = fmaf(t, x, 1.0f / 120.0f);
-  t = fmaf(t, x, 1.0f / 24.0f);
-  t = fmaf(t, x, 1.0f / 6.0f);
-  t = fmaf(t, x, 0.5f);
-  t = fmaf(t, x, 1.0f);
-  const float small = t * x;
-  return (fabsf(x) < 0.5f) ? small : expf(x) - 1.0f;
+// d = a * b on two bf16 lanes, round to nearest (exact for power-of-two b unless the
+// product leaves the bf16 range)
+K3_DEVI uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
-// SiTU-GLU with one exponential per input:  with A = e^(g/2) - 1 and B = e^(2u/25) - 1,
-//   tanh(g/4) = A / (A + 2),  sigmoid(g) = (A+1)^2 / ((A+1)^2 + 1),  tanh(u/25) = B / (B + 2),
-// so h = 100 * A/(A+2) * (A+1)^2/((A+1)^2+1) * B/(B+2).  g is clamped to 80 and u/25 to
-// [-40, 40], where every factor is already 1 (or -1) in f32; NaN passes through.
-K3_DEVI float situ_fast(float g, float u) {
-  g = (g > 80.0f) ? 80.0f : g;
-  float v = u * 0.08f;  // 2u/25
-  v = (v > 80.0f) ? 80.0f : ((v < -80.0f) ? -80.0f : v);
-  const float A = expm1_k3(0.5f * g), B = expm1_k3(v);
-  const float E = (A + 1.0f) * (A + 1.0f);
-  return 100.0f * __fdividef(A, A + 2.0f) * __fdividef(E, E + 1.0f) * __fdividef(B, B + 2.0f);
-}
+// position of element j (0..7) of an 8-element group in the interleaved K order
+K3_DEVI int il_pos(int j) { return (j < 4) ? 2 * j : 2 * (j - 4) + 1; }
 
 // TMEM store: each lane of the warp writes 32 (or 16) consecutive 32-bit columns of its
 // own lane of the warp's lane quarter
@@ -705,7 +698,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x, ++lt) {
         const int n = p.batches[tile / mtiles].n;
         const int N = (n + 15) & ~15;
-        const uint32_t idesc = (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(TM_ROWS >> 4) << 24);  // f16 x f16 -> f32
+        const uint32_t idesc = idesc_bf16(TM_ROWS, N);  // bf16 x bf16 -> f32
         if (!mbar_wait_spin(tempty(0), (lt & 1) ^ 1, abort_flag)) break;  // accumulators emptied
         tc_fence_after();
         const uint32_t d = tmem + mm * TM_NB;
@@ -773,8 +766,8 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
             const int col = c * 16 + j;
             if (col < n) {
               float* o = reinterpret_cast<float*>(p.out) + (size_t)(slot0 + col) * p.R + row0;
-              o[0] = __uint_as_float(r0[j]) * (1.0f / 256.0f);
-              o[TM_ROWS] = __uint_as_float(r1[j]) * (1.0f / 256.0f);
+              o[0] = __uint_as_float(r0[j]);
+              o[TM_ROWS] = __uint_as_float(r1[j]);
             }
           }
         }
@@ -782,22 +775,19 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       tc_fence_before();
       mbar_arrive(tempty(0));
       if (MODE == 0) {
+        // h element `row` of each token, stored at its place in the interleaved K order
         const int row = tm * TM_ROWS + q * 32 + lane;
+        const int hcol = (row & ~7) + il_pos(row & 7);
 #pragma unroll 1
         for (int c = e0, k = 0; c * 16 < n; c += 2, ++k) {
-          // lane j < 16 fetches column j's activation exponent p; the accumulators carry
-          // 2^p, removed exactly by two power-of-two factors (p lies in [-113, 141])
-          const int pw = (lane < 16 && c * 16 + lane < n) ? __ldg(p.slot_pow + slot0 + c * 16 + lane) : 0;
-          const float f1 = pow2f(-(pw >> 1)), f2 = pow2f((pw >> 1) - pw);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float a1 = __shfl_sync(0xffffffffu, f1, j), a2 = __shfl_sync(0xffffffffu, f2, j);
             const int col = c * 16 + j;
             if (col < n) {
-              const float gg = stg[(k * 32 + j) * (TM_EPI * 32)] * a1 * a2;
-              const float uu = stg[(k * 32 + 16 + j) * (TM_EPI * 32)] * a1 * a2;
-              const float h = __uint_as_float((uint32_t)f32_to_bf16_bits(situ_fast(gg, uu)) << 16);  // bf16 rounding
-              reinterpret_cast<__half*>(p.out)[(size_t)(slot0 + col) * p.R + row] = __float2half_rn(h * 256.0f);
+              const float gg = stg[(k * 32 + j) * (TM_EPI * 32)];
+              const float uu = stg[(k * 32 + 16 + j) * (TM_EPI * 32)];
+              reinterpret_cast<uint16_t*>(p.out)[(size_t)(slot0 + col) * p.R + hcol] =
+                  f32_to_bf16_bits(situ_fast(gg, uu));  // bf16 rounding of h
             }
           }
         }
@@ -906,7 +896,6 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
     const int my_tiles = (tiles > (int)blockIdx.x) ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int nchunks = my_tiles * kchunks;
     bool stop = false;
-    bool bad = false;
 #pragma unroll 1
     for (int jc = 0; jc < nchunks && !stop; ++jc) {
       // chunk jc's packed and scale bytes (the copy warp's) have landed
@@ -919,29 +908,40 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       uint2 sc8;
       if constexpr (CKB == 4) sc8 = *reinterpret_cast<const uint2*>(scs);
       else sc8 = make_uint2(*reinterpret_cast<const uint32_t*>(scs), 0u);
-      // decode k-block kq of the chunk (64 elements of row ri) into a[]: f16x2 columns
+      // decode k-block kq of the chunk (64 elements of row ri) into a[]: bf16x2 columns in
+      // the interleaved K order
       uint32_t a[32], a2[32];
       auto decode = [&](int kq, uint32_t (&out)[32]) {
         const uint32_t cs = ((kq < 2) ? sc8.x : sc8.y) >> (16 * (kq & 1));  // this k-block's two scale bytes
+        // per 32-element group: the decoded words are v * 2^-126, so the factor is 2^(s-1),
+        // a bf16 power of two (exponent field s + 126) for s <= 128; a larger byte takes
+        // 2^127 and then 2^(s-128) (exponent field s - 1), each product exact
+        uint32_t f1[2], f2[2];
+        bool big = false;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const uint32_t sb = (cs >> (8 * g)) & 0xFFu;
+          const bool bg = sb > 128u;
+          f1[g] = ((bg ? 254u : sb + 126u) << 7) * 0x10001u;
+          f2[g] = ((bg ? sb - 1u : 127u) << 7) * 0x10001u;
+          big |= bg;
+        }
+        big = __any_sync(0xffffffffu, big);  // warp-uniform: the second multiply is rare
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           const uint4 cq = *reinterpret_cast<const uint4*>(src + (((2 * kq + g) ^ swz(ri)) << 4));
-          // scale byte s in 113..142: 2^(s-127) is a normal f16, exponent field s - 112, in
-          // both halves -- two integer multiply-adds; other bytes take the general decode
-          const uint32_t sb = (cs >> (8 * g)) & 0xFFu;
-          uint32_t sc2 = (sb * 1024u - 114688u) * 0x10001u;
-          if (sb - 113u > 29u) sc2 = ue8m0_to_f16x2(sb, bad);
           const uint32_t w4[4] = {cq.x, cq.y, cq.z, cq.w};
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {  // 8 elements = 4 packed bytes -> 4 f16x2 columns
+          for (int cc = 0; cc < 4; ++cc) {  // 8 elements = 4 packed bytes -> 4 bf16x2 columns
             uint32_t h[4];
-            e2m1x8_to_f16x8(w4[cc], h);
+            e2m1x8_to_bf16x8_il(w4[cc], h);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h[e]), *reinterpret_cast<const __half2*>(&sc2));
-              out[g * 16 + cc * 4 + e] = *reinterpret_cast<uint32_t*>(&v);
-            }
+            for (int e = 0; e < 4; ++e) out[g * 16 + cc * 4 + e] = bf16x2_mul(h[e], f1[g]);
           }
+        }
+        if (big) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) out[i] = bf16x2_mul(out[i], f2[i >> 4]);
         }
       };
       // a tcgen05.st keeps its source registers until tcgen05.wait::st: the stage's second
@@ -972,7 +972,6 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       // the TMEM store and the arrival above): the slot may be refilled
       if (!stop && lane == 0) mbar_arrive(raw_empty(jc % RC));
     }
-    if (bad) flag_status(p.status, K3MOE_DEV_SCALE_RANGE);
   }
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) flag_status(p.status, K3MOE_DEV_TIMEOUT);

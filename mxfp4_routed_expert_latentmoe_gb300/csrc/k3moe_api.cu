@@ -3,6 +3,7 @@
 // no synchronisation (except k3moe_device_status, which is documented to sync).
 #include <atomic>
 #include <cstring>
+#include <mutex>
 #include <utility>
 
 #include "k3_common.cuh"
@@ -22,7 +23,7 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 struct WsLayout {
   size_t status, logits, ids, w, zmax, zpow, counts, offsets, slot_of, slot_tok, inv, uniq, n_uniq, nb_prefix,
-      n_batches, cta_cnt, cta_base, batches, z, z16, h16, o, y, yhat, cpart, ccount, z16p, spow, tmaps, total;
+      n_batches, cta_cnt, cta_base, batches, z, z16, h16, o, y, yhat, cpart, ccount, act, tmaps, total;
 };
 
 WsLayout ws_layout(const k3moe_dims& d, int T) {
@@ -65,10 +66,9 @@ WsLayout ws_layout(const k3moe_dims& d, int T) {
   L.yhat = take(Tz * Lt * 2);
   L.cpart = take(Tz * COMB_MAX_SPLIT * 4);
   L.ccount = take(Tz * 4);
-  // slot-order activation rows for the tensor-core expert path (large T only)
+  // slot-order bf16 activation rows for the tensor-core expert path (large T only)
   const bool tc = T >= 256;
-  L.z16p = take(tc ? slots * Lt * 2 : 0);
-  L.spow = take(tc ? slots * 4 : 0);
+  L.act = take(tc ? slots * Lt * 2 : 0);
   L.tmaps = take(tc ? (size_t)TM_MAX_CTAS * TM_BLOCKS * 2 * 128 : 0);  // packed-weight tensor maps
   L.total = off;
   return L;
@@ -231,24 +231,11 @@ constexpr int kTcMinT = 256;
 // weight-streaming kernels at every T
 bool tc_experts(const k3moe_dims& d, int T) { return T >= kTcMinT && d.latent % 256 == 0 && d.inter % 256 == 0; }
 
-// row-major [rows, cols] f16 matrix, boxes of box_rows x 64 with the 128-byte swizzle
-bool map_f16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {64, box_rows};
-  const cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // grouped MXFP4 expert GEMM on tcgen05; act [slots, K] f16 in slot order
 template <int MODE>
-cudaError_t launch_tc_moe(const __half* act, int slots, TcMoeParams p, int dev, int sms, cudaStream_t st, bool pdl) {
+cudaError_t launch_tc_moe(const uint16_t* act, int slots, TcMoeParams p, int dev, int sms, cudaStream_t st, bool pdl) {
   CUtensorMap mb, ma;
-  if (!map_f16(&mb, act, slots, p.K, TM_NB)) return cudaErrorInvalidValue;
+  if (!map_bf16(&mb, act, slots, p.K, TM_NB)) return cudaErrorInvalidValue;
   // template of the packed-weight maps ([R, K/2] bytes, 128-row boxes): the kernel writes
   // each expert tensor's address into its copies; the workspace stands in until then
   if (!map_u8(&ma, p.tmaps, (uint64_t)p.R, (uint64_t)p.K / 2, TM_ROWS)) return cudaErrorInvalidValue;
@@ -546,7 +533,7 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
     K3_TRY(launch_dense<DN_PROJ>(dp, dev, sms, s, false));
   }
   K3_TRY(mark(events, n_events, 1, s));
-  // top-k with fp64 near-tie refinement, chunk expert union, z -> f16 operand
+  // top-k with double-f32 near-tie refinement, chunk expert union, activation operand prep
   TopkParams tp{};
   tp.logits = at<float>(ws, L.logits); tp.bias = bias; tp.x = x; tp.wr = wr;
   tp.T = T; tp.E = d.n_experts; tp.K = d.top_k; tp.H = d.hidden; tp.tau = kTieTau;
@@ -556,27 +543,31 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   const int nblk = mx_nblk(T);
   const int NB = tc ? TM_NB : 8 * nblk;  // tokens per expert batch
   const PermParams pp = perm_params(d, T, d.top_k, at<int32_t>(ws, L.ids), 0, NB, ws, L, experts);
-  const Z16Params zp{at<uint16_t>(ws, L.z), T, d.latent, at<__half>(ws, L.z16), at<int32_t>(ws, L.zpow)};
-  K3_TRY(launch_route_tail(tp, pp, zp, dev, s, pdl));
   const int slots = T * d.top_k;
-  if (tc) {  // activation rows in expert-sorted slot order for the grouped GEMM (part of routing)
+  if (tc) {
+    // top-k, permutation, then the bf16 activation rows in expert-sorted slot order for
+    // the grouped GEMM (the f16 copy of z that the weight-streaming kernels read is not needed)
+    K3_TRY(launch_topk(tp, dev, s, pdl));
+    K3_TRY(launch_permute(pp, dev, s, pdl));
     const int per = d.latent / 8;
     const int gblocks = (int)(((size_t)slots * per + 255) / 256 < (size_t)sms * 8 ? ((size_t)slots * per + 255) / 256
                                                                                      : (size_t)sms * 8);
-    K3_TRY(launch(k3_gather_rows_kernel, dim3(gblocks), dim3(256), 0, s, pdl, (const __half*)at<__half>(ws, L.z16),
-                  (const int32_t*)at<int32_t>(ws, L.zpow), (const int32_t*)at<int32_t>(ws, L.slot_tok), slots,
-                  (int)d.latent, at<__half>(ws, L.z16p), at<int32_t>(ws, L.spow)));
+    K3_TRY(launch(k3_gather_rows_kernel, dim3(gblocks), dim3(256), 0, s, pdl, (const uint16_t*)at<uint16_t>(ws, L.z),
+                  (const int32_t*)at<int32_t>(ws, L.slot_tok), slots, (int)d.latent, at<uint16_t>(ws, L.act)));
+  } else {
+    const Z16Params zp{at<uint16_t>(ws, L.z), T, d.latent, at<__half>(ws, L.z16), at<int32_t>(ws, L.zpow)};
+    K3_TRY(launch_route_tail(tp, pp, zp, dev, s, pdl));
   }
   K3_TRY(mark(events, n_events, 2, s));
   // experts
   if (tc) {
     TcMoeParams gp{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.inter, d.latent,
-                   at<int32_t>(ws, L.spow), at<void>(ws, L.h16), status, at<void>(ws, L.tmaps)};
-    K3_TRY(launch_tc_moe<0>(at<__half>(ws, L.z16p), slots, gp, dev, sms, s, pdl));
+                   at<void>(ws, L.h16), status, at<void>(ws, L.tmaps)};
+    K3_TRY(launch_tc_moe<0>(at<uint16_t>(ws, L.act), slots, gp, dev, sms, s, pdl));
     K3_TRY(mark(events, n_events, 3, s));
-    TcMoeParams dp2{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.latent, d.inter, nullptr,
+    TcMoeParams dp2{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.latent, d.inter,
                     at<void>(ws, L.o), status, at<void>(ws, L.tmaps)};
-    K3_TRY(launch_tc_moe<1>(at<__half>(ws, L.h16), slots, dp2, dev, sms, s, pdl));
+    K3_TRY(launch_tc_moe<1>(at<uint16_t>(ws, L.h16), slots, dp2, dev, sms, s, pdl));
   } else {
     K3_TRY(launch_mx<MX_GATEUP>(mx_params(d, L, ws, MX_GATEUP, at<__half>(ws, L.z16), at<void>(ws, L.h16)), nblk,
                                 dev, sms, s, pdl));
@@ -684,14 +675,6 @@ k3moe_status k3moe_permute(const k3moe_dims* dims, int32_t T, const int32_t* ids
   return K3MOE_OK;
 }
 
-k3moe_status k3moe_device_status(const void* ws, uint32_t* host_out, void* stream) {
-  if (!ws || !host_out) return K3MOE_ERR_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  K3_TRY(cudaMemcpyAsync(host_out, ws, 4, cudaMemcpyDeviceToHost, s));
-  K3_TRY(cudaStreamSynchronize(s));
-  return K3MOE_OK;
-}
-
 void* k3moe_workspace_view(const k3moe_dims* dims, int32_t T, void* ws, int32_t which) {
   if (check_dims(dims) != K3MOE_OK || T < 0 || !ws) return nullptr;
   const WsLayout L = ws_layout(*dims, T);
@@ -700,6 +683,8 @@ void* k3moe_workspace_view(const k3moe_dims* dims, int32_t T, void* ws, int32_t 
     case 1: return at<void>(ws, L.yhat);
     case 2: return at<void>(ws, L.y);
     case 3: return at<void>(ws, L.logits);
+    case 4: return at<void>(ws, L.h16);
+    case 5: return at<void>(ws, L.o);
     default: return nullptr;
   }
 }
@@ -709,14 +694,74 @@ void* k3moe_workspace_view(const k3moe_dims* dims, int32_t T, void* ws, int32_t 
 // ---------------------------------------------------------------------------- allocation-free entry
 // Scratch for k3moe_forward_noalloc: a fixed array in device memory that every GPU
 // loading this library holds until the process exits.
-#define K3MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
 static __device__ __align__(256) uint8_t g_k3_noalloc_scratch[K3MOE_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-// device address of the scratch array, looked up once per device (host code cannot
-// use the array's name as a device pointer)
-void* g_noalloc_ptr[kMaxDevices];
+// Device address of the scratch array per device, with the id of the context it was
+// looked up in (host code cannot use the array's name as a device pointer, and a reset
+// device gets a new context whose copy of the array may live elsewhere).
+struct NoallocSlot {
+  void* ptr = nullptr;
+  unsigned long long ctx_id = 0;
+};
+NoallocSlot g_noalloc[kMaxDevices];
 std::atomic<bool> g_noalloc_ready[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// id of the calling thread's current context (0 when none is current or the driver
+// entry points are unavailable)
+unsigned long long current_ctx_id() {
+  static std::atomic<CtxGetCurrentFn> get_cur{nullptr};
+  static std::atomic<CtxGetIdFn> get_id{nullptr};
+  CtxGetCurrentFn fc = get_cur.load(std::memory_order_acquire);
+  CtxGetIdFn fi = get_id.load(std::memory_order_acquire);
+  if (!fc || !fi) {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult q1{}, q2{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess)
+      return 0;
+    fc = reinterpret_cast<CtxGetCurrentFn>(a);
+    fi = reinterpret_cast<CtxGetIdFn>(b);
+    get_cur.store(fc, std::memory_order_release);
+    get_id.store(fi, std::memory_order_release);
+  }
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (fc(&c) != CUDA_SUCCESS || !c || fi(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// The scratch array's device address on the current device.  Looked up with
+// cudaGetSymbolAddress on the first call per device, and again only if the current
+// context is no longer the one of that lookup (a device reset in between).
+k3moe_status noalloc_scratch(void** out) {
+  int dev = 0, sms = 0;
+  k3moe_status st = check_device(&dev, &sms);
+  if (st != K3MOE_OK) return st;
+  const unsigned long long cur = current_ctx_id();
+  if (g_noalloc_ready[dev].load(std::memory_order_acquire) && (cur == 0 || cur == g_noalloc[dev].ctx_id)) {
+    *out = g_noalloc[dev].ptr;
+    return K3MOE_OK;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_k3_noalloc_scratch) != cudaSuccess || !p) {
+    (void)cudaGetLastError();  // leave no pending error behind for the caller's next check
+    return K3MOE_ERR_CUDA;
+  }
+  g_noalloc[dev].ptr = p;
+  g_noalloc[dev].ctx_id = current_ctx_id();  // the lookup made the device's context current
+  g_noalloc_ready[dev].store(true, std::memory_order_release);
+  *out = p;
+  return K3MOE_OK;
+}
 }  // namespace
 
 extern "C" {
@@ -730,16 +775,24 @@ k3moe_status k3moe_forward_noalloc(const k3moe_dims* dims, int32_t T, const uint
   if (T < 0) return K3MOE_ERR_ARG;
   if (T == 0) return K3MOE_OK;
   if (ws_layout(*dims, T).total > K3MOE_NOALLOC_SCRATCH_BYTES) return K3MOE_ERR_WORKSPACE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return K3MOE_ERR_DEVICE;
-  if (!g_noalloc_ready[dev].load(std::memory_order_acquire)) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_k3_noalloc_scratch) != cudaSuccess || !p) return K3MOE_ERR_CUDA;
-    g_noalloc_ptr[dev] = p;
-    g_noalloc_ready[dev].store(true, std::memory_order_release);
-  }
-  return k3moe_forward(dims, T, x, wr, bias, w_down, w_up, norm_w, experts, out, ids_out, w_out, g_noalloc_ptr[dev],
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != K3MOE_OK) return st;
+  return k3moe_forward(dims, T, x, wr, bias, w_down, w_up, norm_w, experts, out, ids_out, w_out, scratch,
                        K3MOE_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+k3moe_status k3moe_device_status(const void* ws, uint32_t* host_out, void* stream) {
+  if (!host_out) return K3MOE_ERR_ARG;
+  if (!ws) {  // the allocation-free entry point's scratch on the current device
+    void* scratch = nullptr;
+    const k3moe_status st = noalloc_scratch(&scratch);
+    if (st != K3MOE_OK) return st;
+    ws = scratch;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  K3_TRY(cudaMemcpyAsync(host_out, ws, 4, cudaMemcpyDeviceToHost, s));
+  K3_TRY(cudaStreamSynchronize(s));
+  return K3MOE_OK;
 }
 
 const char* k3moe_status_str(k3moe_status st) {

@@ -41,15 +41,15 @@ def test_workspace_bytes_is_monotone_and_rejects_bad_dims():
 
 
 def test_workspace_holds_the_tensor_core_path_buffers_from_256_tokens():
-    # from 256 tokens the grouped expert GEMM needs the slot-ordered f16 activations, their
-    # per-slot exponents and the weight tensor maps (256 CTAs x 2 blocks x 2 x 128 bytes);
-    # below that the workspace grows by the per-token buffers only
+    # from 256 tokens the grouped expert GEMM needs the slot-ordered bf16 activations and
+    # the weight tensor maps (256 CTAs x 2 blocks x 2 x 128 bytes); below that the
+    # workspace grows by the per-token buffers only
     L = k3.lib()
     d = _d()
     ws = {T: L.k3moe_workspace_bytes(ctypes.byref(d), T) for T in (254, 255, 256)}
     per_token = ws[255] - ws[254]
     slots = 256 * 16
-    tc_bytes = slots * 3584 * 2 + slots * 4 + 256 * 2 * 2 * 128
+    tc_bytes = slots * 3584 * 2 + 256 * 2 * 2 * 128
     assert ws[256] - ws[255] >= tc_bytes
     assert ws[256] - ws[255] <= tc_bytes + 2 * per_token + 3 * 256
 
@@ -115,3 +115,29 @@ def test_dequant_validates_shape():
     assert L.k3moe_dequant_mxfp4(v, v, -1, 64, v, None) == ERR_ARG
     assert L.k3moe_dequant_mxfp4(v, v, 0, 64, v, None) == 0
     assert L.k3moe_dequant_mxfp4(ctypes.c_void_p(8), v, 4, 64, v, None) == ERR_ALIGN
+
+
+def test_noalloc_scratch_limit_is_the_workspace_size_rule():
+    """k3moe_forward_noalloc refuses, before touching a device, any call whose workspace
+    (k3moe_workspace_bytes) exceeds its fixed scratch array: at K3 shapes 11 tokens fit
+    and 12 do not."""
+    import re
+    L = k3.lib()
+    d = _d()
+    text = open(k3._HEADER).read()
+    m = re.search(r"#define K3MOE_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m and (int(m.group(1)) << int(m.group(2))) == k3.NOALLOC_SCRATCH_BYTES
+    cap = k3.NOALLOC_SCRATCH_BYTES
+    assert L.k3moe_workspace_bytes(ctypes.byref(d), 11) <= cap < L.k3moe_workspace_bytes(ctypes.byref(d), 12)
+    v = ctypes.c_void_p(16)
+    ex = k3.ExpertsC(16, 16, 16, 16, 16, 16)
+    assert L.k3moe_forward_noalloc(ctypes.byref(d), 12, v, v, v, v, v, v, ctypes.byref(ex), v, None, None,
+                                   None) == ERR_WS
+    assert L.k3moe_forward_noalloc(ctypes.byref(d), 0, v, v, v, v, v, v, ctypes.byref(ex), v, None, None,
+                                   None) == 0
+    import torch
+    if not torch.cuda.is_available():  # a call that fits reaches the device check
+        assert L.k3moe_forward_noalloc(ctypes.byref(d), 11, v, v, v, v, v, v, ctypes.byref(ex), v, None, None,
+                                       None) == ERR_DEVICE
+        st = ctypes.c_uint32(0)
+        assert L.k3moe_device_status(None, ctypes.byref(st), None) == ERR_DEVICE

@@ -2,7 +2,16 @@
 
 Bars: routed ids and the counting-sort permutation bit-exact; MXFP4 -> f32
 dequantisation bit-exact (IEEE bits); block output rel-L2 <= 2e-3 against the
-oracle's bf16-rounding spec mode (bf16 operands, fp32 accumulation on the GPU).
+oracle's bf16-rounding spec mode (bf16 operands, fp32 accumulation on the GPU), taken
+over a workload's outputs (all its tokens, or all sampled tokens together).
+
+Per token the error is larger in the tail: the spec rounds z, h and yhat to bf16, and
+where the GPU's fp32 sum and the oracle's fp64 sum straddle a rounding boundary the two
+round apart by one bf16 unit (2^-8 relative).  A flip in z moves every g, u of the token
+a little (about 2^-8 / sqrt(L) relative), which flips about 1% of its h; the h flips move
+y by a few 1e-4 relative, which flips some 10% of yhat.  The output error of a token is
+then about 1e-3, and a few tokens in a thousand reach 3e-3.  Each token is therefore held
+to PER_TOKEN_BAR = 5e-3 on its own.
 """
 import math
 
@@ -13,6 +22,8 @@ import datagen
 import oracle
 from datagen import configs as C
 from tests._harness import REL_L2_BAR, oracle_dims, oracle_forward, oracle_route, rel_l2
+
+PER_TOKEN_BAR = 5e-3
 
 pytestmark = pytest.mark.gpu
 
@@ -217,17 +228,30 @@ def _check_block(got, ids, w, ref, ws=None, k3=None):
     return r
 
 
+def _ws_view(k3, L, ws, which, T, n, dtype):
+    """Intermediate `which` of the last forward that used ws (k3moe_workspace_view)."""
+    ptr = k3.workspace_view(L.d, T, ws, which)
+    assert ptr != 0
+    off = ptr - ws.data_ptr()
+    nb = n * torch.empty((), dtype=dtype).element_size()
+    return ws[off: off + nb].view(dtype).float().cpu().numpy().astype(np.float64)
+
+
 def test_forward_tiny(k3, tiny):
     got, ids, w, ws = tiny.forward(k3)
     ref = oracle_forward(C.TINY)
     r = _check_block(got, ids, w, ref)
     assert k3.device_status(ws) == 0
-    # intermediates: z and yhat are bf16 at the spec's rounding points
-    T, Lt = C.TINY.T, C.TINY.latent
-    z = torch.empty(T, Lt, dtype=torch.bfloat16, device="cuda")
-    zp = k3.workspace_view(tiny.d, T, ws, 0)
-    assert zp != 0
     assert r < 1e-4, r
+    # intermediates at the spec's bf16 rounding points: z (latent down), y (combine, f32),
+    # yhat (RMSNorm); fp32 accumulation may flip a bf16 rounding only next to a boundary
+    T, Lt = C.TINY.T, C.TINY.latent
+    z = _ws_view(k3, tiny, ws, 0, T, T * Lt, torch.bfloat16).reshape(T, Lt)
+    yhat = _ws_view(k3, tiny, ws, 1, T, T * Lt, torch.bfloat16).reshape(T, Lt)
+    y = _ws_view(k3, tiny, ws, 2, T, T * Lt, torch.float32).reshape(T, Lt)
+    assert np.mean(z != ref["z"]) <= 0.01 and rel_l2(z, ref["z"]) < 1e-3
+    assert rel_l2(y, ref["y"]) < 1e-4
+    assert np.mean(yhat != ref["yhat"]) <= 0.02 and rel_l2(yhat, ref["yhat"]) < 2e-3
 
 
 def test_forward_decode(k3, decode):
@@ -292,18 +316,148 @@ def test_misaligned_expert_tensor_sets_the_align_status(k3, prefill):
     assert k3.device_status(ws) & k3.DEV_ALIGN
 
 
-def test_forward_prefill_sampled(k3, prefill):
+def _slot_map(ids, E):
+    """Sorted-slot order of the flat (t, k) routed slots (expert ascending, then t, k):
+    expert, token of every slot and per-expert offsets."""
+    T, K = ids.shape
+    flat = ids.ravel()
+    order = np.argsort(flat, kind="stable")
+    offsets = np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=E))])
+    return flat[order], order // K, offsets
+
+
+def _deinterleave(h_il):
+    """Rows stored in the grouped GEMM's interleaved K order (per 8 elements: 0,4,1,5,2,6,3,7)
+    back to the natural order."""
+    pos = np.array([0, 2, 4, 6, 1, 3, 5, 7])
+    g = h_il.reshape(h_il.shape[0], -1, 8)
+    return g[:, :, pos].reshape(h_il.shape)
+
+
+def _check_grouped_gemm_slots(k3, L, ws, ids, experts, cfg):
+    """The grouped tcgen05 GEMMs' own outputs for every slot of the given experts, element by
+    element: h (gate/up + SiTU-GLU, bf16) against the fp64 product of the dequantised weights
+    with the GPU's own z, rounded as the spec rounds h; o (down) against the fp64 product of
+    the dequantised down matrix with the GPU's own h."""
+    T, Lt, I, K = cfg.T, cfg.latent, cfg.inter, cfg.top_k
+    slots = T * K
+    z = _ws_view(k3, L, ws, 0, T, T * Lt, torch.bfloat16).reshape(T, Lt)
+    h_all = _deinterleave(_ws_view(k3, L, ws, 4, T, slots * I, torch.bfloat16).reshape(slots, I))
+    o_all = _ws_view(k3, L, ws, 5, T, slots * Lt, torch.float32).reshape(slots, Lt)
+    s_exp, s_tok, offs = _slot_map(ids, cfg.n_experts)
+    worst_h = worst_o = 0.0
+    flips = total = beyond = 0
+    for e in experts:
+        tens = C.expert_tensors(cfg, int(e))
+        Wg = oracle.dequant(tens["gate_q"], tens["gate_s"])
+        Wu = oracle.dequant(tens["up_q"], tens["up_s"])
+        W2 = oracle.dequant(tens["down_q"], tens["down_s"])
+        sl = np.arange(offs[e], offs[e + 1])
+        assert len(sl) > 0 and np.all(s_exp[sl] == e)
+        zt = z[s_tok[sl]]
+        href = oracle.round_bf16(oracle.situ(zt @ Wg.T, zt @ Wu.T))
+        h = h_all[sl]
+        d = np.abs(h - href)
+        flips += int(np.count_nonzero(d))
+        total += h.size
+        # a differing element is one bf16 rounding apart (fp32 accumulation next to a rounding
+        # boundary), or, where g or u is a small result of cancellation, off by about the fp32
+        # accumulation error of the row (well under one bf16 unit of the row's RMS)
+        rms = np.sqrt(np.mean(href ** 2, axis=1, keepdims=True))
+        bound = np.abs(href) * 2.0 ** -7 + rms * 2.0 ** -8
+        beyond += int(np.count_nonzero(d > bound))
+        oref = h @ W2.T
+        for i in range(len(sl)):
+            worst_h = max(worst_h, rel_l2(h[i], href[i]))
+            worst_o = max(worst_o, rel_l2(o_all[sl[i]], oref[i]))
+    # a g or u that is a tiny remainder of cancelling terms can come out of fp32 accumulation
+    # with a few units of its own size wrong: allowed for about 1 element in 10^5
+    assert beyond <= 1 + total // 100000, (beyond, total)
+    assert flips <= 0.01 * total, (flips, total)
+    assert worst_h <= REL_L2_BAR, worst_h
+    assert worst_o <= 1e-4, worst_o
+    return worst_h, worst_o, flips / total
+
+
+def test_grouped_gemm_slots_prefill(k3, prefill):
+    """4096 tokens: every slot of four experts chosen to cover the batch shapes of the grouped
+    GEMM -- the most-used expert (more than 96 tokens: a full 96-token batch and a remainder
+    batch), the least-used one, and experts whose token counts are not multiples of 16 (MMA N
+    rounded up, the ragged columns masked)."""
+    cfg = C.PREFILL
+    got, ids, w, ws = prefill.forward(k3)
+    assert k3.device_status(ws) == 0
+    counts = np.bincount(ids.ravel(), minlength=cfg.n_experts)
+    e_max, e_min = int(np.argmax(counts)), int(np.argmin(counts))
+    assert counts[e_max] > 96  # split over two batches
+    ragged = [int(e) for e in np.argsort(counts) if counts[e] % 16 not in (0,) and int(e) not in (e_max, e_min)]
+    experts = [e_max, e_min, ragged[len(ragged) // 2], ragged[-1]]
+    wh, wo, fr = _check_grouped_gemm_slots(k3, prefill, ws, ids, experts, cfg)
+    print(f"grouped GEMM slots: counts {[int(counts[e]) for e in experts]}, worst h {wh:.2e}, worst o {wo:.2e}, "
+          f"h flips {fr:.1e}")
+
+
+def test_forward_prefill_per_token(k3, prefill):
+    """64 sampled tokens of the 4096-token prefill (first, last, tile edges, random): ids
+    bit-exact for all 4096 tokens; the sampled outputs within the 2e-3 rel-L2 bar taken over
+    the workload's outputs (all sampled rows together), and every sampled token within
+    PER_TOKEN_BAR on its own (the bf16 rounding cascade of one token can exceed the
+    tensor-wide figure; see the module docstring)."""
     cfg = C.PREFILL
     L = prefill
     got, ids, w, ws = L.forward(k3)
     assert k3.device_status(ws) == 0
     rids, rw, _, _ = oracle_route(cfg)
     assert np.array_equal(ids, rids)
-    rows = [0, 1, 2047, 4095] + list(np.random.default_rng(5).choice(4096, 4, replace=False))
+    rows = sorted({0, 1, 127, 128, 2047, 4095} | set(int(r) for r in np.random.default_rng(5).choice(4096, 58,
+                                                                                                    replace=False)))
     ref = oracle_forward(cfg, token_rows=rows)
     assert np.array_equal(ids[rows], ref["ids"])
-    r = rel_l2(got[rows], ref["out"])
-    assert r <= REL_L2_BAR, r
-    print(f"prefill sampled rel-L2 {r:.3e}")
+    pooled = rel_l2(got[rows], ref["out"])
+    per = [rel_l2(got[r], ref["out"][i]) for i, r in enumerate(rows)]
+    print(f"prefill rel-L2 over {len(rows)} sampled tokens {pooled:.3e}; per token: median {np.median(per):.3e}, "
+          f"max {max(per):.3e} (token {rows[int(np.argmax(per))]})")
+    assert pooled <= REL_L2_BAR, pooled
+    assert max(per) <= PER_TOKEN_BAR, (max(per), rows[int(np.argmax(per))])
     counts = np.bincount(ids.ravel(), minlength=cfg.n_experts)
     assert counts.min() > 0  # every expert is used at zero bias
+
+
+@pytest.mark.parametrize("lo,hi", [(100, 100), (150, 150), (120, 135)])
+def test_grouped_gemm_scale_bytes_beyond_the_workloads(k3, lo, hi):
+    """Scale bytes 100 (weights down to 2^-28), 150 (up to 6 * 2^23, the path that takes a
+    second power-of-two multiply) and 120..135 (both paths inside one warp): the grouped
+    GEMM's bf16 weight decode is exact for every byte.  256 tokens over 64 experts at K3
+    widths; the GEMMs' outputs for every slot of three experts against the oracle's
+    dequantisation, SiTU and rounding applied to the GPU's own z and h.
+    The whole layer is compared with the oracle where it is well conditioned (bytes 100).
+    With large scales g and u reach 1e4..1e9, every h saturates at +-100 and its sign
+    follows u: one bf16 rounding difference in z (fp32 against fp64 accumulation) moves u
+    by 2^-8 |z_i| |W_i| (up to ~1e5 at byte 150), which flips the sign of the few h whose u
+    lies closer to 0 than that -- a property of the inputs, not of the kernels, which the
+    slot checks above cover with shared z."""
+    import dataclasses
+    cfg = dataclasses.replace(C.PREFILL, name=f"scales-{lo}-{hi}", T=256, n_experts=64, scale_lo=lo, scale_hi=hi,
+                              x_seed=23)
+    L = Layer(k3, cfg)
+    got, ids, w, ws = L.forward(k3)
+    assert k3.device_status(ws) == 0
+    rids, rw, _, _ = oracle_route(cfg)
+    assert np.array_equal(ids, rids)
+    counts = np.bincount(ids.ravel(), minlength=cfg.n_experts)
+    experts = [int(np.argmax(counts)), int(np.argmin(counts)), int(np.argsort(counts)[len(counts) // 2])]
+    wh, wo, fr = _check_grouped_gemm_slots(k3, L, ws, ids, experts, cfg)
+    print(f"scale bytes {lo}..{hi}: worst slot h {wh:.2e}, o {wo:.2e}, h flips {fr:.1e}")
+    if hi > 127:
+        del L
+        torch.cuda.empty_cache()
+        return
+    rows = [0, 1, 127, 128, 254, 255] + [int(r) for r in np.random.default_rng(7).choice(256, 2, replace=False)]
+    ref = oracle_forward(cfg, token_rows=rows)
+    pooled = rel_l2(got[rows], ref["out"])
+    per = [rel_l2(got[r], ref["out"][i]) for i, r in enumerate(rows)]
+    print(f"scale bytes {lo}..{hi}: outputs {pooled:.2e}, worst token {max(per):.2e}")
+    assert pooled <= REL_L2_BAR
+    assert max(per) <= PER_TOKEN_BAR
+    del L
+    torch.cuda.empty_cache()

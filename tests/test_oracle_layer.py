@@ -145,6 +145,28 @@ def test_topk_ties_go_to_lower_id_and_bias_only_selects():
     assert np.allclose(w[0], s[ids[0]] / s[ids[0]].sum(), rtol=1e-15)
 
 
+def test_router_sigmoid_closed_form_values():
+    """The sigmoid at points where it has exact closed-form values: sigma(0) = 1/2,
+    sigma(ln 3) = 3/4, sigma(-ln 3) = 1/4, read through the top-K gap (a difference of
+    biased scores) and the renormalised weights."""
+    d = oracle.dims(8, 32, 3, 2, 64)
+    ln3 = math.log(3.0)
+    lg = np.array([[0.0, ln3, -ln3]])
+    ids, w, gap, mingap = oracle.topk(d, lg, np.zeros(3, np.float32))
+    assert list(ids[0]) == [1, 0]
+    assert gap[0] == pytest.approx(0.5 - 0.25, abs=1e-15)      # sigma(0) - sigma(-ln 3)
+    assert mingap[0] == pytest.approx(0.75 - 0.5, abs=1e-15)   # sigma(ln 3) - sigma(0)
+    assert w[0, 0] == pytest.approx(0.75 / 1.25, abs=1e-15) and w[0, 1] == pytest.approx(0.5 / 1.25, abs=1e-15)
+    # a bias shifts the ranking score only: +0.3 on expert 2 puts it first, weights from raw scores
+    ids, w, gap, _ = oracle.topk(d, lg, np.array([0.0, 0.0, 0.6], np.float32))
+    assert list(ids[0]) == [2, 1]
+    assert w[0, 0] == pytest.approx(0.25 / 1.0, abs=1e-15)
+    assert gap[0] == pytest.approx(0.75 - 0.5, abs=1e-15)
+    # saturation: large logits give scores 1 and 0 (equal weights among saturated experts)
+    ids, w, _, _ = oracle.topk(d, np.array([[800.0, 800.0, -800.0]]), np.zeros(3, np.float32))
+    assert list(ids[0]) == [0, 1] and np.array_equal(w[0], [0.5, 0.5])
+
+
 # ------------------------------------------------------------------------------ permutation
 def test_permute_matches_stable_sort():
     rng = np.random.default_rng(6)
