@@ -90,15 +90,17 @@ K3_DEVI bool mbar_test(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// As mbar_wait, but spinning on test_wait: the lowest wake-up latency, for the single
-// thread that issues MMAs (a suspended thread took hundreds of cycles to resume).
-K3_DEVI bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// As mbar_wait, for the single thread that issues MMAs: hardware-suspending try_wait
+// without a time hint (the thread resumes when the phase completes), so that a waiting
+// issuer takes no issue slots from the warps that decode the next stage on its
+// sub-partition (a test_wait spin loop had cost them a large share of the integer pipe).
+K3_DEVI bool mbar_wait_issue(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_test(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_test(bar, parity)) return true;
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > (1ll << 32)) {
       *abort_flag = 1;
@@ -448,7 +450,7 @@ constexpr int TM_ROWS = 128;       // weight rows per MMA (M)
 constexpr int TM_BLOCKS = 2;       // row blocks per tile, each with its own accumulator and MMA issuer
 constexpr int TM_NB = 96;          // tokens per batch (MMA N <= 96): bounded by TMEM columns
 constexpr int TM_BK = 64;          // k-block
-constexpr int TM_PRODUCERS = 8;    // decode warps
+constexpr int TM_PRODUCERS = 16;   // decode warps
 constexpr int TM_EPI = 8;         // epilogue warps: two per TMEM lane quarter, alternate 16-column chunks
 constexpr int TM_COPY_WARP = 3 + TM_EPI + TM_PRODUCERS;  // packed-weight TMA copies
 constexpr int TM_THREADS = (TM_COPY_WARP + 1) * 32;
@@ -554,6 +556,10 @@ K3_DEVI void keep_regs32(const uint32_t (&r)[32]) {
                "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
                "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
                "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
+}
+K3_DEVI void keep_regs16(const uint32_t (&r)[16]) {
+  asm volatile("" ::"r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+               "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
 }
 K3_DEVI void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
@@ -699,13 +705,13 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
         const int n = p.batches[tile / mtiles].n;
         const int N = (n + 15) & ~15;
         const uint32_t idesc = idesc_bf16(TM_ROWS, N);  // bf16 x bf16 -> f32
-        if (!mbar_wait_spin(tempty(0), (lt & 1) ^ 1, abort_flag)) break;  // accumulators emptied
+        if (!mbar_wait_issue(tempty(0), (lt & 1) ^ 1, abort_flag)) break;  // accumulators emptied
         tc_fence_after();
         const uint32_t d = tmem + mm * TM_NB;
         bool ok = true;
         for (int kb = 0; kb < kblocks; kb += TM_AKB, it += TM_AKB) {
           const int st = it / TM_AKB, sa = st % SA, g = st % NBS;
-          if (!mbar_wait_spin(full(g), (st / NBS) & 1, abort_flag)) {
+          if (!mbar_wait_issue(full(g), (st / NBS) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -794,7 +800,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       }
     }
   } else if (warp == TM_COPY_WARP) {
-    // ------------------------------------------------------------ packed-weight copies (warp 19)
+    // ------------------------------------------------------------ packed-weight copies (warp 27)
     // The packed bytes of a tile travel in chunks of CKB k-blocks (ROWB bytes of each of its
     // 256 rows) through a ring of RC slots: per chunk one TMA copy per block (128 rows x
     // ROWB bytes; the 128-byte swizzle puts 16-byte granule c of row r at c ^ (r & 7), the
@@ -880,14 +886,19 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
       }
     }
   } else {
-    // ------------------------------------------------------------ decode producers (warps 11..18)
+    // ------------------------------------------------------------ decode producers (warps 11..26)
     // A chunk's packed and scale bytes come from the copy warp (raw_full / raw_empty);
     // 16-byte granules are XOR-swizzled by row so the decode reads are free of bank
     // conflicts.
-    // Decode: a warp owns the TMEM lane quarter warp % 4 (32 rows) of one block (warps
-    // 11..14 block 0, 15..18 block 1), a k-block's 64 elements per thread (32 columns).
+    // Decode: a warp owns the TMEM lane quarter warp % 4 (32 rows) of one block and one of
+    // the two 32-element scale groups of every k-block (16 TMEM columns): warps 11..14
+    // block 0 group 0, 15..18 block 1 group 0, 19..22 block 0 group 1, 23..26 block 1
+    // group 1; each thread decodes its row's group.
+    static_assert(TM_PRODUCERS == 4 * TM_BLOCKS * 2, "four lane quarters x two blocks x two groups");
+    const int pw = warp - (3 + TM_EPI);
     const int qd = warp & 3;
-    const int mb = (warp - (3 + TM_EPI)) >> 2;
+    const int mb = (pw >> 2) % TM_BLOCKS;
+    const int kg = pw / (4 * TM_BLOCKS);           // scale group within a k-block
     const int ri = mb * TM_ROWS + qd * 32 + lane;  // row of the tile (over both blocks)
     constexpr int CKB = Lay::CKB, ROWB = Lay::ROWB, GPR = Lay::GPR;
     // granule c of row r sits at position c ^ swz(r): conflict-free reads of 8 consecutive rows
@@ -895,6 +906,14 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
     const int kchunks = kblocks / CKB;
     const int my_tiles = (tiles > (int)blockIdx.x) ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int nchunks = my_tiles * kchunks;
+    static_assert(CKB == 4 && TM_AKB == 2, "a chunk is two A stages of two k-blocks");
+    // byte offsets of this thread's granule (its group of k-block kq) inside its row's
+    // ROWB raw bytes, and the byte selector that gathers its four scale bytes (bytes
+    // 2 kq + kg of the row's 8 per chunk)
+    int goff[CKB];
+#pragma unroll
+    for (int kq = 0; kq < CKB; ++kq) goff[kq] = ((2 * kq + kg) ^ swz(ri)) << 4;
+    const uint32_t ssel = kg ? 0x7531u : 0x6420u;
     bool stop = false;
 #pragma unroll 1
     for (int jc = 0; jc < nchunks && !stop; ++jc) {
@@ -904,53 +923,58 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
         break;
       }
       const uint8_t* src = base_ptr + (raw_base - base) + (jc % RC) * Lay::RAW_SLOT + ri * ROWB;
-      const uint8_t* scs = base_ptr + (sraw_base - base) + (jc % RC) * Lay::SC_SLOT + ri * (2 * CKB);
-      uint2 sc8;
-      if constexpr (CKB == 4) sc8 = *reinterpret_cast<const uint2*>(scs);
-      else sc8 = make_uint2(*reinterpret_cast<const uint32_t*>(scs), 0u);
-      // decode k-block kq of the chunk (64 elements of row ri) into a[]: bf16x2 columns in
-      // the interleaved K order
-      uint32_t a[32], a2[32];
-      auto decode = [&](int kq, uint32_t (&out)[32]) {
-        const uint32_t cs = ((kq < 2) ? sc8.x : sc8.y) >> (16 * (kq & 1));  // this k-block's two scale bytes
-        // per 32-element group: the decoded words are v * 2^-126, so the factor is 2^(s-1),
-        // a bf16 power of two (exponent field s + 126) for s <= 128; a larger byte takes
-        // 2^127 and then 2^(s-128) (exponent field s - 1), each product exact
-        uint32_t f1[2], f2[2];
-        bool big = false;
+      const uint2 sc8 = *reinterpret_cast<const uint2*>(base_ptr + (sraw_base - base) + (jc % RC) * Lay::SC_SLOT +
+                                                        ri * (2 * CKB));
+      // the decoded words are v * 2^-126, so a group's factor is 2^(s-1): a bf16 power of
+      // two with exponent field s + 126 when s <= 128.  A chunk in which any thread of the
+      // warp has a larger byte takes 2^127 first and then 2^(s-128) (exponent field s - 1)
+      // for its bytes above 128 (1 for the others); each product is exact.
+      const uint32_t s4 = __byte_perm(sc8.x, sc8.y, ssel);  // byte kq: scale byte of k-block kq
+      bool bg = false;
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          const uint32_t sb = (cs >> (8 * g)) & 0xFFu;
-          const bool bg = sb > 128u;
-          f1[g] = ((bg ? 254u : sb + 126u) << 7) * 0x10001u;
-          f2[g] = ((bg ? sb - 1u : 127u) << 7) * 0x10001u;
-          big |= bg;
+      for (int kq = 0; kq < CKB; ++kq) bg |= ((s4 >> (8 * kq)) & 0xFFu) > 128u;
+      const bool big = __any_sync(0xffffffffu, bg);  // warp-uniform
+      uint32_t f1[CKB], f2[CKB];
+      if (!big) {
+        const uint32_t e4 = s4 + 0x7E7E7E7Eu;  // bytes s + 126 <= 254: no carries
+#pragma unroll
+        for (int kq = 0; kq < CKB; ++kq) {
+          f1[kq] = __byte_perm(e4, 0u, 0x4040u | (kq << 8) | kq) << 7;  // [e, e] in both exponent fields
+          f2[kq] = 0x3F803F80u;                                          // 1.0
         }
-        big = __any_sync(0xffffffffu, big);  // warp-uniform: the second multiply is rare
+      } else {
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          const uint4 cq = *reinterpret_cast<const uint4*>(src + (((2 * kq + g) ^ swz(ri)) << 4));
-          const uint32_t w4[4] = {cq.x, cq.y, cq.z, cq.w};
+        for (int kq = 0; kq < CKB; ++kq) {
+          const uint32_t sb = (s4 >> (8 * kq)) & 0xFFu;
+          f1[kq] = (((sb > 128u) ? 254u : sb + 126u) << 7) * 0x10001u;
+          f2[kq] = (((sb > 128u) ? sb - 1u : 127u) << 7) * 0x10001u;
+        }
+      }
+      // decode this thread's group of k-block kq (32 elements of row ri) into out[]: 16
+      // bf16x2 columns in the interleaved K order
+      auto decode = [&](int kq, uint32_t (&out)[16]) {
+        const uint4 cq = *reinterpret_cast<const uint4*>(src + goff[kq]);
+        const uint32_t w4[4] = {cq.x, cq.y, cq.z, cq.w};
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {  // 8 elements = 4 packed bytes -> 4 bf16x2 columns
-            uint32_t h[4];
-            e2m1x8_to_bf16x8_il(w4[cc], h);
+        for (int cc = 0; cc < 4; ++cc) {  // 8 elements = 4 packed bytes -> 4 bf16x2 columns
+          uint32_t h[4];
+          e2m1x8_to_bf16x8_il(w4[cc], h);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) out[g * 16 + cc * 4 + e] = bf16x2_mul(h[e], f1[g]);
-          }
+          for (int e = 0; e < 4; ++e) out[cc * 4 + e] = bf16x2_mul(h[e], f1[kq]);
         }
         if (big) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) out[i] = bf16x2_mul(out[i], f2[i >> 4]);
+          for (int i = 0; i < 16; ++i) out[i] = bf16x2_mul(out[i], f2[kq]);
         }
       };
       // a tcgen05.st keeps its source registers until tcgen05.wait::st: the stage's second
       // k-block is decoded into other registers while the first one's store is in flight
-      static_assert(TM_AKB == 2, "two k-blocks per A stage");
-#pragma unroll 1
+      uint32_t a[16], a2[16];
+#pragma unroll
       for (int h = 0; h < CKB / TM_AKB; ++h) {
         const int st = jc * (CKB / TM_AKB) + h, sa = st % SA;  // A stage and its slot
-        const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + Lay::A_COL0 + (sa * TM_BLOCKS + mb) * Lay::A_COLS;
+        const uint32_t ta =
+            tmem + ((uint32_t)(qd * 32) << 16) + Lay::A_COL0 + (sa * TM_BLOCKS + mb) * Lay::A_COLS + kg * 16;
         decode(h * TM_AKB, a);
         // the slot's previous stage (st - SA) must have been consumed by the MMAs
         const int j = st - SA;
@@ -959,11 +983,11 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
           break;
         }
         tc_fence_after();
-        tmem_st32(ta, a);
+        tmem_st16(ta, a);
         decode(h * TM_AKB + 1, a2);
-        tmem_st32(ta + 32, a2);
+        tmem_st16(ta + 32, a2);
         tmem_st_wait();
-        keep_regs32(a);
+        keep_regs16(a);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(full(st % NBS));
