@@ -57,6 +57,7 @@ def parse(argv=None):
                     help="profiling case: a smaller expert pool with the same per-expert shapes and top-k")
     ap.add_argument("--tokens", type=int, default=None,
                     help="profiling case: this many tokens instead of the workload's")
+    ap.add_argument("--no-flush", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--oracle-sample", choices=WORKLOADS, default=None, help=argparse.SUPPRESS)
     a = ap.parse_args(argv)
     a.warmup = max(a.warmup, 3)
@@ -84,11 +85,14 @@ def selected_cfgs(a):
 
 
 def kernels_per_step(cfg, tc: bool) -> int:
-    """Kernel launches of one forward (the memsets are not kernels): up to 64 tokens the
-    routing runs as one fused kernel (6 in all); beyond, top-k, the permutation (four
+    """Kernel launches of one forward (the memsets are not kernels): for one token the
+    projections and the routing share one kernel (5 in all); up to 64 tokens the routing
+    runs as one fused kernel (6 in all); beyond, top-k, the permutation (four
     kernels past 2 x 2048 routed slots, else one) and the activation prep (the f16 copy
     of z for the weight-streaming kernels, or on the grouped-GEMM path the slot-order
     gather), around the two projections, the two expert kernels and the combine."""
+    if cfg.T == 1 and cfg.n_experts <= 1024 and cfg.top_k + 8 <= 32:
+        return 5  # one token: projections and routing share one launch
     if cfg.T <= 64:
         return 6
     perm = 4 if cfg.T * cfg.top_k > 2 * 2048 else 1
@@ -460,7 +464,8 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
     torch.cuda.synchronize()
     w0 = time.time()
     for s in range(a.steps):
-        flush.zero_()
+        if not a.no_flush:
+            flush.zero_()
         ev[s][0].record()
         step()
         ev[s][1].record()
@@ -473,7 +478,8 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
     pev = [RawEvents(nph + 1) for _ in range(a.steps)]
     torch.cuda.synchronize()
     for s in range(a.steps):
-        flush.zero_()
+        if not a.no_flush:
+            flush.zero_()
         k3.forward_profiled(*args, pev[s].handles, ids_out=ids, w_out=wts)
     torch.cuda.synchronize()
     phase_ms = {name: statistics.mean(pev[s].ms(i, i + 1) for s in range(a.steps)) for i, name in enumerate(k3.PHASES)}

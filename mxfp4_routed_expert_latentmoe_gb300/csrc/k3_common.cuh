@@ -152,11 +152,40 @@ K3_DEVI float situ_fast(float g, float u) {
 // 2^e as f32 for e in [-126, 127]
 K3_DEVI float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
 
+// Exponent p of a token's f16 activation row: max|z| * 2^p lies in [2^14, 2^15) (0 for an
+// all-zero or non-finite row).  `maxbits` is the f32 bit pattern of max|z| over the row
+// (z values are bf16, so its low 16 bits are zero).
+K3_DEVI int act_exp_from_max(uint32_t maxbits) {
+  const uint32_t mx = maxbits >> 16;
+  int pw = 0;
+  if (mx != 0u && mx < 0x7F80u) {
+    const int ex = (int)(mx >> 7);               // biased exponent field of the largest |z|
+    const int E2 = (ex == 0) ? -127 : ex - 127;  // floor(log2) (subnormal: below -126)
+    pw = 14 - E2;
+  }
+  return pw;
+}
+
 K3_DEVI uint16_t f32_to_bf16_bits(float v) {
   __nv_bfloat16 b = __float2bfloat16_rn(v);
   return *reinterpret_cast<uint16_t*>(&b);
 }
 K3_DEVI float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// Eight bf16 values -> eight f16 values times 2^pw (two exact power-of-two factors, one
+// rounding to f16): the activation operand of the f16 MMAs, from the bf16 row itself.
+K3_DEVI uint4 bf16x8_to_f16x8(uint4 v, int pw) {
+  const float f1 = pow2f(pw >> 1), f2 = pow2f(pw - (pw >> 1));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t r[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const __half2 h = __floats2half2_rn(__uint_as_float(w[k] << 16) * f1 * f2,
+                                        __uint_as_float(w[k] & 0xFFFF0000u) * f1 * f2);
+    r[k] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
 
 // ------------------------------------------------------------------ programmatic dependent launch
 // Wait until the previous kernel in the stream has completed and its writes are

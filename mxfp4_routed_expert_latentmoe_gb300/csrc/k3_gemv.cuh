@@ -41,6 +41,8 @@ struct MxGemvParams {
   int K;                     // reduction length
   const __half* act;         // GATEUP: z16 [T, K]; DOWN: h16 [slots, K]
   const int32_t* act_pow;    // GATEUP: per-token exponent p (z16 = z * 2^p)
+  const uint16_t* act_bf16;  // GATEUP, bulk kernel: z [T, K] bf16 read directly (act unused), or NULL
+  const uint32_t* act_max;   // with act_bf16: per-token max|z| (f32 bits), which fixes p
   void* out;                 // GATEUP: h16 [slots, R] (h * 2^8); DOWN: o f32 [slots, R]
   uint32_t* status;          // device status word (bounded waits of the bulk-copy kernel)
 };
@@ -286,6 +288,7 @@ struct DenseParams {
   float* out0;      // PROJ: logits [T, R0]; PLAIN: out [T, R0]
   uint16_t* out1;   // PROJ: z [T, R1] bf16
   uint32_t* zmax;   // PROJ: per-token max |z| (f32 bits)
+  uint32_t* status; // device status word (bounded waits that run out)
 };
 
 // bytes of one stage: 16 weight rows and NB activation rows of one 64-element chunk

@@ -178,6 +178,7 @@ __global__ void __launch_bounds__((2 + MXB_MAX_WARPS) * 32) k3_mxb_gemv_kernel(M
     // ------------------------------------------------------------ compute warps
     const int c = warp - 2;  // K slice
     const int g = lane >> 2, t = lane & 3;
+    const bool bf_in = (MODE == MX_GATEUP) && p.act_bf16 != nullptr;  // activations read as bf16 z
     grid_dep_wait();
     grid_dep_launch();
     const int total = tiles * (*p.n_batches);
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__((2 + MXB_MAX_WARPS) * 32) k3_mxb_gemv_kernel(M
       int my_tok = 0, my_pow = 0;
       if (c == 0 && lane < n) {
         my_tok = rec->tok[lane];
-        if (MODE == MX_GATEUP) my_pow = p.act_pow[my_tok];
+        if (MODE == MX_GATEUP) my_pow = bf_in ? act_exp_from_max(p.act_max[my_tok]) : p.act_pow[my_tok];
       }
 
       float acc[M][NBLK][4];
@@ -211,21 +212,36 @@ __global__ void __launch_bounds__((2 + MXB_MAX_WARPS) * 32) k3_mxb_gemv_kernel(M
           for (int q = 0; q < 4; ++q) acc[m][nb][q] = 0.f;
       // activation row of this lane's token column in every 8-token block (columns past
       // the batch repeat its last token: their results are never stored)
+      // (GATEUP from bf16 z: 8 bf16 values become the f16 operand, scaled by the token's 2^p)
       const __half* bptr[NBLK];
+      const uint16_t* bptr16[NBLK];
+      int brow[NBLK];
 #pragma unroll
       for (int nb = 0; nb < NBLK; ++nb) {
         const int col = min(nb * 8 + g, n - 1);
         const int row = (MODE == MX_GATEUP) ? rec->tok[col] : slot0 + col;
+        brow[nb] = row;
         bptr[nb] = p.act + (size_t)row * K + c * 256 + 8 * t;
+        bptr16[nb] = (MODE == MX_GATEUP && bf_in) ? p.act_bf16 + (size_t)row * K + c * 256 + 8 * t : nullptr;
       }
+      // the token's 2^p is read when its row is read (the max comes from the previous kernel)
+      auto load_b = [&](int nb, int j, int pw) -> uint4 {
+        if (MODE == MX_GATEUP && bf_in) return bf16x8_to_f16x8(ldg128(bptr16[nb] + 32 * j), pw);
+        return ldg128(bptr[nb] + 32 * j);
+      };
+      auto row_pow = [&](int nb) { return (MODE == MX_GATEUP && bf_in) ? act_exp_from_max(__ldg(p.act_max + brow[nb])) : 0; };
       if (CACHE_B) {
         const int key = (n == 1) ? ((MODE == MX_GATEUP) ? rec->tok[0] : slot0) : -1;
         if (key < 0 || key != bkey) {
+          const int pw = row_pow(0);
 #pragma unroll
-          for (int j = 0; j < MX_GPW; ++j) bcache[CACHE_B ? j : 0] = ldg128(bptr[0] + 32 * j);
+          for (int j = 0; j < MX_GPW; ++j) bcache[CACHE_B ? j : 0] = load_b(0, j, pw);
           bkey = key;
         }
       }
+      int bpw[NBLK];
+#pragma unroll
+      for (int nb = 0; nb < NBLK; ++nb) bpw[nb] = (CACHE_B || !(MODE == MX_GATEUP && bf_in)) ? 0 : row_pow(nb);
       uint2 sc_lo[M], sc_hi[M];
 #pragma unroll
       for (int m = 0; m < M; ++m) {
@@ -261,7 +277,7 @@ __global__ void __launch_bounds__((2 + MXB_MAX_WARPS) * 32) k3_mxb_gemv_kernel(M
 #pragma unroll
         for (int nb = 0; nb < NBLK; ++nb) {
           if (NBLK == 1 || nb * 8 < n) {
-            const uint4 bv = CACHE_B ? bcache[CACHE_B ? j : 0] : ldg128(bptr[nb] + 32 * j);
+            const uint4 bv = CACHE_B ? bcache[CACHE_B ? j : 0] : load_b(nb, j, bpw[nb]);
 #pragma unroll
             for (int m = 0; m < M; ++m) {
               const float z4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -307,6 +323,111 @@ __global__ void __launch_bounds__((2 + MXB_MAX_WARPS) * 32) k3_mxb_gemv_kernel(M
   }
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) flag_status(p.status, K3MOE_DEV_TIMEOUT);
+}
+
+}  // namespace k3
+
+namespace k3 {
+
+// ============================================================================ bf16 GEMV, one token
+// out[r] = W[r, :] . x for the rows of W0 (then W1) with a single activation row x (the
+// decode step's latent projections).  Each CTA owns a contiguous range of rows and its
+// warps take them in turn; a warp reads a whole row with 16-byte non-caching loads, eight
+// per lane in flight (4 KB per warp, the next chunk issued before the current one is
+// used), straight into registers, multiplies with x held in
+// shared memory as f32 and sums in fp32, lanes combined by a fixed butterfly.  Plain
+// vector loads from many warps keep enough bytes in flight per SM to stream at the HBM
+// copy rate (bulk copies of a few KB issued by one thread reach barely half of it).
+constexpr int D1_WARPS = 8;   // warps per CTA
+constexpr int D1_UNR = 8;     // 16-byte loads in flight per lane
+
+K3_DEVI uint4 ldg_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(D1_WARPS * 32, 2) k3_dense_gemv1_kernel(DenseParams p) {
+  extern __shared__ __align__(16) float xs[];  // x as f32, K values
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int K = p.K, KV = K / 8;  // 16-byte vectors per row
+  const int R = p.R0 + p.R1;
+  const int r0 = (int)(((long long)R * blockIdx.x) / gridDim.x);
+  const int r1 = (int)(((long long)R * (blockIdx.x + 1)) / gridDim.x);
+  auto row_ptr = [&](int r) -> const uint4* {
+    return reinterpret_cast<const uint4*>((r < p.R0) ? p.W0 + (size_t)r * K : p.W1 + (size_t)(r - p.R0) * K);
+  };
+  // the first row's first loads do not depend on the previous kernel: issue them before
+  // waiting for it
+  uint4 w[D1_UNR];
+  int r = r0 + warp;
+  if (r < r1) {
+    const uint4* wv = row_ptr(r);
+#pragma unroll
+    for (int u = 0; u < D1_UNR; ++u) {
+      const int v = lane + 32 * u;
+      w[u] = (v < KV) ? ldg_stream(wv + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  grid_dep_wait();
+  grid_dep_launch();
+  for (int v = threadIdx.x; v < K / 2; v += blockDim.x) {
+    const uint32_t xx = __ldg(reinterpret_cast<const uint32_t*>(p.act) + v);
+    reinterpret_cast<float2*>(xs)[v] = make_float2(__uint_as_float(xx << 16), __uint_as_float(xx & 0xFFFF0000u));
+  }
+  __syncthreads();
+  for (; r < r1; r += D1_WARPS) {
+    const uint4* wv = row_ptr(r);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    for (int v0 = 0; v0 < KV; v0 += 32 * D1_UNR) {
+      uint4 cur[D1_UNR];
+#pragma unroll
+      for (int u = 0; u < D1_UNR; ++u) cur[u] = w[u];
+      // next chunk (of this row, else of the warp's next row) in flight while this one is used
+      const int vn = v0 + 32 * D1_UNR;
+      const bool more = vn < KV;
+      const uint4* wn = more ? wv : ((r + D1_WARPS < r1) ? row_ptr(r + D1_WARPS) : nullptr);
+      const int vb = more ? vn : 0;
+      if (wn) {
+#pragma unroll
+        for (int u = 0; u < D1_UNR; ++u) {
+          const int v = vb + lane + 32 * u;
+          w[u] = (v < KV) ? ldg_stream(wn + v) : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < D1_UNR; ++u) {
+        const int v = v0 + lane + 32 * u;
+        if (v < KV) {
+          const float4 xa = reinterpret_cast<const float4*>(xs)[2 * v];
+          const float4 xb = reinterpret_cast<const float4*>(xs)[2 * v + 1];
+          a0 = fmaf(__uint_as_float(cur[u].x << 16), xa.x, a0);
+          a1 = fmaf(__uint_as_float(cur[u].x & 0xFFFF0000u), xa.y, a1);
+          a2 = fmaf(__uint_as_float(cur[u].y << 16), xa.z, a2);
+          a3 = fmaf(__uint_as_float(cur[u].y & 0xFFFF0000u), xa.w, a3);
+          a0 = fmaf(__uint_as_float(cur[u].z << 16), xb.x, a0);
+          a1 = fmaf(__uint_as_float(cur[u].z & 0xFFFF0000u), xb.y, a1);
+          a2 = fmaf(__uint_as_float(cur[u].w << 16), xb.z, a2);
+          a3 = fmaf(__uint_as_float(cur[u].w & 0xFFFF0000u), xb.w, a3);
+        }
+      }
+    }
+    float sum = (a0 + a1) + (a2 + a3);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane == 0) {
+      if (EPI == DN_PROJ && r >= p.R0) {
+        const uint16_t zb = f32_to_bf16_bits(sum);
+        p.out1[r - p.R0] = zb;
+        atomicMax(p.zmax, __float_as_uint(fabsf(bf16_bits_to_f32(zb))));
+      } else {
+        p.out0[r] = sum;
+      }
+    }
+  }
 }
 
 }  // namespace k3

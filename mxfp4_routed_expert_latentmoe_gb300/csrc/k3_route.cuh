@@ -15,6 +15,8 @@ namespace k3 {
 // inputs in double-f32 (about 48 significant bits); candidates are then ranked on the refined values.
 // The ranking compares 64-bit integer images of the (exact) double values: the fp64
 // unit is used only for the rare refinements.
+// Logits are read through L2 (ld.global.cg): the fused one-token front kernel writes them
+// in the same launch that routes, so the read-only path must not be used for them.
 constexpr int REFINE_EXTRA = 8;
 constexpr int TOPK_MAX_P = 64 + REFINE_EXTRA;
 constexpr int TOPK_MAX_E = 2048;
@@ -80,7 +82,7 @@ K3_DEVI void topk_select(const TopkParams& p, int t, TopkScratch& S, int lane, i
 #pragma unroll
   for (int j = 0; j < KPL; ++j) {
     const int e = lane + 32 * j;
-    lg[j] = (e < p.E) ? __ldg(p.logits + (size_t)t * p.E + e) : 0.f;
+    lg[j] = (e < p.E) ? __ldcg(p.logits + (size_t)t * p.E + e) : 0.f;
     bs[j] = (e < p.E) ? __ldg(p.bias + e) : 0.f;
   }
   uint32_t kr[KPL];
@@ -129,7 +131,7 @@ K3_DEVI void topk_select(const TopkParams& p, int t, TopkScratch& S, int lane, i
 K3_DEVI void topk_select_smem(const TopkParams& p, int t, uint32_t* kh, TopkScratch& S, int lane, int P) {
   uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
   for (int e = lane; e < p.E; e += 32) {
-    const float v = sigmoidf_(__ldg(p.logits + (size_t)t * p.E + e)) + __ldg(p.bias + e);
+    const float v = sigmoidf_(__ldcg(p.logits + (size_t)t * p.E + e)) + __ldg(p.bias + e);
     const uint32_t k = f32_order((v == v) ? v + 0.0f : -INFINITY);
     kh[e] = k;
     kmax = max(kmax, k);
@@ -221,11 +223,13 @@ K3_DEVI double refine_logit(const TopkParams& p, int t, int e, int lane) {
 // Everything after the candidate sort, for P <= 32, with candidate k in lane k's
 // registers: near-tie clusters (neighbours by shuffles), fp64 refinement of the flagged
 // candidates, re-ranking when any was refined, weights, stores.
-K3_DEVI void topk_finish_warp(const TopkParams& p, int t, uint64_t key, int lane, int P) {
+// Returns the id of rank `lane` (lanes below K).
+K3_DEVI int topk_finish_warp(const TopkParams& p, int t, uint64_t key, int lane, int P, const float* lg_smem = nullptr) {
   const bool in = lane < P;
   int id = in ? (int)(0xFFFFFFFFu - (uint32_t)key) : 0x7fffffff;
   const float cv = f32_from_order((uint32_t)(key >> 32));
-  float cs = in ? sigmoidf_(__ldg(p.logits + (size_t)t * p.E + id)) : 0.f;  // the weight's score
+  // the weight's score, from the logits copied to shared memory when the caller has them
+  float cs = in ? sigmoidf_(lg_smem ? lg_smem[id] : __ldcg(p.logits + (size_t)t * p.E + id)) : 0.f;
   const float cv_prev = __shfl_up_sync(0xffffffffu, cv, 1);
   const float cv_next = __shfl_down_sync(0xffffffffu, cv, 1);
   const bool linked_prev = in && lane > 0 && (cv_prev - cv) < p.tau;
@@ -279,6 +283,7 @@ K3_DEVI void topk_finish_warp(const TopkParams& p, int t, uint64_t key, int lane
     if (p.w_out) p.w_out[(size_t)t * p.K + lane] = wk;
   }
   __syncwarp();
+  return id;
 }
 
 K3_DEVI void topk_token(const TopkParams& p, int t, float* sb, float* sr, TopkScratch& S, int lane) {
@@ -318,7 +323,7 @@ K3_DEVI void topk_token(const TopkParams& p, int t, float* sb, float* sr, TopkSc
     const int id = (int)(0xFFFFFFFFu - (uint32_t)key);
     S.cv[k] = f32_from_order((uint32_t)(key >> 32));
     S.ci[k] = id;
-    S.cs[k] = sigmoidf_(__ldg(p.logits + (size_t)t * p.E + id));
+    S.cs[k] = sigmoidf_(__ldcg(p.logits + (size_t)t * p.E + id));
   }
   __syncwarp();
   // near-tie clusters: consecutive candidates closer than tau are linked; a cluster
@@ -591,11 +596,12 @@ K3_DEVI void permute_block(const PermParams& p, int32_t* hist, int* wsum) {
 // (expert, flat index) pairs across the lanes gives the stable order; runs of equal
 // experts are the unique experts.  counts/offsets are written for the routed experts
 // only (nothing downstream reads the others).
-K3_DEVI void permute_warp(const PermParams& p, int lane) {
+// lane_id >= 0: the caller's id of slot `lane` (instead of reading p.ids)
+K3_DEVI void permute_warp(const PermParams& p, int lane, const uint8_t* const* tab_smem = nullptr, int lane_id = -1) {
   const int n = p.T * p.K;
   int e = 0x7fffffff, f = 0x7fffffff;
   if (lane < n) {
-    e = p.ids ? p.ids[lane] : p.fixed_expert;
+    e = (lane_id >= 0) ? lane_id : (p.ids ? p.ids[lane] : p.fixed_expert);
     if (e < 0 || e >= p.E) {
       flag_status(p.status, K3MOE_DEV_BAD_ID);
       e = min(max(e, 0), p.E - 1);
@@ -646,14 +652,25 @@ K3_DEVI void permute_warp(const PermParams& p, int lane) {
     if (lane >= off) pre += o;
   }
   const int total = __shfl_sync(0xffffffffu, pre, 31);
+  // tokens of the first batch of this lane's run, taken from the sorted lanes by shuffles
+  int tk0[MX_MAX_NB];
+  const int tokv = valid ? f / p.K : 0;
+#pragma unroll
+  for (int j = 0; j < MX_MAX_NB; ++j) tk0[j] = __shfl_sync(0xffffffffu, tokv, min(run0 + j, 31));
   if (start) {
     p.counts[e] = cnt;
     p.offsets[e] = run0;
     p.uniq[u] = e;
     p.nb_prefix[u] = pre - nbr;
     if (p.ex.gate_q) {
-      const uint8_t* wp[6] = {p.ex.gate_q[e], p.ex.gate_s[e], p.ex.up_q[e], p.ex.up_s[e], p.ex.down_q[e],
-                              p.ex.down_s[e]};
+      const uint8_t* wp[6];
+      if (tab_smem) {
+#pragma unroll
+        for (int k = 0; k < 6; ++k) wp[k] = tab_smem[k * p.E + e];
+      } else {
+        wp[0] = p.ex.gate_q[e]; wp[1] = p.ex.gate_s[e]; wp[2] = p.ex.up_q[e];
+        wp[3] = p.ex.up_s[e]; wp[4] = p.ex.down_q[e]; wp[5] = p.ex.down_s[e];
+      }
       for (int b = 0; b < nbr; ++b) {
         MxBatch* r = p.batches + (pre - nbr) + b;
 #pragma unroll
@@ -662,7 +679,12 @@ K3_DEVI void permute_warp(const PermParams& p, int lane) {
         const int nn = min(p.NB, cnt - b * p.NB);
         r->slot0 = s0;
         r->n = nn;
-        for (int j = 0; j < MX_MAX_NB; ++j) r->tok[j] = (j < nn) ? p.slot_tok[s0 + j] : 0;
+        if (b == 0) {
+#pragma unroll
+          for (int j = 0; j < MX_MAX_NB; ++j) r->tok[j] = (j < nn) ? tk0[j] : 0;
+        } else {
+          for (int j = 0; j < MX_MAX_NB; ++j) r->tok[j] = (j < nn) ? p.slot_tok[s0 + j] : 0;
+        }
         r->pad[0] = r->pad[1] = 0;
       }
     }
@@ -871,29 +893,22 @@ struct Z16Params {
   int32_t* pow2;
 };
 
-// one warp converts one token (L a multiple of 64: 16-byte vectors)
+// one warp converts one token (L a multiple of 64: 16-byte vectors); up to 16 vectors
+// per lane (L <= 4096) the row is read once into registers, all loads in flight together
 K3_DEVI void z16_token(const Z16Params& p, int t, int lane) {
   const uint4* zr = reinterpret_cast<const uint4*>(p.z + (size_t)t * p.L);
-  const int nv = p.L / 8;
-  uint32_t mx = 0;
-  for (int c = lane; c < nv; c += 32) {
-    const uint4 v = zr[c];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  int pw = 0;
-  if (mx != 0u && mx < 0x7F80u) {
-    const int ex = (int)(mx >> 7);               // biased exponent field of the largest |z|
-    const int E2 = (ex == 0) ? -127 : ex - 127;  // floor(log2) (subnormal: below -126)
-    pw = 14 - E2;
-  }
-  if (lane == 0) p.pow2[t] = pw;
   uint4* o = reinterpret_cast<uint4*>(p.z16 + (size_t)t * p.L);
-  for (int c = lane; c < nv; c += 32) {
-    const uint4 v = zr[c];
+  const int nv = p.L / 8;
+  auto exp_of = [&](uint32_t mx) {
+    int pw = 0;
+    if (mx != 0u && mx < 0x7F80u) {
+      const int ex = (int)(mx >> 7);               // biased exponent field of the largest |z|
+      const int E2 = (ex == 0) ? -127 : ex - 127;  // floor(log2) (subnormal: below -126)
+      pw = 14 - E2;
+    }
+    return pw;
+  };
+  auto conv = [&](const uint4& v, int pw) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t r[4];
 #pragma unroll
@@ -902,8 +917,35 @@ K3_DEVI void z16_token(const Z16Params& p, int t, int lane) {
                                           scalbnf(bf16_bits_to_f32(w[k] >> 16), pw));
       r[k] = *reinterpret_cast<const uint32_t*>(&h);
     }
-    o[c] = make_uint4(r[0], r[1], r[2], r[3]);
+    return make_uint4(r[0], r[1], r[2], r[3]);
+  };
+  auto vmax = [](uint32_t mx, const uint4& v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+    return mx;
+  };
+  if (nv <= 16 * 32) {
+    uint4 v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = (lane + 32 * j < nv) ? __ldcg(zr + lane + 32 * j) : make_uint4(0u, 0u, 0u, 0u);
+    uint32_t mx = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) mx = vmax(mx, v[j]);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    const int pw = exp_of(mx);
+    if (lane == 0) p.pow2[t] = pw;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (lane + 32 * j < nv) o[lane + 32 * j] = conv(v[j], pw);
+    return;
   }
+  uint32_t mx = 0;
+  for (int c = lane; c < nv; c += 32) mx = vmax(mx, __ldcg(zr + c));
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  const int pw = exp_of(mx);
+  if (lane == 0) p.pow2[t] = pw;
+  for (int c = lane; c < nv; c += 32) o[c] = conv(__ldcg(zr + c), pw);
 }
 
 __global__ void k3_z16_kernel(Z16Params p) {
@@ -932,6 +974,171 @@ __global__ void k3_gather_rows_kernel(const uint16_t* z, const int32_t* slot_tok
   }
 }
 
+// One token's routing over a whole CTA (E <= TOPK_BLOCK_N, P <= 32), for the decode step.
+// Every thread forms the 32-bit ranking keys of its experts (biased scores' order images),
+// keeps the logits in shared memory for the weights, and copies the expert pointer tables
+// to shared memory for the batch records -- one round trip to memory for all three.  The
+// P-th largest key is then found by a radix select (four passes of an 8-bit digit: a
+// shared histogram of the keys still matching the prefix found so far, scanned from the top
+// by one warp); the keys above it and the lowest ids among the keys equal to it make the
+// P candidates, which one warp sorts (key descending, id ascending) and finishes as
+// topk_finish_warp does.  Short phases with all threads instead of one warp's long chain.
+constexpr int TOPK_BLOCK_N = 1024;
+struct RouteSmem {
+  static constexpr int HIST = 0;                   // 2 x 256 uint32 digit counts
+  static constexpr int CTRL = HIST + 512 * 4;      // prefix, mask, need, n_above, n_tie
+  static constexpr int LG = CTRL + 64;             // E floats: logits
+  static constexpr int CAND = LG + TOPK_BLOCK_N * 4;     // 64 candidate keys
+  static constexpr int TIE = CAND + 64 * 8;        // E ints: ids of keys equal to the threshold
+  static constexpr int TAB = TIE + TOPK_BLOCK_N * 4;     // 6 x E expert tensor pointers
+  __host__ __device__ static constexpr int bytes(int E) { return TAB + 6 * E * 8; }
+};
+
+K3_DEVI void route_one_token_block(const TopkParams& p, const PermParams& pp, uint8_t* sm, int lane, int warp) {
+  uint32_t* hist0 = reinterpret_cast<uint32_t*>(sm + RouteSmem::HIST);  // two buffers, alternating by pass
+  int* ctrl = reinterpret_cast<int*>(sm + RouteSmem::CTRL);
+  float* lgs = reinterpret_cast<float*>(sm + RouteSmem::LG);
+  uint64_t* cand = reinterpret_cast<uint64_t*>(sm + RouteSmem::CAND);
+  int* tie = reinterpret_cast<int*>(sm + RouteSmem::TIE);
+  const uint8_t** tab = reinterpret_cast<const uint8_t**>(sm + RouteSmem::TAB);
+  const int E = p.E, P = min(E, p.K + REFINE_EXTRA);
+  const int nt = blockDim.x;
+  // keys, logits and expert tables (all loads issued before their uses)
+  uint32_t kk[TOPK_BLOCK_N / (PERM_WARPS * 32)];
+#pragma unroll
+  for (int r = 0; r < TOPK_BLOCK_N / (PERM_WARPS * 32); ++r) {
+    const int e = threadIdx.x + r * nt;
+    kk[r] = 0u;  // below every real key
+    if (e < E) {
+      const float l = __ldcg(p.logits + e);
+      lgs[e] = l;
+      const float v = __fdividef(1.0f, 1.0f + __expf(-l)) + __ldg(p.bias + e);
+      kk[r] = f32_order((v == v) ? v + 0.0f : -INFINITY);
+    }
+  }
+  if (pp.ex.gate_q) {
+    const uint8_t* const* src[6] = {pp.ex.gate_q, pp.ex.gate_s, pp.ex.up_q, pp.ex.up_s, pp.ex.down_q, pp.ex.down_s};
+    constexpr int R = TOPK_BLOCK_N / (PERM_WARPS * 32);
+    const uint8_t* v[6][R];
+#pragma unroll
+    for (int k = 0; k < 6; ++k)
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int e = threadIdx.x + r * nt;
+        v[k][r] = (e < E) ? reinterpret_cast<const uint8_t*>(__ldg(reinterpret_cast<const unsigned long long*>(src[k]) + e))
+                          : nullptr;
+      }
+#pragma unroll
+    for (int k = 0; k < 6; ++k)
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int e = threadIdx.x + r * nt;
+        if (e < E) tab[k * E + e] = v[k][r];
+      }
+  }
+  if (threadIdx.x < 512) hist0[threadIdx.x] = 0u;
+  if (threadIdx.x == 0) {
+    ctrl[0] = 0;  // prefix of the P-th largest key found so far
+    ctrl[1] = 0;  // mask of the digits found
+    ctrl[2] = P;  // rank of the wanted key among the keys matching the prefix
+    ctrl[3] = 0;
+    ctrl[4] = 0;
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    uint32_t* hist = hist0 + ((shift >> 3) & 1) * 256;
+    const uint32_t prefix = (uint32_t)ctrl[0], mask = (uint32_t)ctrl[1];
+#pragma unroll
+    for (int r = 0; r < TOPK_BLOCK_N / (PERM_WARPS * 32); ++r) {
+      const int e = threadIdx.x + r * nt;
+      if (e < E && (kk[r] & mask) == prefix) atomicAdd(hist + ((kk[r] >> shift) & 255u), 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l holds the digits 255 - 8l down to 248 - 8l; counts scanned from the top
+      uint32_t c[8], sum = 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[255 - 8 * lane - j];
+        sum += c[j];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      const uint32_t excl = incl - sum, need = (uint32_t)ctrl[2];
+      const unsigned own = __ballot_sync(0xffffffffu, excl < need && need <= incl);
+      if (lane == __ffs(own) - 1) {
+        uint32_t acc = excl;
+#pragma unroll 1
+        for (int j = 0; j < 8; ++j) {
+          if (acc + c[j] >= need) {
+            ctrl[0] = (int)(prefix | ((uint32_t)(255 - 8 * lane - j) << shift));
+            ctrl[1] = (int)(mask | (255u << shift));
+            ctrl[2] = (int)(need - acc);
+            break;
+          }
+          acc += c[j];
+        }
+      }
+    }
+    // the other buffer (read two passes ago, before the barrier above) is cleared for the next pass
+    if (threadIdx.x < 256) hist0[(((shift >> 3) & 1) ^ 1) * 256 + threadIdx.x] = 0u;
+    __syncthreads();
+  }
+  // the P-th largest key is thr; `need` keys equal to it complete the P
+  const uint32_t thr = (uint32_t)ctrl[0];
+  const int need = ctrl[2];
+#pragma unroll
+  for (int r = 0; r < TOPK_BLOCK_N / (PERM_WARPS * 32); ++r) {
+    const int e = threadIdx.x + r * nt;
+    if (e < E && kk[r] > thr) cand[atomicAdd(ctrl + 3, 1)] = ((uint64_t)kk[r] << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e);
+    else if (e < E && kk[r] == thr) tie[atomicAdd(ctrl + 4, 1)] = e;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int n_above = ctrl[3], n_tie = ctrl[4];
+    // the `need` lowest ids among the keys equal to the threshold
+    if (n_tie <= 32) {
+      int id = (lane < n_tie) ? tie[lane] : 0x7fffffff;
+#pragma unroll
+      for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          const int o = __shfl_xor_sync(0xffffffffu, id, stride);
+          const bool up = (lane & size) == 0, lower = (lane & stride) == 0;
+          if ((lower == up) ? (o < id) : (o > id)) id = o;
+        }
+      if (lane < need) cand[n_above + lane] = ((uint64_t)thr << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)id);
+    } else if (lane == 0) {  // many exactly equal scores: selection by smallest id
+      int last = -1;
+      for (int q = 0; q < need; ++q) {
+        int best = 0x7fffffff;
+        for (int i = 0; i < n_tie; ++i)
+          if (tie[i] > last && tie[i] < best) best = tie[i];
+        cand[n_above + q] = ((uint64_t)thr << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)best);
+        last = best;
+      }
+    }
+    __syncwarp();
+    uint64_t v = (lane < P) ? cand[lane] : 0ull;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const uint64_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+        const bool desc = ((lane & size) == 0);
+        const bool lower = ((lane & stride) == 0);
+        if ((lower == desc) ? (o > v) : (o < v)) v = o;
+      }
+    const int id = topk_finish_warp(p, 0, v, lane, P, lgs);
+    permute_warp(pp, lane, pp.ex.gate_q ? tab : nullptr, (lane < p.K) ? id : -1);
+  }
+}
+
 // ============================================================================ fused route tail
 // For small token counts one CTA runs top-k, the permutation and the activation
 // prep back to back (one launch instead of three).
@@ -944,13 +1151,20 @@ __global__ void __launch_bounds__(PERM_WARPS * 32) k3_route_tail_kernel(TopkPara
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   grid_dep_wait();
   grid_dep_launch();
-  // top-k of token t on warp t % 16; the activation prep (independent of routing) of
-  // token t on warp (t + 8) % 16, so both run at once
-  for (int t = warp; t < tp.T; t += PERM_WARPS) {
-    float* sb = reinterpret_cast<float*>(smem) + warp * (2 * tp.E);
-    topk_token(tp, t, sb, sb + tp.E, S[warp], lane);
+  if (tp.T == 1 && tp.E <= TOPK_BLOCK_N && tp.K + REFINE_EXTRA <= 32 && blockDim.x == PERM_WARPS * 32) {
+    // one token: the activation prep (one warp), then the routing over the whole CTA
+    if (warp == 1 && zp.T > 0) z16_token(zp, 0, lane);
+    route_one_token_block(tp, pp, smem, lane, warp);
+    return;
+  } else {
+    // top-k of token t on warp t % 16; the activation prep (independent of routing) of
+    // token t on warp (t + 8) % 16, so both run at once
+    for (int t = warp; t < tp.T; t += PERM_WARPS) {
+      float* sb = reinterpret_cast<float*>(smem) + warp * (2 * tp.E);
+      topk_token(tp, t, sb, sb + tp.E, S[warp], lane);
+    }
+    for (int t = (warp + PERM_WARPS / 2) % PERM_WARPS; t < zp.T; t += PERM_WARPS) z16_token(zp, t, lane);
   }
-  for (int t = (warp + PERM_WARPS / 2) % PERM_WARPS; t < zp.T; t += PERM_WARPS) z16_token(zp, t, lane);
   __syncthreads();
   if (pp.T * pp.K <= 32) {
     if (warp == 0) permute_warp(pp, lane);
@@ -975,14 +1189,15 @@ struct CombineParams {
 
 constexpr int COMB_THREADS = 256;
 constexpr int COMB_MAX_SPLIT = 32;
+constexpr int COMB_ROW_MAX_THREADS = 1024;  // one-column-per-thread row kernel (few tokens)
 
 // grid T, for L <= 8 * 4 * COMB_THREADS: one CTA per token; thread i combines the float4
 // columns i + j * blockDim.x (j < CPT) in k order, the K expert rows read with independent
-// loads, and keeps them in registers; the row's sum of squares is reduced in the CTA
+// loads (KB at a time), and keeps them in registers; the row's sum of squares is reduced in the CTA
 // (warp partials added in warp order) and y and yhat are written from registers.
-template <int CPT>
-__global__ void __launch_bounds__(COMB_THREADS) k3_combine_row_kernel(CombineParams p) {
-  __shared__ float wpart[COMB_THREADS / 32];
+template <int CPT, int MAXT = COMB_THREADS, int KB = 16>
+__global__ void __launch_bounds__(MAXT) k3_combine_row_kernel(CombineParams p) {
+  __shared__ float wpart[MAXT / 32];
   __shared__ const float* rows[64];
   __shared__ float wk[64];
   grid_dep_wait();
@@ -1001,13 +1216,13 @@ __global__ void __launch_bounds__(COMB_THREADS) k3_combine_row_kernel(CombinePar
     const int c4 = threadIdx.x + j * blockDim.x;
     y[j] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (c4 < L4) {
-      for (int k0 = 0; k0 < p.K; k0 += 16) {
-        float4 v[16];
+      for (int k0 = 0; k0 < p.K; k0 += KB) {
+        float4 v[KB];
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
+        for (int q = 0; q < KB; ++q)
           if (k0 + q < p.K) v[q] = reinterpret_cast<const float4*>(rows[k0 + q])[c4];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < KB; ++q) {
           if (k0 + q < p.K) {
             const float wq = wk[k0 + q];
             y[j].x = fmaf(wq, v[q].x, y[j].x);

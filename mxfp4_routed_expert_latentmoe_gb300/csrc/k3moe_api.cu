@@ -11,6 +11,7 @@
 #include "k3_gemv_bulk.cuh"
 #include "k3_route.cuh"
 #include "k3_tc.cuh"
+#include "k3_front.cuh"
 
 namespace {
 
@@ -23,7 +24,7 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 struct WsLayout {
   size_t status, logits, ids, w, zmax, zpow, counts, offsets, slot_of, slot_tok, inv, uniq, n_uniq, nb_prefix,
-      n_batches, cta_cnt, cta_base, batches, z, z16, h16, o, y, yhat, cpart, ccount, act, tmaps, total;
+      n_batches, cta_cnt, cta_base, batches, z, z16, h16, o, y, yhat, cpart, ccount, act, tmaps, zero_end, total;
 };
 
 WsLayout ws_layout(const k3moe_dims& d, int T) {
@@ -37,11 +38,15 @@ WsLayout ws_layout(const k3moe_dims& d, int T) {
   const size_t Tz = (size_t)T, E = (size_t)d.n_experts, K = (size_t)d.top_k, Lt = (size_t)d.latent,
                I = (size_t)d.inter;
   const size_t slots = Tz * K;
+  // the words every forward clears come first (one memset): status word and kernel
+  // counters, per-token max |z|, combine arrival counters
   L.status = take(256);
+  L.zmax = take(Tz * 4);
+  L.ccount = take(Tz * 4);
+  L.zero_end = off;
   L.logits = take(Tz * E * 4);
   L.ids = take(slots * 4);
   L.w = take(slots * 4);
-  L.zmax = take(Tz * 4);
   L.zpow = take(Tz * 4);
   L.counts = take(E * 4);
   L.offsets = take((E + 1) * 4);
@@ -65,7 +70,6 @@ WsLayout ws_layout(const k3moe_dims& d, int T) {
   L.y = take(Tz * Lt * 4);
   L.yhat = take(Tz * Lt * 2);
   L.cpart = take(Tz * COMB_MAX_SPLIT * 4);
-  L.ccount = take(Tz * 4);
   // slot-order bf16 activation rows for the tensor-core expert path (large T only)
   const bool tc = T >= 256;
   L.act = take(tc ? slots * Lt * 2 : 0);
@@ -214,14 +218,36 @@ cudaError_t launch_dense_t(const DenseParams& p, int dev, int sms, cudaStream_t 
   return launch(k3_dense_gemv_kernel<EPI, NBLK, STAGES>, dim3(grid), dim3(DN_WARPS * 32), smem, st, pdl, p);
 }
 
+// one token: rows streamed by plain vector loads (k3_dense_gemv1_kernel), x as f32 in
+// shared memory
+template <int EPI>
+cudaError_t launch_dense1(const DenseParams& p, int dev, int sms, cudaStream_t st, bool pdl) {
+  const int smem = p.K * 4;
+  if (!set_smem<k3_dense_gemv1_kernel<EPI>>(dev, smem)) return cudaErrorInvalidValue;
+  const int per_sm = (2 * (smem + 1024) <= 228 * 1024) ? 2 : 1;  // registers allow two CTAs per SM
+  const int R = p.R0 + p.R1;
+  const int rows_per_cta = 2 * D1_WARPS;  // at least two rows per warp on average
+  int grid = per_sm * sms;
+  if (R < grid * rows_per_cta) grid = (R + rows_per_cta - 1) / rows_per_cta;
+  return launch(k3_dense_gemv1_kernel<EPI>, dim3(grid), dim3(D1_WARPS * 32), smem, st, pdl, p);
+}
+
+bool dense1_ok(const DenseParams& p) {
+  return p.T == 1 && p.K % 8 == 0 && p.K * 4 <= 227 * 1024 && a16(p.act) && a16(p.W0) && (p.R1 == 0 || a16(p.W1));
+}
+
 template <int EPI>
 cudaError_t launch_dense(const DenseParams& p, int dev, int sms, cudaStream_t st, bool pdl) {
+  if (dense1_ok(p)) return launch_dense1<EPI>(p, dev, sms, st, pdl);
   if (p.T <= 8) return launch_dense_t<EPI, 1>(p, dev, sms, st, pdl);
   if (p.T <= 16) return launch_dense_t<EPI, 2>(p, dev, sms, st, pdl);
   return launch_dense_t<EPI, 4>(p, dev, sms, st, pdl);
 }
 
 int mx_nblk(int T) { return T <= 8 ? 1 : 2; }
+
+// the bulk-copy GEMV takes K multiples of 256 up to 256 * MXB_MAX_WARPS
+bool mxb_ok(int K) { return K % 256 == 0 && K / 256 <= MXB_MAX_WARPS; }
 
 // token count from which the projections and experts run on the tcgen05 GEMMs
 // (must match the workspace layout's choice)
@@ -312,7 +338,7 @@ cudaError_t launch_mxb(const MxGemvParams& p, int dev, int sms, cudaStream_t st,
 
 template <int MODE>
 cudaError_t launch_mx(const MxGemvParams& p, int nblk, int dev, int sms, cudaStream_t st, bool pdl) {
-  if (p.K % 256 == 0 && p.K / 256 <= MXB_MAX_WARPS) {
+  if (mxb_ok(p.K)) {
     if constexpr (MODE == MX_GATEUP)
       return nblk == 1 ? launch_mxb<MODE, 1, 3>(p, dev, sms, st, pdl) : launch_mxb<MODE, 2, 2>(p, dev, sms, st, pdl);
     else
@@ -352,7 +378,11 @@ cudaError_t launch_z16(const Z16Params& p, cudaStream_t st, bool pdl) {
   return launch(k3_z16_kernel, dim3((p.T + 7) / 8), dim3(256), 0, st, pdl, p);
 }
 
-int tail_smem(int E) { return PERM_WARPS * 2 * E * 4; }
+int tail_smem(int E) {
+  const int a = PERM_WARPS * 2 * E * 4;  // per-warp top-k buffers; permutation histograms
+  const int b = (E <= TOPK_BLOCK_N) ? RouteSmem::bytes(E) : 0;  // one-token routing
+  return a > b ? a : b;
+}
 bool tail_fits(int T, int E) {
   return T <= TAIL_MAX_T && tail_smem(E) + (int)(PERM_WARPS * sizeof(TopkScratch)) + 1024 <= 227 * 1024;
 }
@@ -371,12 +401,32 @@ cudaError_t launch_route_tail(const TopkParams& tp, const PermParams& pp, const 
   return e;
 }
 
+// one token: router logits, latent down, routing and activation prep in one launch (off:
+// the routing, done by a single warp there, was slower than the separate routing kernel)
+constexpr bool kFusedFront = false;
+bool front1_ok(const DenseParams& dp, const TopkParams& tp) {
+  return dense1_ok(dp) && tp.T == 1 && tp.E <= 1024 && tp.K + REFINE_EXTRA <= 32;
+}
+cudaError_t launch_front1(const FrontParams& f, int dev, int sms, cudaStream_t st) {
+  const int smem = f.d.K * 4;
+  if (!set_smem<k3_front1_kernel>(dev, smem)) return cudaErrorInvalidValue;
+  const int per_sm = (2 * (smem + 4096) <= 228 * 1024) ? 2 : 1;
+  return launch(k3_front1_kernel, dim3(per_sm * sms), dim3(D1_WARPS * 32), smem, st, false, f);
+}
+
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
   // one CTA per token while a thread holds at most 8 float4 columns and there are enough
   // tokens to fill the GPU (few tokens: a row is split over several CTAs for more loads
   // in flight)
   const int L4 = p.L / 4;
-  if (p.T >= kTcMinT && L4 <= 8 * COMB_THREADS && (reinterpret_cast<uintptr_t>(p.gamma) & 15u) == 0) {
+  const bool g16 = (reinterpret_cast<uintptr_t>(p.gamma) & 15u) == 0;
+  if (p.T < kTcMinT && L4 <= COMB_ROW_MAX_THREADS && g16) {
+    // few tokens: one CTA per token, one float4 column per thread (all K rows' loads of a
+    // column in flight at once), the norm reduced inside the CTA
+    const int threads = (L4 + 31) / 32 * 32;
+    return launch(k3_combine_row_kernel<1, COMB_ROW_MAX_THREADS, 8>, dim3(p.T), dim3(threads), 0, st, pdl, p);
+  }
+  if (p.T >= kTcMinT && L4 <= 8 * COMB_THREADS && g16) {
     const int cpt = L4 <= COMB_THREADS ? 1 : L4 <= 2 * COMB_THREADS ? 2 : L4 <= 4 * COMB_THREADS ? 4 : 8;
     const int threads = ((L4 + cpt - 1) / cpt + 31) / 32 * 32;
     switch (cpt) {
@@ -483,6 +533,7 @@ k3moe_status k3moe_route(const k3moe_dims* dims, int32_t T, const uint16_t* x, c
     DenseParams dp{};
     dp.W0 = wr; dp.R0 = d.n_experts; dp.W1 = nullptr; dp.R1 = 0; dp.K = d.hidden; dp.act = x; dp.T = T;
     dp.out0 = at<float>(ws, L.logits);
+    dp.status = at<uint32_t>(ws, L.status);
     K3_TRY(launch_dense<DN_PROJ>(dp, dev, sms, s, false));
   }
   TopkParams tp{};
@@ -517,23 +568,9 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   if (n_events < 0 || (n_events > 0 && !events)) return K3MOE_ERR_ARG;
   const bool pdl = n_events == 0;  // phase events between kernels would serialise them anyway
   K3_TRY(mark(events, n_events, 0, s));
-  K3_TRY(cudaMemsetAsync(status, 0, 256, s));
-  K3_TRY(cudaMemsetAsync(at<void>(ws, L.zmax), 0, (size_t)T * 4, s));
-  K3_TRY(cudaMemsetAsync(at<void>(ws, L.ccount), 0, (size_t)T * 4, s));
-  // router logits and latent down in one weight-streaming pass over x
-  if (T >= kTcMinT) {
-    TcDenseParams tcp{};
-    tcp.out0 = at<float>(ws, L.logits); tcp.out1 = at<uint16_t>(ws, L.z); tcp.zmax = at<uint32_t>(ws, L.zmax);
-    tcp.status = status;
-    K3_TRY(launch_tc_dense<TC_PROJ>(x, T, d.hidden, wr, d.n_experts, w_down, d.latent, tcp, dev, sms, s, false));
-  } else {
-    DenseParams dp{};
-    dp.W0 = wr; dp.R0 = d.n_experts; dp.W1 = w_down; dp.R1 = d.latent; dp.K = d.hidden; dp.act = x; dp.T = T;
-    dp.out0 = at<float>(ws, L.logits); dp.out1 = at<uint16_t>(ws, L.z); dp.zmax = at<uint32_t>(ws, L.zmax);
-    K3_TRY(launch_dense<DN_PROJ>(dp, dev, sms, s, false));
-  }
-  K3_TRY(mark(events, n_events, 1, s));
-  // top-k with double-f32 near-tie refinement, chunk expert union, activation operand prep
+  K3_TRY(cudaMemsetAsync(status, 0, L.zero_end - L.status, s));  // status, counters, z max, combine counts
+  // routing parameters (top-k with double-f32 near-tie refinement, chunk expert union,
+  // activation operand prep)
   TopkParams tp{};
   tp.logits = at<float>(ws, L.logits); tp.bias = bias; tp.x = x; tp.wr = wr;
   tp.T = T; tp.E = d.n_experts; tp.K = d.top_k; tp.H = d.hidden; tp.tau = kTieTau;
@@ -543,20 +580,46 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   const int nblk = mx_nblk(T);
   const int NB = tc ? TM_NB : 8 * nblk;  // tokens per expert batch
   const PermParams pp = perm_params(d, T, d.top_k, at<int32_t>(ws, L.ids), 0, NB, ws, L, experts);
+  // one token: the bulk gate/up GEMV reads z (bf16) and its max itself (converting it once
+  // per warp), so no f16 copy of z is made; batches of several tokens convert per item and
+  // keep the copy made in the routing kernel
+  const bool z_direct = T == 1 && mxb_ok(d.latent);
+  const Z16Params zp{at<uint16_t>(ws, L.z), z_direct ? 0 : T, d.latent, at<__half>(ws, L.z16), at<int32_t>(ws, L.zpow)};
   const int slots = T * d.top_k;
-  if (tc) {
-    // top-k, permutation, then the bf16 activation rows in expert-sorted slot order for
-    // the grouped GEMM (the f16 copy of z that the weight-streaming kernels read is not needed)
-    K3_TRY(launch_topk(tp, dev, s, pdl));
-    K3_TRY(launch_permute(pp, dev, s, pdl));
-    const int per = d.latent / 8;
-    const int gblocks = (int)(((size_t)slots * per + 255) / 256 < (size_t)sms * 8 ? ((size_t)slots * per + 255) / 256
-                                                                                     : (size_t)sms * 8);
-    K3_TRY(launch(k3_gather_rows_kernel, dim3(gblocks), dim3(256), 0, s, pdl, (const uint16_t*)at<uint16_t>(ws, L.z),
-                  (const int32_t*)at<int32_t>(ws, L.slot_tok), slots, (int)d.latent, at<uint16_t>(ws, L.act)));
+  DenseParams dp{};
+  dp.W0 = wr; dp.R0 = d.n_experts; dp.W1 = w_down; dp.R1 = d.latent; dp.K = d.hidden; dp.act = x; dp.T = T;
+  dp.out0 = at<float>(ws, L.logits); dp.out1 = at<uint16_t>(ws, L.z); dp.zmax = at<uint32_t>(ws, L.zmax);
+  dp.status = status;
+  if (kFusedFront && !tc && front1_ok(dp, tp)) {
+    // one token: projections and routing in one launch (the routing runs while the latent
+    // rows stream; the route phase has no launch of its own)
+    FrontParams fp{dp, tp, pp, zp, status + 16};
+    K3_TRY(launch_front1(fp, dev, sms, s));
+    K3_TRY(mark(events, n_events, 1, s));
   } else {
-    const Z16Params zp{at<uint16_t>(ws, L.z), T, d.latent, at<__half>(ws, L.z16), at<int32_t>(ws, L.zpow)};
-    K3_TRY(launch_route_tail(tp, pp, zp, dev, s, pdl));
+    // router logits and latent down in one weight-streaming pass over x
+    if (T >= kTcMinT) {
+      TcDenseParams tcp{};
+      tcp.out0 = at<float>(ws, L.logits); tcp.out1 = at<uint16_t>(ws, L.z); tcp.zmax = at<uint32_t>(ws, L.zmax);
+      tcp.status = status;
+      K3_TRY(launch_tc_dense<TC_PROJ>(x, T, d.hidden, wr, d.n_experts, w_down, d.latent, tcp, dev, sms, s, false));
+    } else {
+      K3_TRY(launch_dense<DN_PROJ>(dp, dev, sms, s, false));
+    }
+    K3_TRY(mark(events, n_events, 1, s));
+    if (tc) {
+      // top-k, permutation, then the bf16 activation rows in expert-sorted slot order for
+      // the grouped GEMM (the f16 copy of z that the weight-streaming kernels read is not needed)
+      K3_TRY(launch_topk(tp, dev, s, pdl));
+      K3_TRY(launch_permute(pp, dev, s, pdl));
+      const int per = d.latent / 8;
+      const int gblocks = (int)(((size_t)slots * per + 255) / 256 < (size_t)sms * 8 ? ((size_t)slots * per + 255) / 256
+                                                                                       : (size_t)sms * 8);
+      K3_TRY(launch(k3_gather_rows_kernel, dim3(gblocks), dim3(256), 0, s, pdl, (const uint16_t*)at<uint16_t>(ws, L.z),
+                    (const int32_t*)at<int32_t>(ws, L.slot_tok), slots, (int)d.latent, at<uint16_t>(ws, L.act)));
+    } else {
+      K3_TRY(launch_route_tail(tp, pp, zp, dev, s, pdl));
+    }
   }
   K3_TRY(mark(events, n_events, 2, s));
   // experts
@@ -569,8 +632,12 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
                     at<void>(ws, L.o), status, at<void>(ws, L.tmaps)};
     K3_TRY(launch_tc_moe<1>(at<uint16_t>(ws, L.h16), slots, dp2, dev, sms, s, pdl));
   } else {
-    K3_TRY(launch_mx<MX_GATEUP>(mx_params(d, L, ws, MX_GATEUP, at<__half>(ws, L.z16), at<void>(ws, L.h16)), nblk,
-                                dev, sms, s, pdl));
+    MxGemvParams gu = mx_params(d, L, ws, MX_GATEUP, at<__half>(ws, L.z16), at<void>(ws, L.h16));
+    if (z_direct) {
+      gu.act_bf16 = at<uint16_t>(ws, L.z);
+      gu.act_max = at<uint32_t>(ws, L.zmax);
+    }
+    K3_TRY(launch_mx<MX_GATEUP>(gu, nblk, dev, sms, s, pdl));
     K3_TRY(mark(events, n_events, 3, s));
     K3_TRY(launch_mx<MX_DOWN>(mx_params(d, L, ws, MX_DOWN, at<__half>(ws, L.h16), at<void>(ws, L.o)), nblk, dev,
                               sms, s, pdl));
@@ -593,6 +660,7 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   } else {
     DenseParams up{};
     up.W0 = w_up; up.R0 = d.hidden; up.K = d.latent; up.act = at<uint16_t>(ws, L.yhat); up.T = T; up.out0 = out;
+    up.status = status;
     K3_TRY(launch_dense<DN_PLAIN>(up, dev, sms, s, pdl));
   }
   K3_TRY(mark(events, n_events, 6, s));
