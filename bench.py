@@ -86,13 +86,14 @@ def selected_cfgs(a):
 
 def kernels_per_step(cfg, tc: bool) -> int:
     """Kernel launches of one forward (the memsets are not kernels): for one token the
-    projections and the routing share one kernel (5 in all); up to 64 tokens the routing
+    router GEMV, then the routing and the latent down projection in one kernel (6 in all);
+    up to 64 tokens the routing
     runs as one fused kernel (6 in all); beyond, top-k, the permutation (four
     kernels past 2 x 2048 routed slots, else one) and the activation prep (the f16 copy
     of z for the weight-streaming kernels, or on the grouped-GEMM path the slot-order
     gather), around the two projections, the two expert kernels and the combine."""
     if cfg.T == 1 and cfg.n_experts <= 1024 and cfg.top_k + 8 <= 32:
-        return 5  # one token: projections and routing share one launch
+        return 6  # one token: router GEMV, then routing and latent down in one launch
     if cfg.T <= 64:
         return 6
     perm = 4 if cfg.T * cfg.top_k > 2 * 2048 else 1

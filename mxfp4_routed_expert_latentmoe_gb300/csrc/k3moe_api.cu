@@ -221,12 +221,12 @@ cudaError_t launch_dense_t(const DenseParams& p, int dev, int sms, cudaStream_t 
 // one token: rows streamed by plain vector loads (k3_dense_gemv1_kernel), x as f32 in
 // shared memory
 template <int EPI>
-cudaError_t launch_dense1(const DenseParams& p, int dev, int sms, cudaStream_t st, bool pdl) {
+cudaError_t launch_dense1(const DenseParams& p, int dev, int sms, cudaStream_t st, bool pdl,
+                          int rows_per_cta = 2 * D1_WARPS) {
   const int smem = p.K * 4;
   if (!set_smem<k3_dense_gemv1_kernel<EPI>>(dev, smem)) return cudaErrorInvalidValue;
   const int per_sm = (2 * (smem + 1024) <= 228 * 1024) ? 2 : 1;  // registers allow two CTAs per SM
   const int R = p.R0 + p.R1;
-  const int rows_per_cta = 2 * D1_WARPS;  // at least two rows per warp on average
   int grid = per_sm * sms;
   if (R < grid * rows_per_cta) grid = (R + rows_per_cta - 1) / rows_per_cta;
   return launch(k3_dense_gemv1_kernel<EPI>, dim3(grid), dim3(D1_WARPS * 32), smem, st, pdl, p);
@@ -401,17 +401,15 @@ cudaError_t launch_route_tail(const TopkParams& tp, const PermParams& pp, const 
   return e;
 }
 
-// one token: router logits, latent down, routing and activation prep in one launch (off:
-// the routing, done by a single warp there, was slower than the separate routing kernel)
-constexpr bool kFusedFront = false;
-bool front1_ok(const DenseParams& dp, const TopkParams& tp) {
-  return dense1_ok(dp) && tp.T == 1 && tp.E <= 1024 && tp.K + REFINE_EXTRA <= 32;
+// one token: router logits, latent down and routing in one launch (k3_front_kernel); the
+// bulk gate/up GEMV then reads z itself
+bool front_ok(const DenseParams& dp, const TopkParams& tp, bool z_direct) {
+  return z_direct && dense1_ok(dp) && tp.T == 1 && tp.E <= TOPK_BLOCK_N && tp.K + REFINE_EXTRA <= 32;
 }
-cudaError_t launch_front1(const FrontParams& f, int dev, int sms, cudaStream_t st) {
-  const int smem = f.d.K * 4;
-  if (!set_smem<k3_front1_kernel>(dev, smem)) return cudaErrorInvalidValue;
-  const int per_sm = (2 * (smem + 4096) <= 228 * 1024) ? 2 : 1;
-  return launch(k3_front1_kernel, dim3(per_sm * sms), dim3(D1_WARPS * 32), smem, st, false, f);
+cudaError_t launch_front(const FrontParams& f, int dev, int sms, cudaStream_t st, bool pdl) {
+  const int smem = front_smem_bytes(f.d.K, f.tp.E);
+  if (!set_smem<k3_front_kernel>(dev, smem)) return cudaErrorInvalidValue;
+  return launch(k3_front_kernel, dim3(2 * sms), dim3(FR_THREADS), smem, st, pdl, f);
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
@@ -590,11 +588,21 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   dp.W0 = wr; dp.R0 = d.n_experts; dp.W1 = w_down; dp.R1 = d.latent; dp.K = d.hidden; dp.act = x; dp.T = T;
   dp.out0 = at<float>(ws, L.logits); dp.out1 = at<uint16_t>(ws, L.z); dp.zmax = at<uint32_t>(ws, L.zmax);
   dp.status = status;
-  if (kFusedFront && !tc && front1_ok(dp, tp)) {
-    // one token: projections and routing in one launch (the routing runs while the latent
-    // rows stream; the route phase has no launch of its own)
-    FrontParams fp{dp, tp, pp, zp, status + 16};
-    K3_TRY(launch_front1(fp, dev, sms, s));
+  if (!tc && front_ok(dp, tp, z_direct) && 2 * (front_smem_bytes(dp.K, d.n_experts) + 1024) <= 228 * 1024) {
+    // one token: the router logits (one warp per row), then routing and latent down in one
+    // launch that starts while the router kernel runs (the latent rows do not depend on it;
+    // the routing waits for it); the route phase has no launch of its own
+    DenseParams rp = dp;
+    rp.W1 = nullptr;
+    rp.R1 = 0;
+    K3_TRY(launch_dense1<DN_PLAIN>(rp, dev, sms, s, false, D1_WARPS));
+    DenseParams zd = dp;
+    zd.W0 = w_down;
+    zd.R0 = d.latent;
+    zd.W1 = nullptr;
+    zd.R1 = 0;
+    FrontParams fp{zd, tp, pp};
+    K3_TRY(launch_front(fp, dev, sms, s, pdl));
     K3_TRY(mark(events, n_events, 1, s));
   } else {
     // router logits and latent down in one weight-streaming pass over x
