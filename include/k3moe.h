@@ -204,9 +204,21 @@ k3moe_status k3moe_permute(const k3moe_dims* dims, int32_t T, const int32_t* ids
  * k3moe_forward_noalloc call on the current device.  Synchronises `stream`. */
 k3moe_status k3moe_device_status(const void* ws, uint32_t* host_out, void* stream);
 
+/* Self-test of the device-side bounded waits (the pages have no counterpart; it checks
+ * the library's own failure reporting): one small kernel waits on an mbarrier that nothing
+ * completes, once with a limit of `limit_cycles` clock cycles (1 .. 2^32) and once with the
+ * kernels' own limit, left early through the abort flag that the first wait sets.  The
+ * kernel returns normally and sets K3MOE_DEV_TIMEOUT in the status word at the start of
+ * `ws` (>= 256 bytes, 16-byte aligned), read with k3moe_device_status(ws, ...).  Nothing
+ * faults, traps or hangs; the wait lasts about limit_cycles plus up to ~0.5 ms. */
+k3moe_status k3moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_cycles, void* stream);
+
 /* Intermediate tensors of the last k3moe_forward that used `ws`, for inspection:
  * 0 = z [T, L] bf16, 1 = yhat [T, L] bf16, 2 = y [T, L] f32 (combined, before the
- * norm), 3 = logits [T, E] f32.  Returns a device pointer inside ws, or NULL. */
+ * norm), 3 = logits [T, E] f32, 4 = h [T*K, I] in expert-sorted slot order (from 256
+ * tokens on, when the grouped GEMM runs: bf16 with the 8 elements of each group stored in
+ * the order 0, 4, 1, 5, 2, 6, 3, 7; below: f16 holding h * 2^8), 5 = o [T*K, L] f32 in
+ * expert-sorted slot order.  Returns a device pointer inside ws, or NULL. */
 void* k3moe_workspace_view(const k3moe_dims* dims, int32_t T, void* ws, int32_t which);
 
 /* Static text for a status code. */

@@ -94,6 +94,7 @@ def lib():
                 "k3moe_permute": ([D, i32, p, p, p, p, p, p, p, sz, p], ctypes.c_int),
                 "k3moe_device_status": ([p, ctypes.POINTER(ctypes.c_uint32), p], ctypes.c_int),
                 "k3moe_workspace_view": ([D, i32, p, i32], p),
+                "k3moe_selftest_wait_timeout": ([p, sz, ctypes.c_int64, p], ctypes.c_int),
                 "k3moe_status_str": ([ctypes.c_int], ctypes.c_char_p),
                 "k3moe_abi_version": ([], i32),
             }
@@ -216,6 +217,12 @@ def device_status(ws, stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check(lib().k3moe_device_status(_ptr(ws), ctypes.byref(v), _stream(stream)), "k3moe_device_status")
     return int(v.value)
+
+
+def selftest_wait_timeout(ws, limit_cycles: int, stream=None):
+    """k3moe_selftest_wait_timeout: a bounded device wait that runs out (sets DEV_TIMEOUT)."""
+    _check(lib().k3moe_selftest_wait_timeout(_ptr(ws), ws.numel() * ws.element_size(), int(limit_cycles),
+                                             _stream(stream)), "k3moe_selftest_wait_timeout")
 
 
 def workspace_view(d: Dims, T: int, ws, which: int) -> int:

@@ -60,8 +60,9 @@ K3_DEVI bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
   return ok != 0;
 }
 // Bounded wait for the phase with the given parity.  Returns false when the CTA's
-// abort flag is set (by this or another thread) or the wait exceeds ~2^32 cycles.
-K3_DEVI bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// abort flag is set (by this or another thread) or the wait exceeds `limit` cycles
+// (~2^32 in the kernels; the self-test uses a short one).
+K3_DEVI bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, long long limit = (1ll << 32)) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
@@ -69,7 +70,7 @@ K3_DEVI bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) 
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait_sleep(bar, parity, 10000u)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > (1ll << 32)) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       return false;
     }
@@ -1003,6 +1004,33 @@ __global__ void __launch_bounds__(TM_THREADS, 1) k3_tc_moe_kernel(const __grid_c
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+}  // namespace k3
+
+namespace k3 {
+
+// Self-test of the bounded waits: an mbarrier that nothing arrives on.  Warp 0 waits with
+// a short limit, runs out, sets the CTA's abort flag; warp 1 waits on the same barrier
+// with the kernels' long limit and leaves through the abort flag.  The kernel then reports
+// K3MOE_DEV_TIMEOUT as every kernel with a bounded wait does, and returns normally.
+__global__ void k3_selftest_timeout_kernel(uint32_t* status, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_sh;
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  volatile int* abort_flag = &abort_sh;
+  bool ok = true;
+  if (warp == 0) ok = mbar_wait(smem_u32(&bar), 0, abort_flag, limit);
+  else if (warp == 1) ok = mbar_wait(smem_u32(&bar), 0, abort_flag);
+  (void)ok;
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) flag_status(status, K3MOE_DEV_TIMEOUT);
 }
 
 }  // namespace k3

@@ -751,6 +751,19 @@ k3moe_status k3moe_permute(const k3moe_dims* dims, int32_t T, const int32_t* ids
   return K3MOE_OK;
 }
 
+k3moe_status k3moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_cycles, void* stream) {
+  if (!ws || ws_bytes < 256 || limit_cycles <= 0 || limit_cycles > (1ll << 32)) return K3MOE_ERR_ARG;
+  if (!a16(ws)) return K3MOE_ERR_ALIGN;
+  int dev, sms;
+  const k3moe_status st = check_device(&dev, &sms);
+  if (st != K3MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  K3_TRY(cudaMemsetAsync(ws, 0, 256, s));
+  k3_selftest_timeout_kernel<<<1, 64, 0, s>>>(static_cast<uint32_t*>(ws), (long long)limit_cycles);
+  K3_TRY(cudaGetLastError());
+  return K3MOE_OK;
+}
+
 void* k3moe_workspace_view(const k3moe_dims* dims, int32_t T, void* ws, int32_t which) {
   if (check_dims(dims) != K3MOE_OK || T < 0 || !ws) return nullptr;
   const WsLayout L = ws_layout(*dims, T);
