@@ -54,11 +54,12 @@ class LayerConfig:
     perturb_sigma: float = 0.0
     rms_eps: float = 1e-6
     x_seed: int | None = None
+    top_p: float = 0.0  # K3_TOPP cumulative-weight pruning of the top-K; 0 = off
 
     @property
     def dims(self):
         return dict(hidden=self.hidden, latent=self.latent, n_experts=self.n_experts, top_k=self.top_k,
-                    inter=self.inter, rms_eps=self.rms_eps)
+                    inter=self.inter, rms_eps=self.rms_eps, top_p=self.top_p)
 
     def with_tokens(self, T: int, x_seed: int | None = None) -> "LayerConfig":
         return dataclasses.replace(self, T=T, x_seed=x_seed)

@@ -25,11 +25,12 @@ EXPERT_TENSORS = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
 
 class Dims(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int), ("latent", ctypes.c_int), ("n_experts", ctypes.c_int),
-                ("top_k", ctypes.c_int), ("inter", ctypes.c_int), ("rms_eps", ctypes.c_double)]
+                ("top_k", ctypes.c_int), ("inter", ctypes.c_int), ("rms_eps", ctypes.c_double),
+                ("top_p", ctypes.c_double)]
 
 
-def dims(hidden, latent, n_experts, top_k, inter, rms_eps=1e-6) -> Dims:
-    return Dims(hidden, latent, n_experts, top_k, inter, rms_eps)
+def dims(hidden, latent, n_experts, top_k, inter, rms_eps=1e-6, top_p=0.0) -> Dims:
+    return Dims(hidden, latent, n_experts, top_k, inter, rms_eps, top_p)
 
 
 def build(force: bool = False) -> str:

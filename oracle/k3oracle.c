@@ -43,6 +43,7 @@
 typedef struct {
   int hidden, latent, n_experts, top_k, inter;
   double rms_eps;
+  double top_p; /* K3_TOPP: 0 < p < 1 prunes the top-K to cumulative weight p; else off */
 } k3o_dims;
 
 /* ----------------------------------------------------------------------------------------
@@ -137,6 +138,49 @@ void k3o_router_logits(const k3o_dims* d, int T, const uint16_t* x, const uint16
  * gap[t] (nullable) = biased score of the k-th minus the (k+1)-th selected expert;
  * mingap[t] (nullable) = smallest difference between consecutive biased scores among
  * the first k+1 (decides whether the selected order is unique). */
+/* K3_TOPP [P1 K3_TOPP paragraph; P2 engine commit "drop the low-weight tail of the top-16
+ * to cumulative weight p, renormalized"]: the K selected experts ordered by weight
+ * (descending; equal weights keep their top-K order), the shortest prefix whose weights
+ * sum to at least p kept (an expert is kept while the weight of those before it is below
+ * p, so the first always is), the kept ones renormalised by their raw scores, the rest
+ * marked id -1 with weight 0.  The kept experts come first, in weight order.  s: raw
+ * scores of all experts; ids, w: one token's K entries, overwritten. */
+static void k3o_top_p(int K, double p, const double* s, int32_t* ids, double* w) {
+  int* ord = (int*)malloc(sizeof(int) * (size_t)K);
+  for (int k = 0; k < K; ++k) ord[k] = k;
+  for (int a = 1; a < K; ++a) { /* insertion sort: stable, descending weight */
+    const int v = ord[a];
+    int b = a - 1;
+    while (b >= 0 && w[ord[b]] < w[v]) {
+      ord[b + 1] = ord[b];
+      --b;
+    }
+    ord[b + 1] = v;
+  }
+  int nkeep = 0;
+  double cum = 0.0;
+  for (int j = 0; j < K; ++j) {
+    if (j > 0 && !(cum < p)) break;
+    cum += w[ord[j]];
+    ++nkeep;
+  }
+  int32_t* id2 = (int32_t*)malloc(sizeof(int32_t) * (size_t)K);
+  double sk = 0.0;
+  for (int j = 0; j < nkeep; ++j) sk += s[ids[ord[j]]];
+  for (int j = 0; j < K; ++j) id2[j] = ids[ord[j]];
+  for (int j = 0; j < K; ++j) {
+    if (j < nkeep) {
+      ids[j] = id2[j];
+      w[j] = s[id2[j]] / sk;
+    } else {
+      ids[j] = -1;
+      w[j] = 0.0;
+    }
+  }
+  free(id2);
+  free(ord);
+}
+
 void k3o_topk(const k3o_dims* d, int T, const double* logits, const float* bias, int32_t* ids, double* w,
               double* gap, double* mingap) {
   const int E = d->n_experts, K = d->top_k;
@@ -166,6 +210,7 @@ void k3o_topk(const k3o_dims* d, int T, const double* logits, const float* bias,
       ids[(size_t)t * K + k] = sel[k];
       w[(size_t)t * K + k] = s[sel[k]] / sum;
     }
+    if (d->top_p > 0.0 && d->top_p < 1.0) k3o_top_p(K, d->top_p, s, ids + (size_t)t * K, w + (size_t)t * K);
     if (gap) gap[t] = (P > K) ? sb[sel[K - 1]] - sb[sel[K]] : INFINITY;
     if (mingap) {
       double m = INFINITY;
@@ -191,12 +236,14 @@ void k3o_permute(int T, int K, int E, const int32_t* ids, int32_t* counts, int32
                  int32_t* uniq, int32_t* n_uniq) {
   const int n = T * K;
   for (int e = 0; e < E; ++e) counts[e] = 0;
-  for (int i = 0; i < n; ++i) counts[ids[i]] += 1;
+  for (int i = 0; i < n; ++i)
+    if (ids[i] >= 0) counts[ids[i]] += 1; /* id -1: a slot pruned by top-p, not placed */
   offsets[0] = 0;
   for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
   int32_t* pos = (int32_t*)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
   for (int e = 0; e < E; ++e) pos[e] = offsets[e];
-  for (int i = 0; i < n; ++i) slot_of[pos[ids[i]]++] = i;
+  for (int i = 0; i < n; ++i)
+    if (ids[i] >= 0) slot_of[pos[ids[i]]++] = i;
   free(pos);
   int u = 0;
   for (int e = 0; e < E; ++e)
@@ -309,15 +356,18 @@ int k3o_forward(const k3o_dims* d, int T, const uint16_t* x, const uint16_t* wr,
   k3o_latent_down(d, T, x, wd, spec, z);
   for (int i = 0; i < T * K; ++i) {
     int e = ids[i];
+    if (e < 0) continue; /* pruned by top-p */
     for (int j = 0; j < 6; ++j)
       if (!ex[j][e]) rc = -(1 + e);
   }
   if (rc) goto done;
+  memset(o, 0, sizeof(double) * (size_t)T * K * L);
 
   if (chunk <= 0) {
 #pragma omp parallel for schedule(dynamic, 1)
     for (int i = 0; i < T * K; ++i) {
       int t = i / K, e = ids[i];
+      if (e < 0) continue;
       k3o_expert(d, z + (size_t)t * L, ex[0][e], ex[1][e], ex[2][e], ex[3][e], ex[4][e], ex[5][e], spec, NULL,
                  o + (size_t)i * L);
     }
@@ -365,6 +415,7 @@ int k3o_forward(const k3o_dims* d, int T, const uint16_t* x, const uint16_t* wr,
   for (int t = 0; t < T; ++t) {
     double* yt = y + (size_t)t * L;
     for (int k = 0; k < K; ++k) {
+      if (ids[(size_t)t * K + k] < 0) continue; /* pruned by top-p */
       const double wk = w[(size_t)t * K + k];
       const double* ok = o + ((size_t)t * K + k) * L;
       for (int c = 0; c < L; ++c) yt[c] += wk * ok[c];
@@ -392,4 +443,4 @@ void k3o_situ_array(int64_t n, const double* g, const double* u, double* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = k3o_situ(g[i], u[i]);
 }
 
-int k3o_abi_version(void) { return 1; }
+int k3o_abi_version(void) { return 2; }

@@ -35,5 +35,5 @@ def oracle_forward(cfg, token_rows=None, spec=True, chunk=0):
         x = np.ascontiguousarray(x[np.asarray(token_rows)])
     d = oracle_dims(cfg)
     ids, _, _, _ = oracle.route(d, x, W["wr"], W["bias"])
-    ex = {int(e): C.expert_tensors(cfg, int(e)) for e in np.unique(ids)}
+    ex = {int(e): C.expert_tensors(cfg, int(e)) for e in np.unique(ids) if e >= 0}
     return oracle.forward(d, x, W["wr"], W["bias"], W["wd"], W["wu"], W["gamma"], ex, spec, chunk)

@@ -2,6 +2,7 @@
 block (CPU only).  Each check compares the oracle with something other than itself:
 closed forms, limits, invariants, brute force on tiny inputs, or numpy library
 primitives in a different summation order."""
+import dataclasses
 import math
 import os
 
@@ -167,6 +168,53 @@ def test_router_sigmoid_closed_form_values():
     assert list(ids[0]) == [0, 1] and np.array_equal(w[0], [0.5, 0.5])
 
 
+def _topk_from_scores(scores, bias, K, top_p):
+    E = len(scores)
+    d = oracle.dims(8, 32, E, K, 64, top_p=top_p)
+    s = np.asarray(scores, dtype=np.float64)
+    lg = np.log(s / (1.0 - s))[None, :]
+    return oracle.topk(d, lg, np.asarray(bias, np.float32))
+
+
+def test_top_p_hand_example():
+    """K3_TOPP (colibri PR #676, K3_TOPP paragraph): weights 0.4, 0.3, 0.2, 0.1 of the top 4."""
+    scores = [0.8, 0.6, 0.4, 0.2, 0.1, 0.05]
+    ids, w, _, _ = _topk_from_scores(scores, np.zeros(6), 4, 0.65)
+    assert list(ids[0]) == [0, 1, -1, -1]
+    assert np.allclose(w[0], [0.8 / 1.4, 0.6 / 1.4, 0.0, 0.0], rtol=1e-14, atol=0)
+    ids, w, _, _ = _topk_from_scores(scores, np.zeros(6), 4, 0.75)  # 0.7 before the third: kept
+    assert list(ids[0]) == [0, 1, 2, -1]
+    assert np.allclose(w[0], [0.8 / 1.8, 0.6 / 1.8, 0.4 / 1.8, 0.0], rtol=1e-14, atol=0)
+    ids, w, _, _ = _topk_from_scores(scores, np.zeros(6), 4, 0.01)  # the first is always kept
+    assert list(ids[0]) == [0, -1, -1, -1] and w[0, 0] == 1.0
+    for off in (0.0, 1.0, 1.5):
+        ids, w, _, _ = _topk_from_scores(scores, np.zeros(6), 4, off)
+        assert list(ids[0]) == [0, 1, 2, 3]
+    # the bias ranks expert 5 first, but the cut follows the weights (raw scores)
+    ids, w, _, _ = _topk_from_scores(scores, [0, 0, 0, 0, 0, 0.9], 4, 0.7)
+    assert list(ids[0]) == [0, 1, -1, -1]
+    assert np.allclose(w[0, :2], [0.8 / 1.4, 0.6 / 1.4], rtol=1e-14, atol=0)
+
+
+def test_top_p_invariants_on_random_routing():
+    d, x, wr, b = _small_router()
+    lg = oracle.router_logits(d, x, wr)
+    ids_all, w_all, _, _ = oracle.topk(d, lg, b)
+    s = 1 / (1 + np.exp(-lg))
+    for p in (0.2, 0.5, 0.8):
+        dp = oracle.dims(d.hidden, d.latent, d.n_experts, d.top_k, d.inter, top_p=p)
+        ids, w, _, _ = oracle.topk(dp, lg, b)
+        for t in range(lg.shape[0]):
+            kept = _np_top_p(s[t, ids_all[t]], w_all[t], p)
+            n = len(kept)
+            assert list(ids[t, :n]) == [int(ids_all[t, k]) for k in kept]
+            assert (ids[t, n:] == -1).all() and (w[t, n:] == 0).all()
+            assert abs(w[t, :n].sum() - 1.0) <= 1e-14
+            cw = np.cumsum(w_all[t, kept])
+            assert cw[-1] >= p - 1e-15 and (n == 1 or cw[-2] < p)
+            assert np.all(np.diff(w_all[t, kept]) <= 0)  # kept in descending weight order
+
+
 # ------------------------------------------------------------------------------ permutation
 def test_permute_matches_stable_sort():
     rng = np.random.default_rng(6)
@@ -224,7 +272,20 @@ def test_expert_matches_dense_numpy():
 
 
 # ------------------------------------------------------------------------------ whole block
-def _np_block(cfg, x, W, experts, spec):
+def _np_top_p(s_sel, w, p):
+    """numpy restatement of K3_TOPP for one token: order by weight (stable), keep while the
+    weight before is below p, renormalise the kept by raw score.  Returns kept positions."""
+    order = sorted(range(len(w)), key=lambda k: -w[k])  # Python's sort is stable
+    kept, cum = [], 0.0
+    for j, k in enumerate(order):
+        if j > 0 and not cum < p:
+            break
+        kept.append(k)
+        cum += w[k]
+    return kept
+
+
+def _np_block(cfg, x, W, experts, spec, top_p=0.0):
     """Brute-force numpy re-implementation of the block from the pages' definitions."""
     E, K, L = cfg.n_experts, cfg.top_k, cfg.latent
     xf = datagen.bf16_to_f64(x)
@@ -237,6 +298,10 @@ def _np_block(cfg, x, W, experts, spec):
     for t in range(x.shape[0]):
         ids = np.argsort(-sb[t], kind="stable")[:K]
         w = s[t, ids] / s[t, ids].sum()
+        if 0.0 < top_p < 1.0:
+            kept = _np_top_p(s[t, ids], w, top_p)
+            ids = ids[kept]
+            w = s[t, ids] / s[t, ids].sum()
         y = np.zeros(L)
         for k, e in enumerate(ids):
             ex = experts[int(e)]
@@ -247,6 +312,21 @@ def _np_block(cfg, x, W, experts, spec):
         yh = rnd(W["gamma"].astype(np.float64) * y / np.sqrt(np.mean(y * y) + cfg.rms_eps))
         out.append(yh @ datagen.bf16_to_f64(W["wu"]).T)
     return np.array(out)
+
+
+@pytest.mark.parametrize("top_p", [0.3, 0.6])
+def test_block_with_top_p_matches_bruteforce_on_tiny(top_p):
+    cfg = dataclasses.replace(C.TINY, top_k=4, top_p=top_p)
+    d = oracle.dims(**cfg.dims)
+    x, W = C.layer_x(cfg), C.layer_weights(cfg)
+    ex = {e: C.expert_tensors(cfg, e) for e in range(cfg.n_experts)}
+    r = oracle.forward(d, x, W["wr"], W["bias"], W["wd"], W["wu"], W["gamma"], ex, False, 0)
+    ref = _np_block(cfg, x, W, ex, False, top_p)
+    assert np.linalg.norm(r["out"] - ref) / np.linalg.norm(ref) < 1e-12
+    assert (r["ids"] == -1).any()  # something was pruned on these tokens
+    # chunked execution (pruned slots take no part in the expert union) is bit-identical
+    r2 = oracle.forward(d, x, W["wr"], W["bias"], W["wd"], W["wu"], W["gamma"], ex, False, 2)
+    assert np.array_equal(r["out"], r2["out"])
 
 
 @pytest.mark.parametrize("spec", [False, True])
