@@ -38,7 +38,9 @@ if ROOT not in sys.path:
 
 METRIC = "K3-shape MXFP4 LatentMoE layer: decode µs/token (HBM GB/s), prefill tokens/s"
 FLUSH_BYTES = 256 << 20
-WORKLOADS = ("decode", "chunk", "prefill")
+WORKLOADS = ("decode", "chunk", "prefill", "decode_top_p")
+DEFAULT_WORKLOADS = ("decode", "chunk", "prefill", "decode_top_p")
+TOP_P = 0.7  # the pages' opt-in K3_TOPP setting
 
 
 def parse(argv=None):
@@ -65,14 +67,17 @@ def parse(argv=None):
 
 
 def workload_cfg(name):
+    import dataclasses
     from datagen import configs as C
+    if name == "decode_top_p":  # decode with the experts pruned to cumulative weight TOP_P
+        return dataclasses.replace(C.DECODE, name="decode_top_p", top_p=TOP_P)
     return {"decode": C.DECODE, "chunk": C.CHUNK, "prefill": C.PREFILL}[name]
 
 
 def selected_cfgs(a):
     """(name, config) of every workload this run times; the first one is the line's headline."""
     import dataclasses
-    names = WORKLOADS if a.workload == "all" else (a.workload,)
+    names = DEFAULT_WORKLOADS if a.workload == "all" else (a.workload,)
     out = []
     for n in names:
         cfg = workload_cfg(n)
@@ -108,8 +113,9 @@ def uses_grouped_gemm(cfg) -> bool:
 
 
 def describe(cfg) -> str:
+    tp = f", top-p {cfg.top_p} (K3_TOPP)" if 0.0 < cfg.top_p < 1.0 else ""
     return (f"{cfg.name}: K3-shape routed layer, T={cfg.T}, H={cfg.hidden}, L={cfg.latent}, E={cfg.n_experts}, "
-            f"K={cfg.top_k}, I={cfg.inter}, MXFP4 experts (scale bytes {cfg.scale_lo}..{cfg.scale_hi}), "
+            f"K={cfg.top_k}{tp}, I={cfg.inter}, MXFP4 experts (scale bytes {cfg.scale_lo}..{cfg.scale_hi}), "
             f"bf16 latent projections")
 
 
@@ -329,7 +335,7 @@ def oracle_sample(cfg, seconds_target: float, min_tokens=1, max_tokens=64):
     def run(rows):
         x = np.ascontiguousarray(x_all[rows])
         ids, _, _, _ = oracle.route(d, x, W["wr"], W["bias"])
-        ex = {int(e): C.expert_tensors(cfg, int(e)) for e in np.unique(ids)}
+        ex = {int(e): C.expert_tensors(cfg, int(e)) for e in np.unique(ids) if e >= 0}
         t0 = time.perf_counter()
         oracle.forward(d, x, W["wr"], W["bias"], W["wd"], W["wu"], W["gamma"], ex, True, 0)
         return time.perf_counter() - t0
@@ -382,7 +388,7 @@ def run_reference(a, cfg, rank, world):
         rows = [rows_cycle[(s * per_step + j) % len(rows_cycle)] for j in range(per_step)]
         x = np.ascontiguousarray(x_all[rows])
         ids, _, _, _ = oracle.route(d, x, W["wr"], W["bias"])
-        prepared.append((x, {int(e): C.expert_tensors(cfg, int(e)) for e in np.unique(ids)}))
+        prepared.append((x, {int(e): C.expert_tensors(cfg, int(e)) for e in np.unique(ids) if e >= 0}))
         if len(prepared) > 8:
             break
     for s in range(a.warmup + a.steps):
@@ -439,7 +445,8 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
         k3.forward(*args, ids_out=ids, w_out=wts)
     torch.cuda.synchronize()
     status = k3.device_status(ws)
-    n_unique = int(np.unique(ids.cpu().numpy()).size)
+    ids_h = ids.cpu().numpy()
+    n_unique = int(np.unique(ids_h[ids_h >= 0]).size)
 
     # the timed step: one k3moe_forward captured into a CUDA graph (its kernels and
     # memsets, chained with programmatic dependent launch) and replayed
@@ -540,7 +547,8 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
     res = {"value": metric_value(cfg, ms, world), "unit": unit, "higher_is_better": hib, "ms_per_step": ms,
            "config": {"workload": describe(cfg), "global_batch": cfg.T * world, "seq_len": cfg.T,
                       "parallelism": f"replicas x{world}", "l2": "flushed by a 256 MiB write before every timed step",
-                      "unique_experts": n_unique, "cuda_graph": graph is not None},
+                      "unique_experts": n_unique, "experts_per_token": float((ids_h >= 0).sum()) / cfg.T,
+                      "cuda_graph": graph is not None},
            "roofline": roof,
            "layer": {"GB_s": step_bytes(cfg, n_unique) / (ms / 1e3) / 1e9,
                      "frac_hbm": step_bytes(cfg, n_unique) / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],

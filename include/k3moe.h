@@ -56,6 +56,12 @@ typedef struct {
   int32_t top_k;     /* K: experts per token (16 for K3); 1..min(E, 64) */
   int32_t inter;     /* I: expert intermediate width (3072 for K3); multiple of 64 */
   float rms_eps;     /* epsilon of the aggregate RMSNorm */
+  float top_p;       /* cumulative-weight pruning of the top-K (K3_TOPP): for 0 < top_p < 1 the
+                        K experts are ordered by weight (equal weights keep their top-K order),
+                        the shortest prefix whose weights reach top_p is kept and renormalised
+                        over its raw scores, and the rest are dropped (id -1, weight 0 in the
+                        routing outputs; no expert work).  0 (or >= 1): off.  With pruning on,
+                        K + 8 <= 32 is required */
 } k3moe_dims;
 
 typedef enum {

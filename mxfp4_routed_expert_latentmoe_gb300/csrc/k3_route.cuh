@@ -28,6 +28,7 @@ struct TopkParams {
   const uint16_t* wr;   // [E, H]
   int T, E, K, H;
   float tau;
+  float top_p;   // cumulative-weight pruning (K3_TOPP): 0 < top_p < 1, else 0 (off)
   int32_t* ids;  // [T, K]
   float* w;      // [T, K]
   int32_t* ids_out;
@@ -275,8 +276,42 @@ K3_DEVI int topk_finish_warp(const TopkParams& p, int t, uint64_t key, int lane,
   float sum = (lane < p.K) ? cs : 0.f;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  float wk = (lane < p.K) ? cs / sum : 0.f;
+  if (p.top_p > 0.f) {
+    // K3_TOPP: the K ordered by weight (equal weights keep their rank order), kept while the
+    // weight before them is below top_p, renormalised over the kept raw scores; the others
+    // become id -1, weight 0.  Lane j ends with the j-th largest weight.
+    uint64_t key = (lane < p.K) ? (((uint64_t)f32_order(wk) << 32) | (uint64_t)(31 - lane)) : 0ull;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const uint64_t ok = __shfl_xor_sync(0xffffffffu, key, stride);
+        const int oi = __shfl_xor_sync(0xffffffffu, id, stride);
+        const float os = __shfl_xor_sync(0xffffffffu, cs, stride);
+        const float ow = __shfl_xor_sync(0xffffffffu, wk, stride);
+        const bool desc = ((lane & size) == 0), lower = ((lane & stride) == 0);
+        if ((lower == desc) ? (ok > key) : (ok < key)) {
+          key = ok;
+          id = oi;
+          cs = os;
+          wk = ow;
+        }
+      }
+    float incl = (lane < p.K) ? wk : 0.f;  // inclusive prefix of the ordered weights
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    const bool keep = lane < p.K && (lane == 0 || (incl - wk) < p.top_p);
+    float ks = keep ? cs : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ks += __shfl_xor_sync(0xffffffffu, ks, off);
+    wk = keep ? cs / ks : 0.f;
+    if (!keep) id = -1;
+  }
   if (lane < p.K) {
-    const float wk = cs / sum;
     p.ids[(size_t)t * p.K + lane] = id;
     p.w[(size_t)t * p.K + lane] = wk;
     if (p.ids_out) p.ids_out[(size_t)t * p.K + lane] = id;
@@ -476,6 +511,18 @@ K3_DEVI int block_scan4(int (&v)[4], int* wsum) {
 }
 
 // hist: PERM_WARPS * E ints of shared memory; wsum: PERM_WARPS + 1 ints
+// Expert of routed slot i: -1 for a slot pruned by top-p (id -1: no position, inv -1);
+// an id outside [0, E) is reported (K3MOE_DEV_BAD_ID) and clamped.
+K3_DEVI int slot_expert(const PermParams& p, int i, bool flag_bad) {
+  int e = p.ids ? p.ids[i] : p.fixed_expert;
+  if (e == -1) return -1;
+  if (e < 0 || e >= p.E) {
+    if (flag_bad) flag_status(p.status, K3MOE_DEV_BAD_ID);
+    e = min(max(e, 0), p.E - 1);
+  }
+  return e;
+}
+
 K3_DEVI void permute_block(const PermParams& p, int32_t* hist, int* wsum) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n = p.T * p.K;
@@ -485,12 +532,8 @@ K3_DEVI void permute_block(const PermParams& p, int32_t* hist, int* wsum) {
   for (int i = threadIdx.x; i < PERM_WARPS * p.E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   for (int i = b0 + lane; i < b1; i += 32) {
-    int e = p.ids ? p.ids[i] : p.fixed_expert;
-    if (e < 0 || e >= p.E) {
-      flag_status(p.status, K3MOE_DEV_BAD_ID);
-      e = min(max(e, 0), p.E - 1);
-    }
-    atomicAdd(&hist[warp * p.E + e], 1);
+    const int e = slot_expert(p, i, true);
+    if (e >= 0) atomicAdd(&hist[warp * p.E + e], 1);
   }
   __syncthreads();
   // per expert: warp-major running offsets, and the expert's count
@@ -524,12 +567,8 @@ K3_DEVI void permute_block(const PermParams& p, int32_t* hist, int* wsum) {
   // stable placement
   for (int base = b0; base < b1; base += 32) {
     const int i = base + lane;
-    const bool valid = i < b1;
-    int e = -1;
-    if (valid) {
-      e = p.ids ? p.ids[i] : p.fixed_expert;
-      e = min(max(e, 0), p.E - 1);
-    }
+    const int e = (i < b1) ? slot_expert(p, i, false) : -2;
+    const bool valid = e >= 0;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     const int leader = __ffs(peers) - 1;
@@ -538,6 +577,8 @@ K3_DEVI void permute_block(const PermParams& p, int32_t* hist, int* wsum) {
       p.slot_of[pos] = i;
       p.slot_tok[pos] = i / p.K;
       p.inv[i] = pos;
+    } else if (e == -1) {
+      p.inv[i] = -1;  // pruned: no position
     }
     __syncwarp();
     if (valid && lane == leader) hist[warp * p.E + e] += __popc(peers);
@@ -597,17 +638,28 @@ K3_DEVI void permute_block(const PermParams& p, int32_t* hist, int* wsum) {
 // experts are the unique experts.  counts/offsets are written for the routed experts
 // only (nothing downstream reads the others).
 // lane_id >= 0: the caller's id of slot `lane` (instead of reading p.ids)
-K3_DEVI void permute_warp(const PermParams& p, int lane, const uint8_t* const* tab_smem = nullptr, int lane_id = -1) {
-  const int n = p.T * p.K;
+K3_DEVI void permute_warp(const PermParams& p, int lane, const uint8_t* const* tab_smem = nullptr, bool have_id = false,
+                          int lane_id = 0) {
+  const int n_all = p.T * p.K;
   int e = 0x7fffffff, f = 0x7fffffff;
-  if (lane < n) {
-    e = (lane_id >= 0) ? lane_id : (p.ids ? p.ids[lane] : p.fixed_expert);
-    if (e < 0 || e >= p.E) {
-      flag_status(p.status, K3MOE_DEV_BAD_ID);
-      e = min(max(e, 0), p.E - 1);
+  if (lane < n_all) {
+    if (have_id) {
+      e = lane_id;
+      if (e != -1 && (e < 0 || e >= p.E)) {
+        flag_status(p.status, K3MOE_DEV_BAD_ID);
+        e = min(max(e, 0), p.E - 1);
+      }
+    } else {
+      e = slot_expert(p, lane, true);
     }
-    f = lane;
+    if (e == -1) {  // pruned by top-p: no position; sorts after every placed slot
+      p.inv[lane] = -1;
+      e = 0x7fffffff;
+    } else {
+      f = lane;
+    }
   }
+  const int n = __popc(__ballot_sync(0xffffffffu, e != 0x7fffffff));  // placed slots
   // bitonic sort ascending by (e, f)
 #pragma unroll
   for (int size = 2; size <= 32; size <<= 1) {
@@ -727,12 +779,8 @@ K3_DEVI void perm_warp_hist(const PermParams& p, int32_t* hist, int& b0, int& b1
   for (int i = threadIdx.x; i < PERM_WARPS * p.E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   for (int i = b0 + lane; i < b1; i += 32) {
-    int e = p.ids ? p.ids[i] : p.fixed_expert;
-    if (e < 0 || e >= p.E) {
-      if (flag_bad) flag_status(p.status, K3MOE_DEV_BAD_ID);
-      e = min(max(e, 0), p.E - 1);
-    }
-    atomicAdd(&hist[warp * p.E + e], 1);
+    const int e = slot_expert(p, i, flag_bad);
+    if (e >= 0) atomicAdd(&hist[warp * p.E + e], 1);
   }
   __syncthreads();
 }
@@ -832,12 +880,8 @@ __global__ void __launch_bounds__(PERM_WARPS * 32) k3_perm_scatter_kernel(PermPa
   __syncthreads();
   for (int base = b0; base < b1; base += 32) {
     const int i = base + lane;
-    const bool valid = i < b1;
-    int e = -1;
-    if (valid) {
-      e = p.ids ? p.ids[i] : p.fixed_expert;
-      e = min(max(e, 0), p.E - 1);
-    }
+    const int e = (i < b1) ? slot_expert(p, i, false) : -2;
+    const bool valid = e >= 0;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     const int leader = __ffs(peers) - 1;
@@ -846,6 +890,8 @@ __global__ void __launch_bounds__(PERM_WARPS * 32) k3_perm_scatter_kernel(PermPa
       p.slot_of[pos] = i;
       p.slot_tok[pos] = i / p.K;
       p.inv[i] = pos;
+    } else if (e == -1) {
+      p.inv[i] = -1;  // pruned: no position
     }
     __syncwarp();
     if (valid && lane == leader) hist[warp * p.E + e] += __popc(peers);
@@ -959,11 +1005,13 @@ __global__ void k3_z16_kernel(Z16Params p) {
 // act[s] = z[slot_tok[s]] for every routed slot: the B operand rows of the tensor-core
 // expert GEMM (one expert's tokens contiguous), bf16, each group of 8 elements stored in
 // the interleaved order 0, 4, 1, 5, 2, 6, 3, 7 that the GEMM's weight decode produces.
-__global__ void k3_gather_rows_kernel(const uint16_t* z, const int32_t* slot_tok, int slots, int L, uint16_t* out) {
+__global__ void k3_gather_rows_kernel(const uint16_t* z, const int32_t* slot_tok, const int32_t* n_placed, int slots,
+                                      int L, uint16_t* out) {
   grid_dep_wait();
   grid_dep_launch();
   const int per = L / 8;  // 16-byte chunks (8 elements) per row
-  const size_t total = (size_t)slots * per;
+  const int ns = min(slots, *n_placed);  // slots pruned by top-p have no position
+  const size_t total = (size_t)ns * per;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const int s = (int)(i / per), c = (int)(i - (size_t)s * per);
     const int t = __ldg(slot_tok + s);
@@ -1135,7 +1183,7 @@ K3_DEVI void route_one_token_block(const TopkParams& p, const PermParams& pp, ui
         if ((lower == desc) ? (o > v) : (o < v)) v = o;
       }
     const int id = topk_finish_warp(p, 0, v, lane, P, lgs);
-    permute_warp(pp, lane, pp.ex.gate_q ? tab : nullptr, (lane < p.K) ? id : -1);
+    permute_warp(pp, lane, pp.ex.gate_q ? tab : nullptr, true, id);
   }
 }
 
@@ -1204,7 +1252,11 @@ __global__ void __launch_bounds__(MAXT) k3_combine_row_kernel(CombineParams p) {
   grid_dep_launch();
   const int t = blockIdx.x;
   if ((int)threadIdx.x < p.K) {
-    rows[threadIdx.x] = p.o + (size_t)p.inv[(size_t)t * p.K + threadIdx.x] * p.L;
+    // a slot pruned by top-p (inv -1, weight 0) has no row: it reads the token's first
+    // slot, which is always kept, and adds nothing
+    int sl = p.inv[(size_t)t * p.K + threadIdx.x];
+    if (sl < 0) sl = p.inv[(size_t)t * p.K];
+    rows[threadIdx.x] = p.o + (size_t)sl * p.L;
     wk[threadIdx.x] = p.w[(size_t)t * p.K + threadIdx.x];
   }
   __syncthreads();
@@ -1272,7 +1324,11 @@ __global__ void __launch_bounds__(COMB_THREADS) k3_combine_norm_kernel(CombinePa
   grid_dep_launch();
   const int t = blockIdx.x, sp = blockIdx.y, nsplit = gridDim.y;
   if ((int)threadIdx.x < p.K) {
-    rows[threadIdx.x] = p.o + (size_t)p.inv[(size_t)t * p.K + threadIdx.x] * p.L;
+    // a slot pruned by top-p (inv -1, weight 0) has no row: it reads the token's first
+    // slot, which is always kept, and adds nothing
+    int sl = p.inv[(size_t)t * p.K + threadIdx.x];
+    if (sl < 0) sl = p.inv[(size_t)t * p.K];
+    rows[threadIdx.x] = p.o + (size_t)sl * p.L;
     wk[threadIdx.x] = p.w[(size_t)t * p.K + threadIdx.x];
   }
   __syncthreads();

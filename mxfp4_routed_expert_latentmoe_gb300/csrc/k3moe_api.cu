@@ -85,6 +85,8 @@ T* at(void* ws, size_t off) {
 
 bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool top_p_on(const k3moe_dims& d) { return d.top_p > 0.0f && d.top_p < 1.0f; }
+
 k3moe_status check_dims(const k3moe_dims* d) {
   if (!d) return K3MOE_ERR_ARG;
   if (d->hidden <= 0 || d->latent <= 0 || d->inter <= 0 || d->n_experts <= 0 || d->top_k <= 0)
@@ -93,6 +95,8 @@ k3moe_status check_dims(const k3moe_dims* d) {
   if (d->n_experts > TOPK_MAX_E || d->top_k > 64 || d->top_k > d->n_experts) return K3MOE_ERR_SHAPE;
   if (d->latent > 32768 || d->inter > 32768 || d->hidden > 65536) return K3MOE_ERR_SHAPE;
   if (!(d->rms_eps >= 0.0f) || d->rms_eps > 1.0f) return K3MOE_ERR_ARG;
+  if (!(d->top_p >= 0.0f)) return K3MOE_ERR_ARG;
+  if (top_p_on(*d) && d->top_k + REFINE_EXTRA > 32) return K3MOE_ERR_SHAPE;
   return K3MOE_OK;
 }
 
@@ -537,6 +541,7 @@ k3moe_status k3moe_route(const k3moe_dims* dims, int32_t T, const uint16_t* x, c
   TopkParams tp{};
   tp.logits = at<float>(ws, L.logits); tp.bias = bias; tp.x = x; tp.wr = wr;
   tp.T = T; tp.E = d.n_experts; tp.K = d.top_k; tp.H = d.hidden; tp.tau = kTieTau;
+  tp.top_p = top_p_on(d) ? d.top_p : 0.f;
   tp.ids = ids; tp.w = w; tp.status = at<uint32_t>(ws, L.status);
   K3_TRY(launch_topk(tp, dev, s, true));
   return K3MOE_OK;
@@ -572,6 +577,7 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   TopkParams tp{};
   tp.logits = at<float>(ws, L.logits); tp.bias = bias; tp.x = x; tp.wr = wr;
   tp.T = T; tp.E = d.n_experts; tp.K = d.top_k; tp.H = d.hidden; tp.tau = kTieTau;
+  tp.top_p = top_p_on(d) ? d.top_p : 0.f;
   tp.ids = at<int32_t>(ws, L.ids); tp.w = at<float>(ws, L.w); tp.ids_out = ids_out; tp.w_out = w_out;
   tp.status = status;
   const bool tc = tc_experts(d, T);
@@ -624,7 +630,9 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
       const int gblocks = (int)(((size_t)slots * per + 255) / 256 < (size_t)sms * 8 ? ((size_t)slots * per + 255) / 256
                                                                                        : (size_t)sms * 8);
       K3_TRY(launch(k3_gather_rows_kernel, dim3(gblocks), dim3(256), 0, s, pdl, (const uint16_t*)at<uint16_t>(ws, L.z),
-                    (const int32_t*)at<int32_t>(ws, L.slot_tok), slots, (int)d.latent, at<uint16_t>(ws, L.act)));
+                    (const int32_t*)at<int32_t>(ws, L.slot_tok),
+                    (const int32_t*)(at<int32_t>(ws, L.offsets) + d.n_experts), slots, (int)d.latent,
+                    at<uint16_t>(ws, L.act)));
     } else {
       K3_TRY(launch_route_tail(tp, pp, zp, dev, s, pdl));
     }
@@ -897,6 +905,6 @@ const char* k3moe_status_str(k3moe_status st) {
   return "unknown status";
 }
 
-int32_t k3moe_abi_version(void) { return 1; }
+int32_t k3moe_abi_version(void) { return 2; }
 
 }  // extern "C"

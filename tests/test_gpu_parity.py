@@ -13,6 +13,7 @@ y by a few 1e-4 relative, which flips some 10% of yhat.  The output error of a t
 then about 1e-3, and a few tokens in a thousand reach 3e-3.  Each token is therefore held
 to PER_TOKEN_BAR = 5e-3 on its own.
 """
+import dataclasses
 import math
 
 import numpy as np
@@ -461,3 +462,71 @@ def test_grouped_gemm_scale_bytes_beyond_the_workloads(k3, lo, hi):
     assert max(per) <= PER_TOKEN_BAR
     del L
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------------------ top-p pruning
+def _top_p_order_gaps(cfg):
+    """Per token: the smallest gap between consecutive weights (descending) of the unpruned
+    top-K, from the oracle (where two weights are closer than fp32 can tell apart, the
+    order of those two in the pruned output is not fixed by the GPU's f32 weights)."""
+    W = C.layer_weights(cfg)
+    d = oracle.dims(**dict(cfg.dims, top_p=0.0))
+    _, w, _, _ = oracle.route(d, C.layer_x(cfg), W["wr"], W["bias"])
+    ws = -np.sort(-w, axis=1)
+    return np.min(np.abs(np.diff(ws, axis=1)), axis=1)
+
+
+def _check_top_p(got, ids, w, ref, gaps, rows=None):
+    rows = list(range(ids.shape[0])) if rows is None else rows
+    rids, rw = ref["ids"], ref["w"]
+    for i, t in enumerate(rows):
+        kept = ids[t] >= 0
+        rk = rids[i] >= 0
+        assert sorted(ids[t][kept]) == sorted(rids[i][rk]), t  # the kept set
+        assert (ids[t][kept.sum():] == -1).all() and np.all(w[t][~kept] == 0)
+        assert abs(w[t].sum() - 1.0) <= 1e-5
+        if gaps[t] > 2e-6:  # the order (weight descending) as well
+            assert np.array_equal(ids[t], rids[i]), t
+            assert np.allclose(w[t], rw[i], rtol=0, atol=2e-6), t
+    r = rel_l2(got[rows], ref["out"])
+    assert r <= REL_L2_BAR, r
+    return r
+
+
+@pytest.mark.parametrize("p", [0.5, 0.7])
+def test_forward_top_p_decode(k3, decode, p):
+    """K3_TOPP on the decode token: the experts kept to cumulative weight p, renormalised;
+    the cut decisions lie at least 5e-3 from p (fp32 and fp64 weights decide alike)."""
+    cfg = dataclasses.replace(C.DECODE, top_p=p)
+    L = decode.with_tokens(k3, cfg)
+    got, ids, w, ws = L.forward(k3)
+    assert k3.device_status(ws) == 0
+    ref = oracle_forward(cfg)
+    r = _check_top_p(got, ids, w, ref, _top_p_order_gaps(cfg))
+    print(f"top-p {p}: {int((ids >= 0).sum())} of {cfg.top_k} experts kept, rel-L2 {r:.2e}")
+
+
+def test_forward_top_p_chunk(k3, decode):
+    cfg = dataclasses.replace(C.CHUNK, top_p=0.5)
+    L = decode.with_tokens(k3, cfg)
+    got, ids, w, ws = L.forward(k3)
+    assert k3.device_status(ws) == 0
+    _check_top_p(got, ids, w, oracle_forward(cfg), _top_p_order_gaps(cfg))
+
+
+def test_forward_top_p_tensor_core_path(k3, prefill):
+    """300 tokens with top-p 0.5: pruned slots leave holes in the permutation that the
+    slot gather, the grouped GEMMs and the combine skip."""
+    cfg = dataclasses.replace(C.PREFILL.with_tokens(300, x_seed=11), top_p=0.5)
+    L = prefill.with_tokens(k3, cfg)
+    got, ids, w, ws = L.forward(k3)
+    assert k3.device_status(ws) == 0
+    rows = [0, 1, 127, 128, 255, 256, 299]
+    gaps = _top_p_order_gaps(cfg)
+    ref = oracle_forward(cfg, token_rows=rows)
+    _check_top_p(got, ids, w, ref, gaps, rows)
+    # every token's kept set, through the router alone
+    Wt = C.layer_weights(cfg)
+    rids, _, _, _ = oracle.route(oracle_dims(cfg), C.layer_x(cfg), Wt["wr"], Wt["bias"])
+    for t in range(cfg.T):
+        assert sorted(ids[t][ids[t] >= 0]) == sorted(rids[t][rids[t] >= 0]), t
