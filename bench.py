@@ -59,6 +59,11 @@ def parse(argv=None):
                     help="profiling case: a smaller expert pool with the same per-expert shapes and top-k")
     ap.add_argument("--tokens", type=int, default=None,
                     help="profiling case: this many tokens instead of the workload's")
+    ap.add_argument("--sweep", type=str, default=None, metavar="T1,T2,...",
+                    help="crossover sweep: time the forward at these token counts on both expert paths "
+                         "(weight-streaming GEMVs and tensor-core GEMMs) and print one JSON line per count")
+    ap.add_argument("--tc-min-tokens", type=int, default=None,
+                    help="token count from which the tensor-core path runs (library default if omitted)")
     ap.add_argument("--no-flush", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--oracle-sample", choices=WORKLOADS, default=None, help=argparse.SUPPRESS)
     a = ap.parse_args(argv)
@@ -97,19 +102,19 @@ def kernels_per_step(cfg, tc: bool) -> int:
     kernels past 2 x 2048 routed slots, else one) and the activation prep (the f16 copy
     of z for the weight-streaming kernels, or on the grouped-GEMM path the slot-order
     gather), around the two projections, the two expert kernels and the combine."""
-    if cfg.T == 1 and cfg.n_experts <= 1024 and cfg.top_k + 8 <= 32:
+    if not tc and cfg.T == 1 and cfg.n_experts <= 1024 and cfg.top_k + 8 <= 32:
         return 6  # one token: router GEMV, then routing and latent down in one launch
-    if cfg.T <= 64:
+    if not tc and cfg.T <= 64:
         return 6
     perm = 4 if cfg.T * cfg.top_k > 2 * 2048 else 1
     return 7 + perm
 
 
-def uses_grouped_gemm(cfg) -> bool:
-    """The library runs the experts on the grouped tcgen05 GEMM from 256 tokens on when both
-    contraction lengths are multiples of 256; smaller batches stream the weights through
-    the MXFP4 GEMV kernels."""
-    return cfg.T >= 256 and cfg.latent % 256 == 0 and cfg.inter % 256 == 0
+def uses_grouped_gemm(cfg, tc_min_tokens: int) -> bool:
+    """The library runs the experts on the grouped tcgen05 GEMM from tc_min_tokens tokens
+    on (k3moe_tc_min_tokens) when both contraction lengths are multiples of 256; smaller
+    batches stream the weights through the MXFP4 GEMV kernels."""
+    return cfg.T >= tc_min_tokens and cfg.latent % 256 == 0 and cfg.inter % 256 == 0
 
 
 def describe(cfg) -> str:
@@ -521,7 +526,7 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
     peaks, peak_kind = measured_peaks()
     alg = algorithmic(cfg, n_unique)
     dom = "gateup"
-    tc = uses_grouped_gemm(cfg)
+    tc = uses_grouped_gemm(cfg, k3.tc_min_tokens())
     if tc:
         # the grouped GEMM runs for milliseconds inside a step of a few milliseconds: the
         # burst bf16 peak is its denominator
@@ -562,6 +567,71 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
     return res
 
 
+def sweep(a, local_rank):
+    """The GEMV / tensor-core crossover: the whole forward of the prefill-shape layer at each
+    token count, once with the tensor-core path forced off and once forced on (the threshold
+    is the library's process-wide k3moe_set_tc_min_tokens), replayed from a CUDA graph with
+    the L2 flushed before each step."""
+    import torch
+
+    import __graft_entry__ as g
+    g.build()
+    import mxfp4_routed_expert_latentmoe_gb300 as k3
+    from datagen import configs as C
+    from datagen import device as D
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    base = C.PREFILL
+    pool, eb, offs = D.expert_pool(base, dev)
+    tables = k3.ExpertTables.from_pool(pool, eb, offs)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    default = k3.tc_min_tokens()
+    for T in [int(v) for v in a.sweep.split(",")]:
+        cfg = base.with_tokens(T, x_seed=base.x_seed)
+        d = k3.dims(**cfg.dims)
+        t = D.layer_tensors(cfg, dev)
+        out = torch.empty(T, cfg.hidden, dtype=torch.float32, device=dev)
+        row = {"sweep": "gemv_vs_tensor_core", "T": T, "default_tc_min_tokens": default}
+        outs = {}
+        for path, thr in (("gemv", 1 << 30), ("tc", 1)):
+            k3.set_tc_min_tokens(thr)
+            ws = torch.empty(k3.workspace_bytes(d, T), dtype=torch.uint8, device=dev)
+            args = (d, t["x"], t["wr"], t["bias"], t["wd"], t["wu"], t["gamma"], tables, out, ws)
+            for _ in range(a.warmup):
+                k3.forward(*args)
+            torch.cuda.synchronize()
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                k3.forward(*args)
+            torch.cuda.current_stream(dev).wait_stream(side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                k3.forward(*args)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+            torch.cuda.synchronize()
+            for s in range(a.steps):
+                flush.zero_()
+                ev[s][0].record()
+                graph.replay()
+                ev[s][1].record()
+            torch.cuda.synchronize()
+            ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+            row[f"{path}_us"] = ms * 1e3
+            row[f"{path}_tokens_per_s"] = T / (ms / 1e3)
+            row[f"{path}_device_status"] = k3.device_status(ws)
+            outs[path] = out.clone()
+            del graph, ws
+        k3.set_tc_min_tokens(default)
+        rel = ((outs["tc"] - outs["gemv"]).norm() / outs["gemv"].norm()).item()
+        row["rel_l2_between_paths"] = rel
+        row["faster"] = "tc" if row["tc_us"] < row["gemv_us"] else "gemv"
+        print(json.dumps(row), flush=True)
+        del t, out, outs
+        torch.cuda.empty_cache()
+
+
 def run_ours(a, cfgs, rank, world, local_rank):
     import torch
 
@@ -569,6 +639,8 @@ def run_ours(a, cfgs, rank, world, local_rank):
     g.build()
     import mxfp4_routed_expert_latentmoe_gb300 as k3
 
+    if a.tc_min_tokens:
+        k3.set_tc_min_tokens(a.tc_min_tokens)
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -622,6 +694,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if a.sweep:
+        sweep(a, local_rank)
+        return
     cfgs = selected_cfgs(a)
     if a.impl == "reference":
         run_reference(a, cfgs[0][1], rank, world)

@@ -125,7 +125,8 @@ k3moe_status k3moe_route(const k3moe_dims* dims, int32_t T, const uint16_t* x, c
                          const float* bias, int32_t* ids, float* w, void* ws, size_t ws_bytes, void* stream);
 
 /* The whole block for T tokens (the chunk's expert union is built once; each
- * selected expert's weights are streamed once per call).
+ * selected expert's weights are streamed once per call).  From 256 tokens on (see
+ * k3moe_set_tc_min_tokens) the projections and experts run on tensor-core GEMMs.
  *   x      [T, H] bf16;  wr [E, H] bf16;  bias [E] f32
  *   w_down [L, H] bf16   latent down;  w_up [H, L] bf16 latent up
  *   norm_w [L]    f32    RMSNorm weight gamma
@@ -209,6 +210,16 @@ k3moe_status k3moe_permute(const k3moe_dims* dims, int32_t T, const int32_t* ids
  * into *host_out.  ws = NULL reads the status word of the last
  * k3moe_forward_noalloc call on the current device.  Synchronises `stream`. */
 k3moe_status k3moe_device_status(const void* ws, uint32_t* host_out, void* stream);
+
+/* Token count from which k3moe_forward (and k3moe_route) run the projections and the
+ * experts on the tensor-core GEMMs instead of the weight-streaming GEMVs (default 256, the
+ * crossover measured on GB300 at K3 shapes).  Process-wide: it changes the workspace size
+ * and the launch sequence of every later call, so set it before sizing workspaces and with
+ * no call in flight.  Returns the previous value, or -1 for t < 1 (nothing changed).  A
+ * tuning control for measuring the crossover; the pages have no counterpart. */
+int32_t k3moe_set_tc_min_tokens(int32_t t);
+/* The current value of that token count. */
+int32_t k3moe_tc_min_tokens(void);
 
 /* Self-test of the device-side bounded waits (the pages have no counterpart; it checks
  * the library's own failure reporting): one small kernel waits on an mbarrier that nothing

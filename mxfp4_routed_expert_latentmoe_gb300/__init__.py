@@ -96,6 +96,8 @@ def lib():
                 "k3moe_device_status": ([p, ctypes.POINTER(ctypes.c_uint32), p], ctypes.c_int),
                 "k3moe_workspace_view": ([D, i32, p, i32], p),
                 "k3moe_selftest_wait_timeout": ([p, sz, ctypes.c_int64, p], ctypes.c_int),
+                "k3moe_set_tc_min_tokens": ([i32], i32),
+                "k3moe_tc_min_tokens": ([], i32),
                 "k3moe_status_str": ([ctypes.c_int], ctypes.c_char_p),
                 "k3moe_abi_version": ([], i32),
             }
@@ -218,6 +220,20 @@ def device_status(ws, stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check(lib().k3moe_device_status(_ptr(ws), ctypes.byref(v), _stream(stream)), "k3moe_device_status")
     return int(v.value)
+
+
+def set_tc_min_tokens(t: int) -> int:
+    """k3moe_set_tc_min_tokens: the token count from which the tensor-core GEMMs run
+    (process-wide); returns the previous value."""
+    prev = int(lib().k3moe_set_tc_min_tokens(int(t)))
+    if prev < 0:
+        raise ValueError("token threshold must be >= 1")
+    return prev
+
+
+def tc_min_tokens() -> int:
+    """k3moe_tc_min_tokens: the token count from which the tensor-core GEMMs run."""
+    return int(lib().k3moe_tc_min_tokens())
 
 
 def selftest_wait_timeout(ws, limit_cycles: int, stream=None):

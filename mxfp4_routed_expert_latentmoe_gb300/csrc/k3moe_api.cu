@@ -19,8 +19,10 @@ using namespace k3;
 
 constexpr float kTieTau = 3e-5f;
 constexpr int kMaxDevices = 64;
+constexpr int kTcMinTokensDefault = 256;  // measured crossover (bench.py --sweep)
 
 size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+int tc_min_t();
 
 struct WsLayout {
   size_t status, logits, ids, w, zmax, zpow, counts, offsets, slot_of, slot_tok, inv, uniq, n_uniq, nb_prefix,
@@ -71,7 +73,7 @@ WsLayout ws_layout(const k3moe_dims& d, int T) {
   L.yhat = take(Tz * Lt * 2);
   L.cpart = take(Tz * COMB_MAX_SPLIT * 4);
   // slot-order bf16 activation rows for the tensor-core expert path (large T only)
-  const bool tc = T >= 256;
+  const bool tc = T >= tc_min_t();
   L.act = take(tc ? slots * Lt * 2 : 0);
   L.tmaps = take(tc ? (size_t)TM_MAX_CTAS * TM_BLOCKS * 2 * 128 : 0);  // packed-weight tensor maps
   L.total = off;
@@ -253,13 +255,16 @@ int mx_nblk(int T) { return T <= 8 ? 1 : 2; }
 // the bulk-copy GEMV takes K multiples of 256 up to 256 * MXB_MAX_WARPS
 bool mxb_ok(int K) { return K % 256 == 0 && K / 256 <= MXB_MAX_WARPS; }
 
-// token count from which the projections and experts run on the tcgen05 GEMMs
-// (must match the workspace layout's choice)
-constexpr int kTcMinT = 256;
+// token count from which the projections and experts run on the tcgen05 GEMMs (the
+// workspace layout follows it); process-wide, set by k3moe_set_tc_min_tokens
+std::atomic<int> g_tc_min_t{kTcMinTokensDefault};
+int tc_min_t() { return g_tc_min_t.load(std::memory_order_relaxed); }
+// token count from which the combine runs one CTA per token with several columns a thread
+constexpr int kCombRowMinT = 256;
 // the grouped expert GEMM moves scale bytes four k-blocks (8 bytes) at a time, so it
 // needs both expert contraction lengths to be multiples of 256; other shapes keep the
 // weight-streaming kernels at every T
-bool tc_experts(const k3moe_dims& d, int T) { return T >= kTcMinT && d.latent % 256 == 0 && d.inter % 256 == 0; }
+bool tc_experts(const k3moe_dims& d, int T) { return T >= tc_min_t() && d.latent % 256 == 0 && d.inter % 256 == 0; }
 
 // grouped MXFP4 expert GEMM on tcgen05; act [slots, K] f16 in slot order
 template <int MODE>
@@ -422,13 +427,13 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
   // in flight)
   const int L4 = p.L / 4;
   const bool g16 = (reinterpret_cast<uintptr_t>(p.gamma) & 15u) == 0;
-  if (p.T < kTcMinT && L4 <= COMB_ROW_MAX_THREADS && g16) {
+  if (p.T < kCombRowMinT && L4 <= COMB_ROW_MAX_THREADS && g16) {
     // few tokens: one CTA per token, one float4 column per thread (all K rows' loads of a
     // column in flight at once), the norm reduced inside the CTA
     const int threads = (L4 + 31) / 32 * 32;
     return launch(k3_combine_row_kernel<1, COMB_ROW_MAX_THREADS, 8>, dim3(p.T), dim3(threads), 0, st, pdl, p);
   }
-  if (p.T >= kTcMinT && L4 <= 8 * COMB_THREADS && g16) {
+  if (p.T >= kCombRowMinT && L4 <= 8 * COMB_THREADS && g16) {
     const int cpt = L4 <= COMB_THREADS ? 1 : L4 <= 2 * COMB_THREADS ? 2 : L4 <= 4 * COMB_THREADS ? 4 : 8;
     const int threads = ((L4 + cpt - 1) / cpt + 31) / 32 * 32;
     switch (cpt) {
@@ -526,7 +531,7 @@ k3moe_status k3moe_route(const k3moe_dims* dims, int32_t T, const uint16_t* x, c
   if ((st = check_device(&dev, &sms)) != K3MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   K3_TRY(cudaMemsetAsync(at<void>(ws, L.status), 0, 256, s));
-  if (T >= kTcMinT) {
+  if (T >= tc_min_t()) {
     TcDenseParams tcp{};
     tcp.out0 = at<float>(ws, L.logits);
     tcp.status = at<uint32_t>(ws, L.status);
@@ -612,7 +617,7 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
     K3_TRY(mark(events, n_events, 1, s));
   } else {
     // router logits and latent down in one weight-streaming pass over x
-    if (T >= kTcMinT) {
+    if (T >= tc_min_t()) {
       TcDenseParams tcp{};
       tcp.out0 = at<float>(ws, L.logits); tcp.out1 = at<uint16_t>(ws, L.z); tcp.zmax = at<uint32_t>(ws, L.zmax);
       tcp.status = status;
@@ -667,7 +672,7 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   K3_TRY(launch_combine(cp, s, pdl));
   K3_TRY(mark(events, n_events, 5, s));
   // latent up
-  if (T >= kTcMinT) {
+  if (T >= tc_min_t()) {
     TcDenseParams tcp{};
     tcp.out0 = out;
     tcp.status = status;
@@ -758,6 +763,13 @@ k3moe_status k3moe_permute(const k3moe_dims* dims, int32_t T, const int32_t* ids
   K3_TRY(launch_permute(pp, dev, s, false));
   return K3MOE_OK;
 }
+
+int32_t k3moe_set_tc_min_tokens(int32_t t) {
+  if (t < 1) return -1;
+  return g_tc_min_t.exchange(t);
+}
+
+int32_t k3moe_tc_min_tokens(void) { return tc_min_t(); }
 
 k3moe_status k3moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_cycles, void* stream) {
   if (!ws || ws_bytes < 256 || limit_cycles <= 0 || limit_cycles > (1ll << 32)) return K3MOE_ERR_ARG;

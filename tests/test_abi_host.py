@@ -141,3 +141,22 @@ def test_noalloc_scratch_limit_is_the_workspace_size_rule():
                                        None) == ERR_DEVICE
         st = ctypes.c_uint32(0)
         assert L.k3moe_device_status(None, ctypes.byref(st), None) == ERR_DEVICE
+
+
+def test_tensor_core_threshold_moves_the_workspace_step():
+    """k3moe_set_tc_min_tokens moves the token count at which the workspace grows by the
+    tensor-core path's buffers, returns the previous value and rejects t < 1."""
+    L = k3.lib()
+    d = _d()
+    prev = k3.set_tc_min_tokens(64)
+    try:
+        assert prev == 256
+        step = lambda T: L.k3moe_workspace_bytes(ctypes.byref(d), T) - L.k3moe_workspace_bytes(ctypes.byref(d), T - 1)
+        tc_bytes = 64 * 16 * 3584 * 2
+        assert step(64) >= tc_bytes and step(63) < tc_bytes and step(256) < tc_bytes
+        with pytest.raises(ValueError):
+            k3.set_tc_min_tokens(0)
+        assert k3.set_tc_min_tokens(64) == 64
+    finally:
+        k3.set_tc_min_tokens(prev)
+    assert L.k3moe_set_tc_min_tokens(256) == 256

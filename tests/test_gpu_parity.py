@@ -530,3 +530,36 @@ def test_forward_top_p_tensor_core_path(k3, prefill):
     rids, _, _, _ = oracle.route(oracle_dims(cfg), C.layer_x(cfg), Wt["wr"], Wt["bias"])
     for t in range(cfg.T):
         assert sorted(ids[t][ids[t] >= 0]) == sorted(rids[t][rids[t] >= 0]), t
+
+
+_CROSSOVER_REF = {}
+
+
+@pytest.mark.parametrize("T", [64, 128, 256, 512, 1024])
+@pytest.mark.parametrize("path", ["gemv", "tc"])
+def test_forward_both_expert_paths_across_the_crossover(k3, prefill, T, path):
+    """The token counts around the GEMV / tensor-core crossover, each run on both paths
+    (k3moe_set_tc_min_tokens forces one or the other): ids bit-exact for every token,
+    sampled outputs within the pooled bar and each within PER_TOKEN_BAR."""
+    cfg = C.PREFILL.with_tokens(T, x_seed=17 + T)
+    L = prefill.with_tokens(k3, cfg)
+    prev = k3.set_tc_min_tokens(1 if path == "tc" else 1 << 30)
+    try:
+        got, ids, w, ws = L.forward(k3)
+        status = k3.device_status(ws)
+    finally:
+        k3.set_tc_min_tokens(prev)
+    assert status == 0
+    if T not in _CROSSOVER_REF:
+        rows = sorted({0, T // 2 - 1, T // 2, T - 1} | set(int(r) for r in np.random.default_rng(T).choice(T, 8,
+                                                                                                        replace=False)))
+        rids, rw, _, _ = oracle_route(cfg)
+        _CROSSOVER_REF[T] = (rows, rids, rw, oracle_forward(cfg, token_rows=rows))
+    rows, rids, rw, ref = _CROSSOVER_REF[T]
+    assert np.array_equal(ids, rids)
+    assert np.allclose(w, rw, rtol=0, atol=2e-6)
+    pooled = rel_l2(got[rows], ref["out"])
+    per = [rel_l2(got[r], ref["out"][i]) for i, r in enumerate(rows)]
+    print(f"T={T} {path}: rel-L2 {pooled:.3e}, worst token {max(per):.3e}")
+    assert pooled <= REL_L2_BAR, pooled
+    assert max(per) <= PER_TOKEN_BAR, max(per)
