@@ -38,8 +38,8 @@ if ROOT not in sys.path:
 
 METRIC = "K3-shape MXFP4 LatentMoE layer: decode µs/token (HBM GB/s), prefill tokens/s"
 FLUSH_BYTES = 256 << 20
-WORKLOADS = ("decode", "chunk", "prefill", "decode_top_p")
-DEFAULT_WORKLOADS = ("decode", "chunk", "prefill", "decode_top_p")
+WORKLOADS = ("decode", "chunk", "prefill", "decode_top_p", "prefill_mxfp8")
+DEFAULT_WORKLOADS = ("decode", "chunk", "prefill", "decode_top_p", "prefill_mxfp8")
 TOP_P = 0.7  # the pages' opt-in K3_TOPP setting
 
 
@@ -76,6 +76,8 @@ def workload_cfg(name):
     from datagen import configs as C
     if name == "decode_top_p":  # decode with the experts pruned to cumulative weight TOP_P
         return dataclasses.replace(C.DECODE, name="decode_top_p", top_p=TOP_P)
+    if name == "prefill_mxfp8":  # prefill with the low-precision-activation variant
+        return dataclasses.replace(C.PREFILL, name="prefill_mxfp8", act_mxfp8=1)
     return {"decode": C.DECODE, "chunk": C.CHUNK, "prefill": C.PREFILL}[name]
 
 
@@ -121,11 +123,15 @@ def describe(cfg) -> str:
     tp = f", top-p {cfg.top_p} (K3_TOPP)" if 0.0 < cfg.top_p < 1.0 else ""
     return (f"{cfg.name}: K3-shape routed layer, T={cfg.T}, H={cfg.hidden}, L={cfg.latent}, E={cfg.n_experts}, "
             f"K={cfg.top_k}{tp}, I={cfg.inter}, MXFP4 experts (scale bytes {cfg.scale_lo}..{cfg.scale_hi}), "
-            f"bf16 latent projections")
+            f"bf16 latent projections" + (", MXFP8 expert activations (lossy variant)" if cfg.act_mxfp8 else ""))
+
+
+def is_prefill(cfg) -> bool:
+    return cfg.name.startswith("prefill")
 
 
 def unit_of(cfg):
-    return ("tokens/s", True) if cfg.name == "prefill" else ("µs/token", False)
+    return ("tokens/s", True) if is_prefill(cfg) else ("µs/token", False)
 
 
 def max_over_ranks(ms: float, world: int, device=None) -> float:
@@ -142,7 +148,7 @@ def max_over_ranks(ms: float, world: int, device=None) -> float:
 
 def metric_value(cfg, ms_per_step, world):
     """Whole-job value of N replicas that each process cfg.T tokens per step."""
-    if cfg.name == "prefill":
+    if is_prefill(cfg):
         return cfg.T * world / (ms_per_step / 1e3)
     return ms_per_step * 1e3 / (cfg.T * world)
 
@@ -158,10 +164,14 @@ def algorithmic(cfg, n_unique):
     """Algorithmic bytes (HBM) and flops per phase for one step."""
     T, H, L, E, K, I = cfg.T, cfg.hidden, cfg.latent, cfg.n_experts, cfg.top_k, cfg.inter
     gu, dn = expert_bytes(cfg)
+    if cfg.act_mxfp8:  # the slot-order MXFP8 activation rows: one code byte + 1/32 scale byte
+        za, ha = T * K * L * 33 // 32, T * K * I * 33 // 32
+    else:
+        za, ha = T * L * 2, T * K * I * 2
     return {
         "proj": dict(bytes=(E * H + L * H) * 2 + T * H * 2 + T * (E * 4 + L * 2), flops=2 * T * H * (E + L)),
-        "gateup": dict(bytes=n_unique * gu + T * L * 2 + T * K * I * 2, flops=2 * T * K * 2 * I * L),
-        "down": dict(bytes=n_unique * dn + T * K * I * 2 + T * K * L * 4, flops=2 * T * K * L * I),
+        "gateup": dict(bytes=n_unique * gu + za + ha, flops=2 * T * K * 2 * I * L),
+        "down": dict(bytes=n_unique * dn + ha + T * K * L * 4, flops=2 * T * K * L * I),
         "up": dict(bytes=H * L * 2 + T * L * 2 + T * H * 4, flops=2 * T * H * L),
     }
 
@@ -350,7 +360,7 @@ def oracle_sample(cfg, seconds_target: float, min_tokens=1, max_tokens=64):
     n = int(max(min_tokens, min(max_tokens, T, seconds_target / max(t1, 1e-3))))
     rows = list(range(n)) if n <= T else [i % T for i in range(n)]
     el = run(rows)
-    val = (n / el) if cfg.name == "prefill" else (el / n * 1e6)
+    val = (n / el) if is_prefill(cfg) else (el / n * 1e6)
     return val, oracle.threads_used(), f"the first {n} token(s) of the {cfg.name} workload, token at a time", el
 
 
@@ -385,7 +395,7 @@ def run_reference(a, cfg, rank, world):
     d = oracle.dims(**cfg.dims)
     W = C.layer_weights(cfg)
     x_all = C.layer_x(cfg)
-    per_step = 1 if cfg.name != "prefill" else 2
+    per_step = 1 if not is_prefill(cfg) else 2
     steps = []
     rows_cycle = list(range(x_all.shape[0]))
     prepared = []
@@ -404,7 +414,7 @@ def run_reference(a, cfg, rank, world):
         if s >= a.warmup:
             steps.append(el)
     ms = statistics.mean(steps) * 1e3
-    val = (per_step / (ms / 1e3)) if cfg.name == "prefill" else ms * 1e3 / per_step
+    val = (per_step / (ms / 1e3)) if is_prefill(cfg) else ms * 1e3 / per_step
     cores = oracle.threads_used()
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": unit, "n_gpus": a.gpus, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": hib, "scaling": "weak", "vs_baseline": None,
@@ -527,7 +537,24 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
     alg = algorithmic(cfg, n_unique)
     dom = "gateup"
     tc = uses_grouped_gemm(cfg, k3.tc_min_tokens())
-    if tc:
+    if tc and cfg.act_mxfp8:
+        # block-scaled MMAs at the fp8 rate: peak = the measured bf16 burst x the nominal
+        # 2x fp8/bf16 ratio; the weights also stream from HBM once -- report the tighter bound
+        t_s = phase_ms[dom] / 1e3
+        tf = alg[dom]["flops"] / t_s / 1e12
+        gb = alg[dom]["bytes"] / t_s / 1e9
+        fp8_peak = 2 * peaks["bf16_tflops"]
+        f_t, f_h = tf / fp8_peak, gb / peaks["hbm_gbs"]
+        if f_h >= f_t:
+            roof = {"bound": "hbm", "achieved": gb, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": f_h,
+                    "peak_kind": f"{peak_kind} HBM copy"}
+        else:
+            roof = {"bound": "tensor", "achieved": tf, "peak": fp8_peak, "unit": "TFLOP/s", "frac": f_t,
+                    "peak_kind": f"{peak_kind} bf16 burst x 2 (nominal fp8/bf16 ratio)"}
+        roof.update({"traffic": profiled_traffic(dom, cfg.name), "kernel": "k3_mx8_moe_kernel<0> (gate/up)",
+                     "other_bound_frac": f_t if f_h >= f_t else f_h,
+                     "tflops_bf16_equivalent_frac": tf / peaks["bf16_tflops"]})
+    elif tc:
         # the grouped GEMM runs for milliseconds inside a step of a few milliseconds: the
         # burst bf16 peak is its denominator
         achieved = alg[dom]["flops"] / (phase_ms[dom] / 1e3) / 1e12

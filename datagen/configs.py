@@ -55,11 +55,12 @@ class LayerConfig:
     rms_eps: float = 1e-6
     x_seed: int | None = None
     top_p: float = 0.0  # K3_TOPP cumulative-weight pruning of the top-K; 0 = off
+    act_mxfp8: int = 0  # 1: MXFP8 activations into the expert contractions (the low-precision variant)
 
     @property
     def dims(self):
         return dict(hidden=self.hidden, latent=self.latent, n_experts=self.n_experts, top_k=self.top_k,
-                    inter=self.inter, rms_eps=self.rms_eps, top_p=self.top_p)
+                    inter=self.inter, rms_eps=self.rms_eps, top_p=self.top_p, act_mxfp8=self.act_mxfp8)
 
     def with_tokens(self, T: int, x_seed: int | None = None) -> "LayerConfig":
         return dataclasses.replace(self, T=T, x_seed=x_seed)

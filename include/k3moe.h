@@ -62,6 +62,13 @@ typedef struct {
                         over its raw scores, and the rest are dropped (id -1, weight 0 in the
                         routing outputs; no expert work).  0 (or >= 1): off.  With pruning on,
                         K + 8 <= 32 is required */
+  int32_t act_mxfp8; /* 0: the expert contractions read the bf16 activations (exact path).
+                        1: the low-precision-activation variant: the tensor-core expert GEMMs
+                        (T >= k3moe_tc_min_tokens) read z and h quantized to MXFP8 (OCP MX
+                        E4M3 elements, one E8M0 scale per 32 consecutive elements along the
+                        contraction) and run block-scaled on the MXFP4 weights as stored;
+                        smaller batches run the exact path.  Lossy by about one E4M3 step
+                        per activation element */
 } k3moe_dims;
 
 typedef enum {

@@ -63,11 +63,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
 class Dims(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("latent", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("inter", ctypes.c_int32), ("rms_eps", ctypes.c_float),
-                ("top_p", ctypes.c_float)]
+                ("top_p", ctypes.c_float), ("act_mxfp8", ctypes.c_int32)]
 
 
-def dims(hidden, latent, n_experts, top_k, inter, rms_eps=1e-6, top_p=0.0) -> Dims:
-    return Dims(hidden, latent, n_experts, top_k, inter, rms_eps, top_p)
+def dims(hidden, latent, n_experts, top_k, inter, rms_eps=1e-6, top_p=0.0, act_mxfp8=0) -> Dims:
+    return Dims(hidden, latent, n_experts, top_k, inter, rms_eps, top_p, int(act_mxfp8))
 
 
 class ExpertsC(ctypes.Structure):

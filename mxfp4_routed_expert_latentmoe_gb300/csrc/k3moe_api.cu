@@ -12,6 +12,7 @@
 #include "k3_route.cuh"
 #include "k3_tc.cuh"
 #include "k3_front.cuh"
+#include "k3_mx8.cuh"
 
 namespace {
 
@@ -99,6 +100,11 @@ k3moe_status check_dims(const k3moe_dims* d) {
   if (!(d->rms_eps >= 0.0f) || d->rms_eps > 1.0f) return K3MOE_ERR_ARG;
   if (!(d->top_p >= 0.0f)) return K3MOE_ERR_ARG;
   if (top_p_on(*d) && d->top_k + REFINE_EXTRA > 32) return K3MOE_ERR_SHAPE;
+  if (d->act_mxfp8 != 0 && d->act_mxfp8 != 1) return K3MOE_ERR_ARG;
+  // the variant's grouped GEMM: 256-row tiles and at least X8_STAGES stages of 128 elements
+  if (d->act_mxfp8 && (d->latent % 256 || d->inter % 256 || d->latent < X8_BK * X8_STAGES ||
+                       d->inter < X8_BK * X8_STAGES))
+    return K3MOE_ERR_SHAPE;
   return K3MOE_OK;
 }
 
@@ -182,6 +188,21 @@ bool map_u8(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint3
   const cuuint32_t box[2] = {128, box_rows};
   const cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// row-major [rows, cols] E2M1 matrix (cols 4-bit elements, packed two per byte, rows
+// cols / 2 bytes apart), boxes of 128 rows x 128 elements; in shared memory each 16
+// elements take a 16-byte granule (8 bytes of codes, 8 of padding), 128-byte swizzle
+bool map_e2m1(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols / 2};
+  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(ptr), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -278,6 +299,19 @@ cudaError_t launch_tc_moe(const uint16_t* act, int slots, TcMoeParams p, int dev
   if (!set_smem<k3_tc_moe_kernel<MODE>>(dev, smem)) return cudaErrorInvalidValue;
   const int grid = sms < TM_MAX_CTAS ? sms : TM_MAX_CTAS;
   return launch(k3_tc_moe_kernel<MODE>, dim3(grid), dim3(TM_THREADS), smem, st, pdl, mb, ma, p);
+}
+
+// grouped expert GEMM of the MXFP8-activation variant; act [slots, K] E4M3 codes in slot order
+template <int MODE>
+cudaError_t launch_mx8_moe(const uint8_t* act, Mx8Params p, int dev, int sms, cudaStream_t st, bool pdl) {
+  CUtensorMap mb, ma;
+  if (!map_u8(&mb, act, (uint64_t)p.slots, (uint64_t)p.K, X8_NB)) return cudaErrorInvalidValue;
+  // template of the weight maps ([R, K] E2M1): the kernel writes each expert tensor's address
+  // into its copies; the (256-byte aligned) workspace stands in until then
+  if (!map_e2m1(&ma, p.tmaps, (uint64_t)p.R, (uint64_t)p.K)) return cudaErrorInvalidValue;
+  if (!set_smem<k3_mx8_moe_kernel<MODE>>(dev, X8_SMEM)) return cudaErrorInvalidValue;
+  const int grid = sms < TM_MAX_CTAS ? sms : TM_MAX_CTAS;
+  return launch(k3_mx8_moe_kernel<MODE>, dim3(grid), dim3(X8_THREADS), X8_SMEM, st, pdl, mb, ma, p);
 }
 
 // D[M, N0 (+N1)] = A[M, K] . [B0; B1]^T on tcgen05 (A, B bf16 row-major)
@@ -627,24 +661,48 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
     }
     K3_TRY(mark(events, n_events, 1, s));
     if (tc) {
-      // top-k, permutation, then the bf16 activation rows in expert-sorted slot order for
-      // the grouped GEMM (the f16 copy of z that the weight-streaming kernels read is not needed)
+      // top-k, permutation, then the activation rows in expert-sorted slot order for the
+      // grouped GEMM (the f16 copy of z that the weight-streaming kernels read is not needed)
       K3_TRY(launch_topk(tp, dev, s, pdl));
       K3_TRY(launch_permute(pp, dev, s, pdl));
-      const int per = d.latent / 8;
-      const int gblocks = (int)(((size_t)slots * per + 255) / 256 < (size_t)sms * 8 ? ((size_t)slots * per + 255) / 256
-                                                                                       : (size_t)sms * 8);
-      K3_TRY(launch(k3_gather_rows_kernel, dim3(gblocks), dim3(256), 0, s, pdl, (const uint16_t*)at<uint16_t>(ws, L.z),
-                    (const int32_t*)at<int32_t>(ws, L.slot_tok),
-                    (const int32_t*)(at<int32_t>(ws, L.offsets) + d.n_experts), slots, (int)d.latent,
-                    at<uint16_t>(ws, L.act)));
+      if (d.act_mxfp8) {
+        // z quantized to MXFP8 rows in slot order (codes, then the scale bytes)
+        uint8_t* a8 = at<uint8_t>(ws, L.act);
+        const size_t groups = (size_t)slots * (d.latent / 32);
+        const int gblocks = (int)((groups + 255) / 256 < (size_t)sms * 8 ? (groups + 255) / 256 : (size_t)sms * 8);
+        K3_TRY(launch(k3_gather_mx8_kernel, dim3(gblocks), dim3(256), 0, s, pdl, (const uint16_t*)at<uint16_t>(ws, L.z),
+                      (const int32_t*)at<int32_t>(ws, L.slot_tok),
+                      (const int32_t*)(at<int32_t>(ws, L.offsets) + d.n_experts), slots, (int)d.latent, a8,
+                      a8 + (size_t)slots * d.latent));
+      } else {
+        // bf16 rows in slot order (interleaved K order)
+        const int per = d.latent / 8;
+        const size_t items = (size_t)slots * per;
+        const int gblocks = (int)((items + 255) / 256 < (size_t)sms * 8 ? (items + 255) / 256 : (size_t)sms * 8);
+        K3_TRY(launch(k3_gather_rows_kernel, dim3(gblocks), dim3(256), 0, s, pdl,
+                      (const uint16_t*)at<uint16_t>(ws, L.z), (const int32_t*)at<int32_t>(ws, L.slot_tok),
+                      (const int32_t*)(at<int32_t>(ws, L.offsets) + d.n_experts), slots, (int)d.latent,
+                      at<uint16_t>(ws, L.act)));
+      }
     } else {
       K3_TRY(launch_route_tail(tp, pp, zp, dev, s, pdl));
     }
   }
   K3_TRY(mark(events, n_events, 2, s));
   // experts
-  if (tc) {
+  if (tc && d.act_mxfp8) {
+    // MXFP8 activations, block-scaled MMAs on the stored MXFP4 weights; h leaves the gate/up
+    // epilogue as MXFP8 rows in slot order (codes, then the scale bytes)
+    const uint8_t* a8 = at<uint8_t>(ws, L.act);
+    uint8_t* h8 = at<uint8_t>(ws, L.h16);
+    Mx8Params gp{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.inter, d.latent,
+                 a8 + (size_t)slots * d.latent, slots, h8, h8 + (size_t)slots * d.inter, status, at<void>(ws, L.tmaps)};
+    K3_TRY(launch_mx8_moe<0>(a8, gp, dev, sms, s, pdl));
+    K3_TRY(mark(events, n_events, 3, s));
+    Mx8Params dp2{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.latent, d.inter,
+                  h8 + (size_t)slots * d.inter, slots, at<void>(ws, L.o), nullptr, status, at<void>(ws, L.tmaps)};
+    K3_TRY(launch_mx8_moe<1>(h8, dp2, dev, sms, s, pdl));
+  } else if (tc) {
     TcMoeParams gp{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.inter, d.latent,
                    at<void>(ws, L.h16), status, at<void>(ws, L.tmaps)};
     K3_TRY(launch_tc_moe<0>(at<uint16_t>(ws, L.act), slots, gp, dev, sms, s, pdl));
@@ -794,6 +852,10 @@ void* k3moe_workspace_view(const k3moe_dims* dims, int32_t T, void* ws, int32_t 
     case 3: return at<void>(ws, L.logits);
     case 4: return at<void>(ws, L.h16);
     case 5: return at<void>(ws, L.o);
+    case 6: return dims->act_mxfp8 ? at<void>(ws, L.act) : nullptr;
+    case 7: return dims->act_mxfp8 ? at<uint8_t>(ws, L.act) + (size_t)T * dims->top_k * dims->latent : nullptr;
+    case 8: return dims->act_mxfp8 ? at<void>(ws, L.h16) : nullptr;
+    case 9: return dims->act_mxfp8 ? at<uint8_t>(ws, L.h16) + (size_t)T * dims->top_k * dims->inter : nullptr;
     default: return nullptr;
   }
 }
@@ -917,6 +979,6 @@ const char* k3moe_status_str(k3moe_status st) {
   return "unknown status";
 }
 
-int32_t k3moe_abi_version(void) { return 2; }
+int32_t k3moe_abi_version(void) { return 3; }
 
 }  // extern "C"

@@ -26,11 +26,11 @@ EXPERT_TENSORS = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
 class Dims(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int), ("latent", ctypes.c_int), ("n_experts", ctypes.c_int),
                 ("top_k", ctypes.c_int), ("inter", ctypes.c_int), ("rms_eps", ctypes.c_double),
-                ("top_p", ctypes.c_double)]
+                ("top_p", ctypes.c_double), ("act_mxfp8", ctypes.c_int)]
 
 
-def dims(hidden, latent, n_experts, top_k, inter, rms_eps=1e-6, top_p=0.0) -> Dims:
-    return Dims(hidden, latent, n_experts, top_k, inter, rms_eps, top_p)
+def dims(hidden, latent, n_experts, top_k, inter, rms_eps=1e-6, top_p=0.0, act_mxfp8=0) -> Dims:
+    return Dims(hidden, latent, n_experts, top_k, inter, rms_eps, top_p, int(act_mxfp8))
 
 
 def build(force: bool = False) -> str:
@@ -62,6 +62,10 @@ def _L():
             sig = {
                 "k3o_e2m1": ([ctypes.c_uint], d),
                 "k3o_ue8m0": ([ctypes.c_uint], d),
+                "k3o_e4m3": ([ctypes.c_uint], d),
+                "k3o_e4m3_encode": ([d], ctypes.c_uint),
+                "k3o_mxfp8_quant": ([i64, p, p, p], None),
+                "k3o_mxfp8_round": ([i64, p, p], None),
                 "k3o_round_bf16": ([d], d),
                 "k3o_situ": ([d, d], d),
                 "k3o_dequant": ([p, p, i, i, p], None),
@@ -105,6 +109,34 @@ def e2m1(code: int) -> float:
 
 def ue8m0(s: int) -> float:
     return _L().k3o_ue8m0(s)
+
+
+def e4m3(code: int) -> float:
+    return _L().k3o_e4m3(code)
+
+
+def e4m3_encode(v: float) -> int:
+    return int(_L().k3o_e4m3_encode(float(v)))
+
+
+def mxfp8_quant(x):
+    """x [..., n] (n a multiple of 32, groups along the last axis) -> (E4M3 codes uint8
+    [..., n], scale bytes uint8 [..., n/32])."""
+    x, px = _c(x, np.float64)
+    assert x.shape[-1] % 32 == 0
+    codes = np.empty(x.shape, dtype=np.uint8)
+    scales = np.empty(x.shape[:-1] + (x.shape[-1] // 32,), dtype=np.uint8)
+    _L().k3o_mxfp8_quant(x.size, px, codes.ctypes.data, scales.ctypes.data)
+    return codes, scales
+
+
+def mxfp8_round(x) -> np.ndarray:
+    """The values of x's MXFP8 quantization (groups of 32 along the last axis)."""
+    x, px = _c(x, np.float64)
+    assert x.shape[-1] % 32 == 0
+    out = np.empty_like(x)
+    _L().k3o_mxfp8_round(x.size, px, out.ctypes.data)
+    return out
 
 
 def round_bf16(a) -> np.ndarray:

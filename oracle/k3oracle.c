@@ -34,6 +34,14 @@
  *  - The combine sums the K weighted expert outputs in that order.
  *  - Gate rows first, then up rows, when gate/up are viewed as one [2I, L] matrix.
  *  - No routed scaling factor; no grouped routing.
+ *  - The low-precision-activation variant (act_mxfp8) reads the pages' per-32-group
+ *    quantized activations [P1 "What's in the commits" item 7; P2 quant.h commit:
+ *    matmul_mxfp4_i8] as OCP MX v1.0 MXFP8: E4M3 elements (bias 7, S.1111.111 NaN, max
+ *    448) sharing one E8M0 scale per 32 consecutive elements along the contraction.  The
+ *    shared exponent is floor(log2(max |x|)) - 8 (8 = the largest E4M3 exponent), the
+ *    elements are x / 2^X rounded to nearest even and saturated to +-448; an all-zero
+ *    group takes scale byte 0.  z (after R1) and h (after R2) are quantized before the
+ *    expert contractions that read them; nothing else changes.
  */
 #include <math.h>
 #include <stdint.h>
@@ -44,6 +52,7 @@ typedef struct {
   int hidden, latent, n_experts, top_k, inter;
   double rms_eps;
   double top_p; /* K3_TOPP: 0 < p < 1 prunes the top-K to cumulative weight p; else off */
+  int act_mxfp8; /* 1: the experts read MXFP8 (E4M3, 32-element groups) activations */
 } k3o_dims;
 
 /* ----------------------------------------------------------------------------------------
@@ -73,6 +82,73 @@ static double k3o_mx_elem(const uint8_t* q, const uint8_t* s, int I, int o, int 
 void k3o_dequant(const uint8_t* q, const uint8_t* s, int O, int I, double* out) {
   for (int o = 0; o < O; ++o)
     for (int c = 0; c < I; ++c) out[(size_t)o * I + c] = k3o_mx_elem(q, s, I, o, c);
+}
+
+/* ----------------------------------------------------------------------------------------
+ * MXFP8 activations [P1 "What's in the commits" item 7 and P2 quant.h commit (per-32-group
+ * quantized activations, the variant's idea); OCP MX v1.0 E4M3 element and E8M0 scale]
+ * -------------------------------------------------------------------------------------- */
+/* value of an E4M3 code: bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0 mantissa;
+ * exponent 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN (no infinities) */
+double k3o_e4m3(unsigned code) {
+  const unsigned e = (code >> 3) & 15u, m = code & 7u;
+  if (e == 15u && m == 7u) return NAN;
+  const double mag = e ? ldexp(1.0 + m / 8.0, (int)e - 7) : ldexp(m / 8.0, -6);
+  return (code & 0x80u) ? -mag : mag;
+}
+
+/* nearest E4M3 code to v (ties to the even code, i.e. even mantissa), saturating at
+ * +-448; the sign bit follows v's sign (a negative value that rounds to zero is -0).
+ * The non-negative finite codes 0..126 are increasing in value: binary search for the
+ * largest code not above |v|, then compare with its successor. */
+unsigned k3o_e4m3_encode(double v) {
+  const unsigned sign = signbit(v) ? 0x80u : 0u;
+  const double a = fabs(v);
+  if (a >= 448.0) return sign | 126u;
+  unsigned lo = 0, hi = 126;
+  while (lo < hi) { /* invariant: value(lo) <= a */
+    const unsigned mid = (lo + hi + 1) / 2;
+    if (k3o_e4m3((int)mid) <= a) lo = mid;
+    else hi = mid - 1;
+  }
+  if (k3o_e4m3(lo) == a) return sign | lo;
+  const unsigned up = lo + 1;
+  const double dl = a - k3o_e4m3(lo), du = k3o_e4m3(up) - a;
+  const unsigned c = (dl < du) ? lo : (du < dl) ? up : ((lo & 1u) ? up : lo);
+  return sign | c;
+}
+
+/* scale byte of one group from its largest magnitude: 127 + floor(log2(amax)) - 8,
+ * clamped to [0, 254]; 0 for an all-zero group */
+static unsigned k3o_mxfp8_scale(double amax) {
+  if (amax == 0.0) return 0u;
+  int ex = 0;
+  frexp(amax, &ex); /* amax = f 2^ex, f in [0.5, 1): floor(log2(amax)) = ex - 1 */
+  int s = 127 + (ex - 1) - 8;
+  if (s < 0) s = 0;
+  if (s > 254) s = 254;
+  return (unsigned)s;
+}
+
+/* x [n] (n a multiple of 32) -> E4M3 codes [n] and scale bytes [n/32] */
+void k3o_mxfp8_quant(int64_t n, const double* x, uint8_t* codes, uint8_t* scales) {
+  for (int64_t g = 0; g < n / 32; ++g) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i) amax = fmax(amax, fabs(x[g * 32 + i]));
+    const unsigned s = k3o_mxfp8_scale(amax);
+    scales[g] = (uint8_t)s;
+    for (int i = 0; i < 32; ++i) codes[g * 32 + i] = (uint8_t)k3o_e4m3_encode(ldexp(x[g * 32 + i], 127 - (int)s));
+  }
+}
+
+/* x -> the values of its MXFP8 quantization (code value times 2^(s-127)) */
+void k3o_mxfp8_round(int64_t n, const double* x, double* out) {
+  uint8_t* c = (uint8_t*)malloc((size_t)(n > 0 ? n : 1));
+  uint8_t* s = (uint8_t*)malloc((size_t)(n / 32 > 0 ? n / 32 : 1));
+  k3o_mxfp8_quant(n, x, c, s);
+  for (int64_t i = 0; i < n; ++i) out[i] = ldexp(k3o_e4m3(c[i]), (int)s[i / 32] - 127);
+  free(c);
+  free(s);
 }
 
 /* ----------------------------------------------------------------------------------------
@@ -287,6 +363,12 @@ void k3o_expert(const k3o_dims* d, const double* z, const uint8_t* gq, const uin
                 const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int spec, double* h_out, double* o) {
   const int L = d->latent, I = d->inter;
   double* h = (double*)malloc(sizeof(double) * (size_t)I);
+  double* zq = NULL;
+  if (d->act_mxfp8) { /* the variant's gate/up input: z quantized to MXFP8 */
+    zq = (double*)malloc(sizeof(double) * (size_t)L);
+    k3o_mxfp8_round(L, z, zq);
+    z = zq;
+  }
   for (int j = 0; j < I; ++j) {
     double g = 0.0, u = 0.0;
     for (int c = 0; c < L; ++c) g += k3o_mx_elem(gq, gs, L, j, c) * z[c];
@@ -294,6 +376,8 @@ void k3o_expert(const k3o_dims* d, const double* z, const uint8_t* gq, const uin
     double v = k3o_situ(g, u);
     h[j] = spec ? k3o_round_bf16(v) : v;
   }
+  if (d->act_mxfp8) k3o_mxfp8_round(I, h, h); /* the down input: h quantized to MXFP8 */
+  free(zq);
   for (int c = 0; c < L; ++c) {
     double acc = 0.0;
     for (int j = 0; j < I; ++j) acc += k3o_mx_elem(dq, ds, I, c, j) * h[j];
@@ -310,8 +394,13 @@ static void k3o_expert_dense(const k3o_dims* d, int n, const double* const* zs, 
                              const double* Wdn, int spec, double* const* os) {
   const int L = d->latent, I = d->inter;
   double* h = (double*)malloc(sizeof(double) * (size_t)I);
+  double* zq = (double*)malloc(sizeof(double) * (size_t)L);
   for (int i = 0; i < n; ++i) {
     const double* z = zs[i];
+    if (d->act_mxfp8) {
+      k3o_mxfp8_round(L, z, zq);
+      z = zq;
+    }
     for (int j = 0; j < I; ++j) {
       double g = 0.0, u = 0.0;
       const double* rg = Wg + (size_t)j * L;
@@ -321,6 +410,7 @@ static void k3o_expert_dense(const k3o_dims* d, int n, const double* const* zs, 
       double v = k3o_situ(g, u);
       h[j] = spec ? k3o_round_bf16(v) : v;
     }
+    if (d->act_mxfp8) k3o_mxfp8_round(I, h, h);
     for (int c = 0; c < L; ++c) {
       double acc = 0.0;
       const double* rd = Wdn + (size_t)c * I;
@@ -329,6 +419,7 @@ static void k3o_expert_dense(const k3o_dims* d, int n, const double* const* zs, 
     }
   }
   free(h);
+  free(zq);
 }
 
 /* ----------------------------------------------------------------------------------------
@@ -443,4 +534,4 @@ void k3o_situ_array(int64_t n, const double* g, const double* u, double* out) {
   for (int64_t i = 0; i < n; ++i) out[i] = k3o_situ(g[i], u[i]);
 }
 
-int k3o_abi_version(void) { return 2; }
+int k3o_abi_version(void) { return 3; }

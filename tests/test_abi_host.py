@@ -16,7 +16,7 @@ def test_library_exports_every_declared_function():
     L = k3.lib()
     missing = [n for n in names if not hasattr(L, n)]
     assert not missing, missing
-    assert L.k3moe_abi_version() == 2
+    assert L.k3moe_abi_version() == 3
     for code, text in k3.STATUS.items():
         assert L.k3moe_status_str(code).decode() == text
 

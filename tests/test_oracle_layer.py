@@ -285,8 +285,9 @@ def _np_top_p(s_sel, w, p):
     return kept
 
 
-def _np_block(cfg, x, W, experts, spec, top_p=0.0):
-    """Brute-force numpy re-implementation of the block from the pages' definitions."""
+def _np_block(cfg, x, W, experts, spec, top_p=0.0, mx=None):
+    """Brute-force numpy re-implementation of the block from the pages' definitions;
+    mx (optional) rounds the experts' activations (z before gate/up, h before down)."""
     E, K, L = cfg.n_experts, cfg.top_k, cfg.latent
     xf = datagen.bf16_to_f64(x)
     lg = xf @ datagen.bf16_to_f64(W["wr"]).T
@@ -305,9 +306,11 @@ def _np_block(cfg, x, W, experts, spec, top_p=0.0):
         y = np.zeros(L)
         for k, e in enumerate(ids):
             ex = experts[int(e)]
-            g = np_dequant(ex["gate_q"], ex["gate_s"]) @ z[t]
-            u = np_dequant(ex["up_q"], ex["up_s"]) @ z[t]
+            ze = mx(z[t]) if mx else z[t]
+            g = np_dequant(ex["gate_q"], ex["gate_s"]) @ ze
+            u = np_dequant(ex["up_q"], ex["up_s"]) @ ze
             h = rnd(4 * np.tanh(g / 4) / (1 + np.exp(-g)) * 25 * np.tanh(u / 25))
+            h = mx(h) if mx else h
             y += w[k] * (np_dequant(ex["down_q"], ex["down_s"]) @ h)
         yh = rnd(W["gamma"].astype(np.float64) * y / np.sqrt(np.mean(y * y) + cfg.rms_eps))
         out.append(yh @ datagen.bf16_to_f64(W["wu"]).T)
