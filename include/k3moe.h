@@ -132,7 +132,7 @@ k3moe_status k3moe_route(const k3moe_dims* dims, int32_t T, const uint16_t* x, c
                          const float* bias, int32_t* ids, float* w, void* ws, size_t ws_bytes, void* stream);
 
 /* The whole block for T tokens (the chunk's expert union is built once; each
- * selected expert's weights are streamed once per call).  From 256 tokens on (see
+ * selected expert's weights are streamed once per call).  From 9 tokens on (see
  * k3moe_set_tc_min_tokens) the projections and experts run on tensor-core GEMMs.
  *   x      [T, H] bf16;  wr [E, H] bf16;  bias [E] f32
  *   w_down [L, H] bf16   latent down;  w_up [H, L] bf16 latent up
@@ -172,7 +172,8 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
  *  - Scratch lives in one fixed array of K3MOE_NOALLOC_SCRATCH_BYTES (4 MiB) in device
  *    memory that every GPU which loads the library holds until the process exits.  A
  *    call fits when k3moe_workspace_bytes(dims, T) is at most that size: at K3 shapes
- *    (H 7168, L 3584, E 896, K 16, I 3072) that is up to 11 tokens per call.  A call
+ *    (H 7168, L 3584, E 896, K 16, I 3072) that is up to 8 tokens per call (the
+ *    weight-streaming regime below k3moe_tc_min_tokens).  A call
  *    that needs more returns K3MOE_ERR_WORKSPACE and launches nothing.
  *  - The first call on a device looks up the array's device address with
  *    cudaGetSymbolAddress (with that device current); make that first call before
@@ -219,8 +220,9 @@ k3moe_status k3moe_permute(const k3moe_dims* dims, int32_t T, const int32_t* ids
 k3moe_status k3moe_device_status(const void* ws, uint32_t* host_out, void* stream);
 
 /* Token count from which k3moe_forward (and k3moe_route) run the projections and the
- * experts on the tensor-core GEMMs instead of the weight-streaming GEMVs (default 256, the
- * crossover measured on GB300 at K3 shapes).  Process-wide: it changes the workspace size
+ * experts on the tensor-core GEMMs instead of the weight-streaming GEMVs (default 9, the
+ * crossover measured on GB300 at K3 shapes: 8 random tokens 523 us on the GEMVs against
+ * 712 us, 9 tokens 836 us against 786 us).  Process-wide: it changes the workspace size
  * and the launch sequence of every later call, so set it before sizing workspaces and with
  * no call in flight.  Returns the previous value, or -1 for t < 1 (nothing changed).  A
  * tuning control for measuring the crossover; the pages have no counterpart. */

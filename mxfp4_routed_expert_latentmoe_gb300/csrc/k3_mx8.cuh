@@ -430,9 +430,8 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
           for (int jj = 0; jj < 16; ++jj) {
             const int col = c * 16 + jj;  // warp-uniform
             const float h = bf16_bits_to_f32(f32_to_bf16_bits(situ_fast(__uint_as_float(r0[jj]), __uint_as_float(r1[jj]))));
-            float m = fabsf(h);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            // largest |h| of the group: the bit patterns of non-negative floats order as integers
+            const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
             const uint32_t sb = mx8_scale_byte(m);
             const uint32_t code = e4m3_code(h * mx8_inv_scale(sb));
             if (col < n) {

@@ -20,7 +20,7 @@ using namespace k3;
 
 constexpr float kTieTau = 3e-5f;
 constexpr int kMaxDevices = 64;
-constexpr int kTcMinTokensDefault = 256;  // measured crossover (bench.py --sweep)
+constexpr int kTcMinTokensDefault = 9;  // measured crossover on GB300 at K3 shapes (bench.py --sweep)
 
 size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 int tc_min_t();

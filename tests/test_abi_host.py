@@ -40,18 +40,20 @@ def test_workspace_bytes_is_monotone_and_rejects_bad_dims():
     assert L.k3moe_workspace_bytes(ctypes.byref(d), -1) == 0
 
 
-def test_workspace_holds_the_tensor_core_path_buffers_from_256_tokens():
-    # from 256 tokens the grouped expert GEMM needs the slot-ordered bf16 activations and
-    # the weight tensor maps (256 CTAs x 2 blocks x 2 x 128 bytes); below that the
-    # workspace grows by the per-token buffers only
+def test_workspace_holds_the_tensor_core_path_buffers_from_the_threshold():
+    # from k3moe_tc_min_tokens tokens the grouped expert GEMM needs the slot-ordered bf16
+    # activations and the weight tensor maps (256 CTAs x 2 blocks x 2 x 128 bytes); below
+    # that the workspace grows by the per-token buffers only
     L = k3.lib()
     d = _d()
-    ws = {T: L.k3moe_workspace_bytes(ctypes.byref(d), T) for T in (254, 255, 256)}
-    per_token = ws[255] - ws[254]
-    slots = 256 * 16
+    t0 = k3.tc_min_tokens()
+    assert t0 == 9  # the measured GEMV / tensor-core crossover
+    ws = {T: L.k3moe_workspace_bytes(ctypes.byref(d), T) for T in (t0 - 2, t0 - 1, t0)}
+    per_token = ws[t0 - 1] - ws[t0 - 2]
+    slots = t0 * 16
     tc_bytes = slots * 3584 * 2 + 256 * 2 * 2 * 128
-    assert ws[256] - ws[255] >= tc_bytes
-    assert ws[256] - ws[255] <= tc_bytes + 2 * per_token + 3 * 256
+    assert ws[t0] - ws[t0 - 1] >= tc_bytes
+    assert ws[t0] - ws[t0 - 1] <= tc_bytes + 2 * per_token + 3 * 256
 
 
 def test_device_status_bits_match_the_header():
@@ -119,8 +121,8 @@ def test_dequant_validates_shape():
 
 def test_noalloc_scratch_limit_is_the_workspace_size_rule():
     """k3moe_forward_noalloc refuses, before touching a device, any call whose workspace
-    (k3moe_workspace_bytes) exceeds its fixed scratch array: at K3 shapes 11 tokens fit
-    and 12 do not."""
+    (k3moe_workspace_bytes) exceeds its fixed scratch array: at K3 shapes 8 tokens fit
+    and 9 (the first tensor-core batch) do not."""
     import re
     L = k3.lib()
     d = _d()
@@ -128,16 +130,16 @@ def test_noalloc_scratch_limit_is_the_workspace_size_rule():
     m = re.search(r"#define K3MOE_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
     assert m and (int(m.group(1)) << int(m.group(2))) == k3.NOALLOC_SCRATCH_BYTES
     cap = k3.NOALLOC_SCRATCH_BYTES
-    assert L.k3moe_workspace_bytes(ctypes.byref(d), 11) <= cap < L.k3moe_workspace_bytes(ctypes.byref(d), 12)
+    assert L.k3moe_workspace_bytes(ctypes.byref(d), 8) <= cap < L.k3moe_workspace_bytes(ctypes.byref(d), 9)
     v = ctypes.c_void_p(16)
     ex = k3.ExpertsC(16, 16, 16, 16, 16, 16)
-    assert L.k3moe_forward_noalloc(ctypes.byref(d), 12, v, v, v, v, v, v, ctypes.byref(ex), v, None, None,
+    assert L.k3moe_forward_noalloc(ctypes.byref(d), 9, v, v, v, v, v, v, ctypes.byref(ex), v, None, None,
                                    None) == ERR_WS
     assert L.k3moe_forward_noalloc(ctypes.byref(d), 0, v, v, v, v, v, v, ctypes.byref(ex), v, None, None,
                                    None) == 0
     import torch
     if not torch.cuda.is_available():  # a call that fits reaches the device check
-        assert L.k3moe_forward_noalloc(ctypes.byref(d), 11, v, v, v, v, v, v, ctypes.byref(ex), v, None, None,
+        assert L.k3moe_forward_noalloc(ctypes.byref(d), 8, v, v, v, v, v, v, ctypes.byref(ex), v, None, None,
                                        None) == ERR_DEVICE
         st = ctypes.c_uint32(0)
         assert L.k3moe_device_status(None, ctypes.byref(st), None) == ERR_DEVICE
@@ -150,13 +152,13 @@ def test_tensor_core_threshold_moves_the_workspace_step():
     d = _d()
     prev = k3.set_tc_min_tokens(64)
     try:
-        assert prev == 256
+        assert prev == 9
         step = lambda T: L.k3moe_workspace_bytes(ctypes.byref(d), T) - L.k3moe_workspace_bytes(ctypes.byref(d), T - 1)
         tc_bytes = 64 * 16 * 3584 * 2
-        assert step(64) >= tc_bytes and step(63) < tc_bytes and step(256) < tc_bytes
+        assert step(64) >= tc_bytes and step(63) < tc_bytes and step(9) < tc_bytes
         with pytest.raises(ValueError):
             k3.set_tc_min_tokens(0)
         assert k3.set_tc_min_tokens(64) == 64
     finally:
         k3.set_tc_min_tokens(prev)
-    assert L.k3moe_set_tc_min_tokens(256) == 256
+    assert L.k3moe_set_tc_min_tokens(9) == 9
