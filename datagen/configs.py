@@ -29,6 +29,7 @@ from . import bf16_bits, f32, int_u8, normal_f64, u8, uniform_f64
 
 # stream ids (mirror k3gen.h)
 S_X, S_WR, S_BIAS, S_WD, S_WU, S_XBASE, S_XNOISE, S_EXPERT0 = 1, 2, 3, 4, 5, 6, 7, 0x1000
+S_SGU, S_SDN = 8, 9
 EXPERT_TENSORS = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
 
 
@@ -140,6 +141,22 @@ def layer_weights(cfg: LayerConfig) -> dict:
     else:
         out["bias"] = np.zeros(E, dtype=np.float32)
     return out
+
+
+# Shared experts beside the routed block: two SiTU-GLU experts on the hidden width, fused
+# along the intermediate dimension.  The pages give no width; each is read as wide as a
+# routed expert (I = 3072), so the fused width is 2 x 3072.
+SHARED_INTER = 6144
+
+
+def shared_weights(cfg: LayerConfig, inter_s: int = SHARED_INTER) -> dict:
+    """Fused shared-expert weights as bf16 bits: wgu [2 Is, H] (gate rows, then up rows) and
+    wdn [H, Is]."""
+    H, s = cfg.hidden, cfg.seed
+    return {
+        "wgu": bf16_bits(normal_f64(s, S_SGU, 2 * inter_s * H, 1.0 / math.sqrt(H))).reshape(2 * inter_s, H),
+        "wdn": bf16_bits(normal_f64(s, S_SDN, H * inter_s, 1.0 / math.sqrt(inter_s))).reshape(H, inter_s),
+    }
 
 
 def expert_tensors(cfg, e: int) -> dict:

@@ -70,6 +70,8 @@ enum {
   K3GEN_S_WU = 5,     /* latent up [H, L] */
   K3GEN_S_XBASE = 6,  /* base vectors of the temporal-locality chunk */
   K3GEN_S_XNOISE = 7, /* per-token perturbations of the temporal-locality chunk */
+  K3GEN_S_SGU = 8,    /* shared experts: fused gate and up rows [2 Is, H] */
+  K3GEN_S_SDN = 9,    /* shared experts: fused down matrix [H, Is] */
   K3GEN_S_EXPERT0 = 0x1000
 };
 /* which: 0 gate packed, 1 gate scales, 2 up packed, 3 up scales, 4 down packed, 5 down scales */

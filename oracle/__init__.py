@@ -77,6 +77,7 @@ def _L():
                 "k3o_latent_up": ([D, i, p, p, p], None),
                 "k3o_expert": ([D, p, p, p, p, p, p, p, i, p, p], None),
                 "k3o_forward": ([D, i, p, p, p, p, p, p, p, i, i, p, p, p, p, p, p], i),
+                "k3o_shared": ([D, i, i, p, p, p, i, p, p], None),
                 "k3o_round_bf16_array": ([i64, p, p], None),
                 "k3o_situ_array": ([i64, p, p, p], None),
                 "k3o_abi_version": ([], i),
@@ -239,6 +240,21 @@ def expert(d: Dims, z: np.ndarray, tensors: dict, spec: bool):
     o = np.empty(d.latent, dtype=np.float64)
     _L().k3o_expert(ctypes.byref(d), pz, *[k.ctypes.data for k in keep], int(spec), h.ctypes.data, o.ctypes.data)
     return h, o
+
+
+def shared(d: Dims, x_bits, wgu_bits, wdn_bits, spec: bool = True):
+    """Fused shared experts on x [T, H] (bf16 bits): wgu [2 Is, H] (gate rows, then up rows),
+    wdn [H, Is] -> (h [T, Is], out [T, H]) fp64."""
+    T = x_bits.shape[0]
+    Is = wdn_bits.shape[1]
+    assert wgu_bits.shape == (2 * Is, d.hidden) and wdn_bits.shape == (d.hidden, Is)
+    x, px = _c(x_bits, np.uint16)
+    wgu, pg = _c(wgu_bits, np.uint16)
+    wdn, pd = _c(wdn_bits, np.uint16)
+    h = np.empty((T, Is), dtype=np.float64)
+    out = np.empty((T, d.hidden), dtype=np.float64)
+    _L().k3o_shared(ctypes.byref(d), T, Is, px, pg, pd, int(spec), h.ctypes.data, out.ctypes.data)
+    return h, out
 
 
 def forward(d: Dims, x_bits, wr_bits, bias, wd_bits, wu_bits, gamma, experts: dict, spec: bool = True,

@@ -423,6 +423,39 @@ static void k3o_expert_dense(const k3o_dims* d, int n, const double* const* zs, 
 }
 
 /* ----------------------------------------------------------------------------------------
+ * shared experts beside the routed block [P1 architecture bullets, P2 engine commit "2
+ * fused shared experts"]: SiTU-GLU experts on the hidden width whose weights are fused
+ * along the intermediate dimension (gate rows 0..Is-1 and up rows Is..2Is-1 of wgu [2Is,
+ * H]; wdn [H, Is]), so the fused expert computes the sum of the separate ones:
+ *   g_j = sum_c wgu[j][c] x_c,  u_j = sum_c wgu[Is + j][c] x_c,  h_j = SiTU(g_j, u_j)
+ *   (bf16-rounded in spec mode, as the routed h),  out_c = sum_j wdn[c][j] h_j.
+ * The block's output adds it to the routed output. h_out (nullable) [T, Is], out [T, H].
+ * -------------------------------------------------------------------------------------- */
+void k3o_shared(const k3o_dims* d, int T, int Is, const uint16_t* x, const uint16_t* wgu, const uint16_t* wdn,
+                int spec, double* h_out, double* out) {
+  const int H = d->hidden;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    double* h = (double*)malloc(sizeof(double) * (size_t)Is);
+    const uint16_t* xt = x + (size_t)t * H;
+    for (int j = 0; j < Is; ++j) {
+      double g = 0.0, u = 0.0;
+      for (int c = 0; c < H; ++c) g += k3o_from_bf16(wgu[(size_t)j * H + c]) * k3o_from_bf16(xt[c]);
+      for (int c = 0; c < H; ++c) u += k3o_from_bf16(wgu[(size_t)(Is + j) * H + c]) * k3o_from_bf16(xt[c]);
+      const double v = k3o_situ(g, u);
+      h[j] = spec ? k3o_round_bf16(v) : v;
+    }
+    for (int c = 0; c < H; ++c) {
+      double acc = 0.0;
+      for (int j = 0; j < Is; ++j) acc += k3o_from_bf16(wdn[(size_t)c * Is + j]) * h[j];
+      out[(size_t)t * H + c] = acc;
+    }
+    if (h_out) memcpy(h_out + (size_t)t * Is, h, sizeof(double) * (size_t)Is);
+    free(h);
+  }
+}
+
+/* ----------------------------------------------------------------------------------------
  * whole block.  Expert e's tensors are ex[0..5][e] = gate_q, gate_s, up_q, up_s,
  * down_q, down_s; entries of experts that no token routes to may be NULL.
  * chunk = 0: token at a time (each expert decoded where it is used);
