@@ -38,8 +38,8 @@ if ROOT not in sys.path:
 
 METRIC = "K3-shape MXFP4 LatentMoE layer: decode µs/token (HBM GB/s), prefill tokens/s"
 FLUSH_BYTES = 256 << 20
-WORKLOADS = ("decode", "chunk", "prefill", "decode_top_p", "prefill_mxfp8")
-DEFAULT_WORKLOADS = ("decode", "chunk", "prefill", "decode_top_p", "prefill_mxfp8")
+WORKLOADS = ("decode", "chunk", "prefill", "decode_top_p", "prefill_mxfp8", "shared_decode", "shared_prefill")
+DEFAULT_WORKLOADS = WORKLOADS
 TOP_P = 0.7  # the pages' opt-in K3_TOPP setting
 
 
@@ -78,6 +78,10 @@ def workload_cfg(name):
         return dataclasses.replace(C.DECODE, name="decode_top_p", top_p=TOP_P)
     if name == "prefill_mxfp8":  # prefill with the low-precision-activation variant
         return dataclasses.replace(C.PREFILL, name="prefill_mxfp8", act_mxfp8=1)
+    if name == "shared_decode":  # the fused shared experts beside the routed block, one token
+        return dataclasses.replace(C.DECODE, name="shared_decode")
+    if name == "shared_prefill":
+        return dataclasses.replace(C.PREFILL, name="shared_prefill")
     return {"decode": C.DECODE, "chunk": C.CHUNK, "prefill": C.PREFILL}[name]
 
 
@@ -120,6 +124,11 @@ def uses_grouped_gemm(cfg, tc_min_tokens: int) -> bool:
 
 
 def describe(cfg) -> str:
+    if is_shared(cfg):
+        from datagen import configs as C
+        return (f"{cfg.name}: the 2 fused shared experts beside the routed block (SiTU-GLU on the hidden width), "
+                f"T={cfg.T}, H={cfg.hidden}, fused width {C.SHARED_INTER}, bf16 weights, accumulated into the "
+                f"block output")
     tp = f", top-p {cfg.top_p} (K3_TOPP)" if 0.0 < cfg.top_p < 1.0 else ""
     return (f"{cfg.name}: K3-shape routed layer, T={cfg.T}, H={cfg.hidden}, L={cfg.latent}, E={cfg.n_experts}, "
             f"K={cfg.top_k}{tp}, I={cfg.inter}, MXFP4 experts (scale bytes {cfg.scale_lo}..{cfg.scale_hi}), "
@@ -127,7 +136,11 @@ def describe(cfg) -> str:
 
 
 def is_prefill(cfg) -> bool:
-    return cfg.name.startswith("prefill")
+    return cfg.name.startswith("prefill") or cfg.name == "shared_prefill"
+
+
+def is_shared(cfg) -> bool:
+    return cfg.name.startswith("shared_")
 
 
 def unit_of(cfg):
@@ -344,16 +357,25 @@ def oracle_sample(cfg, seconds_target: float, min_tokens=1, max_tokens=64):
     from datagen import configs as C
 
     d = oracle.dims(**cfg.dims)
-    W = C.layer_weights(cfg)
     x_all = C.layer_x(cfg)
+    if is_shared(cfg):
+        SW = C.shared_weights(cfg)
 
-    def run(rows):
-        x = np.ascontiguousarray(x_all[rows])
-        ids, _, _, _ = oracle.route(d, x, W["wr"], W["bias"])
-        ex = {int(e): C.expert_tensors(cfg, int(e)) for e in np.unique(ids) if e >= 0}
-        t0 = time.perf_counter()
-        oracle.forward(d, x, W["wr"], W["bias"], W["wd"], W["wu"], W["gamma"], ex, True, 0)
-        return time.perf_counter() - t0
+        def run(rows):
+            x = np.ascontiguousarray(x_all[rows])
+            t0 = time.perf_counter()
+            oracle.shared(d, x, SW["wgu"], SW["wdn"], True)
+            return time.perf_counter() - t0
+    else:
+        W = C.layer_weights(cfg)
+
+        def run(rows):
+            x = np.ascontiguousarray(x_all[rows])
+            ids, _, _, _ = oracle.route(d, x, W["wr"], W["bias"])
+            ex = {int(e): C.expert_tensors(cfg, int(e)) for e in np.unique(ids) if e >= 0}
+            t0 = time.perf_counter()
+            oracle.forward(d, x, W["wr"], W["bias"], W["wd"], W["wu"], W["gamma"], ex, True, 0)
+            return time.perf_counter() - t0
 
     T = x_all.shape[0]
     t1 = run([0])
@@ -556,14 +578,21 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
                      "tflops_bf16_equivalent_frac": tf / peaks["bf16_tflops"]})
     elif tc:
         # the grouped GEMM runs for milliseconds inside a step of a few milliseconds: the
-        # burst bf16 peak is its denominator
-        achieved = alg[dom]["flops"] / (phase_ms[dom] / 1e3) / 1e12
-        peak = peaks["bf16_tflops"]
+        # burst bf16 peak is its tensor denominator; with few tokens per expert (chunks) the
+        # weight bytes bound it instead -- the tighter of the two is reported
+        t_s = phase_ms[dom] / 1e3
+        tf, gb = alg[dom]["flops"] / t_s / 1e12, alg[dom]["bytes"] / t_s / 1e9
+        f_t, f_h = tf / peaks["bf16_tflops"], gb / peaks["hbm_gbs"]
         kv = profiled(dom, cfg.name) or {}
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(dom, cfg.name), "kernel": "k3_tc_moe_kernel<0> (gate/up)",
-                "peak_kind": f"{peak_kind} bf16 burst",
-                "tensor_pipe_active_pct": float(kv["tensor_pipe_active_pct"]) if "tensor_pipe_active_pct" in kv else None}
+        if f_t >= f_h:
+            roof = {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": f_t,
+                    "peak_kind": f"{peak_kind} bf16 burst", "other_bound_frac": f_h}
+        else:
+            roof = {"bound": "hbm", "achieved": gb, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": f_h,
+                    "peak_kind": f"{peak_kind} HBM copy", "other_bound_frac": f_t}
+        roof.update({"traffic": profiled_traffic(dom, cfg.name), "kernel": "k3_tc_moe_kernel<0> (gate/up)",
+                     "tensor_pipe_active_pct": float(kv["tensor_pipe_active_pct"]) if "tensor_pipe_active_pct" in kv
+                     else None})
     else:
         achieved = alg[dom]["bytes"] / (phase_ms[dom] / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
@@ -659,6 +688,96 @@ def sweep(a, local_rank):
         torch.cuda.empty_cache()
 
 
+def measure_shared(a, cfg, k3, dev, world):
+    """Times k3moe_shared_forward (the fused shared experts accumulated into the output) on
+    one workload: CUDA-graph replay with the L2 flushed, and end to end with host buffers."""
+    import torch
+    from datagen import configs as C
+    from datagen import device as D
+
+    unit, hib = unit_of(cfg)
+    T, H, Is = cfg.T, cfg.hidden, C.SHARED_INTER
+    d = k3.dims(**cfg.dims)
+    SW = C.shared_weights(cfg, Is)
+    wgu, wdn = D.bf16_tensor(SW["wgu"], dev), D.bf16_tensor(SW["wdn"], dev)
+    x = D.bf16_tensor(C.layer_x(cfg), dev)
+    out = torch.zeros(T, H, dtype=torch.float32, device=dev)
+    ws = torch.empty(k3.shared_workspace_bytes(d, T, Is), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    step = lambda: k3.shared_forward(d, x, wgu, wdn, out, ws)
+    for _ in range(a.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    status = k3.device_status(ws)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(a.warmup):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    w0 = time.time()
+    for s in range(a.steps):
+        flush.zero_()
+        ev[s][0].record()
+        graph.replay()
+        ev[s][1].record()
+    torch.cuda.synchronize()
+    w1 = time.time()
+    ms = max_over_ranks(statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev), world, dev)
+    e2e = None
+    if not a.no_e2e:
+        xh = x.cpu().pin_memory()
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        xd = torch.empty_like(x)
+        ms_e2e = []
+        for s in range(a.warmup + max(10, a.steps // 4)):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            xd.copy_(xh, non_blocking=True)
+            k3.shared_forward(d, xd, wgu, wdn, out, ws)
+            oh.copy_(out, non_blocking=True)
+            e1.record()
+            e1.synchronize()
+            if s >= a.warmup:
+                ms_e2e.append(e0.elapsed_time(e1))
+        me = max_over_ranks(statistics.mean(ms_e2e), world, dev)
+        e2e = {"value": metric_value(cfg, me, world), "unit": unit, "h2d_bytes_per_step": xh.numel() * 2,
+               "d2h_bytes_per_step": oh.numel() * 4, "ms_per_step": me}
+    peaks, peak_kind = measured_peaks()
+    wbytes = 3 * H * Is * 2
+    bytes_ = wbytes + T * H * (2 + 4 + 4) + T * Is * (2 * 4 + 4 * 2 + 2 * 2)
+    flops = 2 * T * 3 * H * Is
+    gbs = bytes_ / (ms / 1e3) / 1e9
+    tfs = flops / (ms / 1e3) / 1e12
+    if T >= k3.tc_min_tokens():
+        roof = {"bound": "tensor", "achieved": tfs, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": tfs / peaks["bf16_tflops"], "peak_kind": f"{peak_kind} bf16 burst",
+                "kernel": "whole call: k3_tc_dense_kernel<PLAIN>, k3_shared_glu_kernel, k3_tc_dense_kernel<ACC>"}
+    else:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"], "peak_kind": f"{peak_kind} HBM copy",
+                "kernel": "whole call: dense GEMV<PLAIN>, k3_shared_glu_kernel, dense GEMV<ACC>"}
+    roof["traffic"] = None
+    roof["algorithmic_per_call"] = {"bytes": bytes_, "flops": flops}
+    del ws, flush, wgu, wdn
+    torch.cuda.empty_cache()
+    return {"value": metric_value(cfg, ms, world), "unit": unit, "higher_is_better": hib, "ms_per_step": ms,
+            "config": {"workload": describe(cfg), "global_batch": T * world, "seq_len": T,
+                       "parallelism": f"replicas x{world}", "l2": "flushed by a 256 MiB write before every timed step",
+                       "cuda_graph": True},
+            "roofline": roof, "e2e": e2e, "gpu_launches": 3 * a.steps, "device_status": status,
+            "_window": (w0, w1)}
+
+
 def run_ours(a, cfgs, rank, world, local_rank):
     import torch
 
@@ -676,7 +795,8 @@ def run_ours(a, cfgs, rank, world, local_rank):
     pools = {}
     results = {}
     for name, cfg in cfgs:
-        results[name] = measure(a, cfg, k3, dev, world, pools, sampler)
+        results[name] = (measure_shared(a, cfg, k3, dev, world) if is_shared(cfg)
+                         else measure(a, cfg, k3, dev, world, pools, sampler))
     time.sleep(0.1)
     sampler.stop()
     for r in results.values():
@@ -699,8 +819,8 @@ def run_ours(a, cfgs, rank, world, local_rank):
             "warmup": a.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": head["higher_is_better"],
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(head["config"], timed_workloads=[n for n, _ in cfgs]),
-            "roofline": head["roofline"], "layer": head["layer"], "expert_phase": head["expert_phase"],
-            "phases": head["phases"], "profiled_ms_per_step": head["profiled_ms_per_step"], "clocks": clocks,
+            "roofline": head["roofline"], "layer": head.get("layer"), "expert_phase": head.get("expert_phase"),
+            "phases": head.get("phases"), "profiled_ms_per_step": head.get("profiled_ms_per_step"), "clocks": clocks,
             "e2e": head["e2e"], "gpu_launches": sum(results[n]["gpu_launches"] for n, _ in cfgs),
             "device_status": head["device_status"]}
     if "cpu_baseline" in head:

@@ -219,6 +219,28 @@ k3moe_status k3moe_permute(const k3moe_dims* dims, int32_t T, const int32_t* ids
  * k3moe_forward_noalloc call on the current device.  Synchronises `stream`. */
 k3moe_status k3moe_device_status(const void* ws, uint32_t* host_out, void* stream);
 
+/* ---- Shared experts beside the routed block (colibri PR #684, engine commit: "2 fused
+ * shared experts"; colibri PR #676, architecture bullets: SiTU-GLU).  Two SiTU-GLU experts
+ * on the hidden width H, fused along the intermediate dimension into one of width inter_s
+ * (the pages give no width; at K3 shapes each is read as a routed expert's 3072, inter_s
+ * = 6144):
+ *   g = x . Wgu[0:Is]^T,  u = x . Wgu[Is:2Is]^T  (fp32 accumulation),
+ *   h = bf16(SiTU(g, u)),  out[t] += h . Wdn^T   (fp32).
+ * The block's output is the routed output plus this: call it after k3moe_forward on the
+ * same stream with the same out (or on a zeroed buffer of its own).
+ *   x          [T, H] bf16, device, 16-byte aligned
+ *   w_gate_up  [2 inter_s, H] bf16 (gate rows first, then up rows), device
+ *   w_down     [H, inter_s] bf16, device
+ *   out        [T, H] f32, device, read and written (accumulated into)
+ *   ws         device workspace of k3moe_shared_workspace_bytes(dims, T, inter_s) bytes
+ * inter_s must be a positive multiple of 64 (ERR_SHAPE otherwise).  Below
+ * k3moe_tc_min_tokens tokens the products run on the weight-streaming GEMVs, from it on
+ * the tcgen05 GEMMs.  Status word at the start of ws (k3moe_device_status). */
+size_t k3moe_shared_workspace_bytes(const k3moe_dims* dims, int32_t T, int32_t inter_s);
+k3moe_status k3moe_shared_forward(const k3moe_dims* dims, int32_t T, int32_t inter_s, const uint16_t* x,
+                                  const uint16_t* w_gate_up, const uint16_t* w_down, float* out, void* ws,
+                                  size_t ws_bytes, void* stream);
+
 /* Token count from which k3moe_forward (and k3moe_route) run the projections and the
  * experts on the tensor-core GEMMs instead of the weight-streaming GEMVs (default 9, the
  * crossover measured on GB300 at K3 shapes: 8 random tokens 523 us on the GEMVs against

@@ -90,6 +90,8 @@ def lib():
                 "k3moe_forward": ([D, i32, p, p, p, p, p, p, X, p, p, p, p, sz, p], ctypes.c_int),
                 "k3moe_forward_profiled": ([D, i32, p, p, p, p, p, p, X, p, p, p, p, sz, p, p, i32], ctypes.c_int),
                 "k3moe_expert_forward": ([D, i32, p, i32, X, p, p, sz, p], ctypes.c_int),
+                "k3moe_shared_workspace_bytes": ([D, i32, i32], sz),
+                "k3moe_shared_forward": ([D, i32, i32, p, p, p, p, p, sz, p], ctypes.c_int),
                 "k3moe_forward_noalloc": ([D, i32, p, p, p, p, p, p, X, p, p, p, p], ctypes.c_int),
                 "k3moe_dequant_mxfp4": ([p, p, i32, i32, p, p], ctypes.c_int),
                 "k3moe_permute": ([D, i32, p, p, p, p, p, p, p, sz, p], ctypes.c_int),
@@ -200,6 +202,19 @@ def expert_forward(d: Dims, z, expert: int, experts: ExpertTables, out, ws, stre
     _check(lib().k3moe_expert_forward(ctypes.byref(d), z.shape[0], _ptr(z), expert, ctypes.byref(experts.c),
                                       _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "k3moe_expert_forward")
+
+
+def shared_workspace_bytes(d: Dims, T: int, inter_s: int) -> int:
+    return int(lib().k3moe_shared_workspace_bytes(ctypes.byref(d), T, inter_s))
+
+
+def shared_forward(d: Dims, x, w_gate_up, w_down, out, ws, stream=None):
+    """k3moe_shared_forward: out [T, H] += the fused shared experts of x [T, H];
+    w_gate_up [2 Is, H] (gate rows, then up rows), w_down [H, Is], all bf16."""
+    inter_s = w_down.shape[1]
+    _check(lib().k3moe_shared_forward(ctypes.byref(d), x.shape[0], inter_s, _ptr(x), _ptr(w_gate_up), _ptr(w_down),
+                                      _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "k3moe_shared_forward")
 
 
 def dequant_mxfp4(q, s, out, stream=None):

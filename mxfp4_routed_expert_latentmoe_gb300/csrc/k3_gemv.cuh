@@ -275,7 +275,7 @@ constexpr int DN_CHUNK = 64;  // elements per row per stage
 constexpr int DN_WARPS = 8;
 constexpr int DN_A_BYTES = 16 * DN_CHUNK * 2;  // 2048: 16 weight rows
 
-enum { DN_PROJ = 0, DN_PLAIN = 1 };
+enum { DN_PROJ = 0, DN_PLAIN = 1, DN_ACC = 2 };  // ACC: out0 += the product
 
 struct DenseParams {
   const uint16_t* W0;
@@ -285,7 +285,7 @@ struct DenseParams {
   int K;
   const uint16_t* act;  // [T, K] bf16
   int T;
-  float* out0;      // PROJ: logits [T, R0]; PLAIN: out [T, R0]
+  float* out0;      // PROJ: logits [T, R0]; PLAIN: out [T, R0]; ACC: out [T, R0], added to
   uint16_t* out1;   // PROJ: z [T, R1] bf16
   uint32_t* zmax;   // PROJ: per-token max |z| (f32 bits)
   uint32_t* status; // device status word (bounded waits that run out)
@@ -434,6 +434,8 @@ __global__ void __launch_bounds__(DN_WARPS * 32) k3_dense_gemv_kernel(DenseParam
           const uint16_t zb = f32_to_bf16_bits(sum);
           p.out1[(size_t)tok * p.R1 + row0 + row] = zb;
           atomicMax(p.zmax + tok, __float_as_uint(fabsf(bf16_bits_to_f32(zb))));
+        } else if (EPI == DN_ACC) {
+          p.out0[(size_t)tok * p.R0 + row0 + row] += sum;
         } else {
           p.out0[(size_t)tok * p.R0 + row0 + row] = sum;
         }

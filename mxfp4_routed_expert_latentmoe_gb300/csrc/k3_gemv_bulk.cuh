@@ -423,6 +423,8 @@ __global__ void __launch_bounds__(D1_WARPS * 32, 2) k3_dense_gemv1_kernel(DenseP
         const uint16_t zb = f32_to_bf16_bits(sum);
         p.out1[r - p.R0] = zb;
         atomicMax(p.zmax, __float_as_uint(fabsf(bf16_bits_to_f32(zb))));
+      } else if (EPI == DN_ACC) {
+        p.out0[r] += sum;
       } else {
         p.out0[r] = sum;
       }

@@ -221,13 +221,13 @@ constexpr int TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;
 constexpr int TC_THREADS = 192;
 constexpr int TC_SMEM = 1024 + TC_STAGES * TC_STAGE_BYTES + 256;  // alignment slack, ring, barriers
 
-enum { TC_PROJ = 0, TC_PLAIN = 1 };
+enum { TC_PROJ = 0, TC_PLAIN = 1, TC_ACC = 2 };  // ACC: out0 += the product
 
 struct TcDenseParams {
   int M;       // rows of A (tokens)
   int N0, N1;  // output features from B map 0 and from B map 1 (0: none)
   int K;       // reduction length (multiple of 64)
-  float* out0;     // PROJ: logits [M, N0]; PLAIN: out [M, N0]
+  float* out0;     // PROJ: logits [M, N0]; PLAIN: out [M, N0]; ACC: out [M, N0], added to
   uint16_t* out1;  // PROJ: z [M, N1] bf16
   uint32_t* zmax;  // PROJ: per-row max |z| (f32 bits)
   uint32_t* status;
@@ -391,12 +391,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             float* dst = p.out0 + (size_t)row * p.N0 + col0;
             if (col0 + 32 <= N && (p.N0 % 4) == 0) {
 #pragma unroll
-              for (int v = 0; v < 8; ++v)
-                reinterpret_cast<float4*>(dst)[v] =
-                    make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]), __uint_as_float(r[4 * v + 2]),
-                                __uint_as_float(r[4 * v + 3]));
+              for (int v = 0; v < 8; ++v) {
+                float4 o = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                       __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                if (EPI == TC_ACC) {
+                  const float4 prev = reinterpret_cast<const float4*>(dst)[v];
+                  o = make_float4(prev.x + o.x, prev.y + o.y, prev.z + o.z, prev.w + o.w);
+                }
+                reinterpret_cast<float4*>(dst)[v] = o;
+              }
             } else {
-              for (int e = 0; e < 32 && col0 + e < N; ++e) dst[e] = __uint_as_float(r[e]);
+              for (int e = 0; e < 32 && col0 + e < N; ++e)
+                dst[e] = (EPI == TC_ACC) ? dst[e] + __uint_as_float(r[e]) : __uint_as_float(r[e]);
             }
           }
         }

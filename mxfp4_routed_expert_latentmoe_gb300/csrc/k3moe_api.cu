@@ -13,6 +13,7 @@
 #include "k3_tc.cuh"
 #include "k3_front.cuh"
 #include "k3_mx8.cuh"
+#include "k3_shared.cuh"
 
 namespace {
 
@@ -754,6 +755,30 @@ k3moe_status k3moe_forward(const k3moe_dims* dims, int32_t T, const uint16_t* x,
                                 ws_bytes, stream, nullptr, 0);
 }
 
+// ---------------------------------------------------------------------------- shared experts
+namespace {
+struct SharedLayout {
+  size_t status, gu, h, total;
+};
+SharedLayout shared_layout(const k3moe_dims& d, int T, int Is) {
+  SharedLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t b) {
+    const size_t o = off;
+    off += align256(b);
+    return o;
+  };
+  L.status = take(256);
+  L.gu = take((size_t)T * 2 * Is * 4);
+  L.h = take((size_t)T * Is * 2);
+  L.total = off;
+  return L;
+}
+bool shared_ok(const k3moe_dims* d, int Is) {
+  return check_dims(d) == K3MOE_OK && Is > 0 && Is % 64 == 0 && Is <= 65536;
+}
+}  // namespace
+
 k3moe_status k3moe_expert_forward(const k3moe_dims* dims, int32_t T, const uint16_t* z, int32_t expert,
                                   const k3moe_experts* experts, float* out, void* ws, size_t ws_bytes, void* stream) {
   k3moe_status st = check_dims(dims);
@@ -777,6 +802,62 @@ k3moe_status k3moe_expert_forward(const k3moe_dims* dims, int32_t T, const uint1
                               sms, s, true));
   // one expert: sorted slots are the tokens in order, so the down output lands in `out` directly
   K3_TRY(launch_mx<MX_DOWN>(mx_params(d, L, ws, MX_DOWN, at<__half>(ws, L.h16), out), nblk, dev, sms, s, true));
+  return K3MOE_OK;
+}
+
+size_t k3moe_shared_workspace_bytes(const k3moe_dims* dims, int32_t T, int32_t inter_s) {
+  if (!shared_ok(dims, inter_s) || T < 0) return 0;
+  return shared_layout(*dims, T, inter_s).total;
+}
+
+k3moe_status k3moe_shared_forward(const k3moe_dims* dims, int32_t T, int32_t inter_s, const uint16_t* x,
+                                  const uint16_t* w_gate_up, const uint16_t* w_down, float* out, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  k3moe_status st = check_dims(dims);
+  if (st != K3MOE_OK) return st;
+  if (!shared_ok(dims, inter_s)) return K3MOE_ERR_SHAPE;
+  if (T < 0) return K3MOE_ERR_ARG;
+  if (T == 0) return K3MOE_OK;
+  if (!x || !w_gate_up || !w_down || !out || !ws) return K3MOE_ERR_ARG;
+  if (!a16(x) || !a16(w_gate_up) || !a16(w_down) || !a16(out) || !a16(ws)) return K3MOE_ERR_ALIGN;
+  const k3moe_dims d = *dims;
+  const int Is = inter_s, H = d.hidden;
+  const SharedLayout L = shared_layout(d, T, Is);
+  if (ws_bytes < L.total) return K3MOE_ERR_WORKSPACE;
+  int dev, sms;
+  if ((st = check_device(&dev, &sms)) != K3MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  float* gu = at<float>(ws, L.gu);
+  uint16_t* h = at<uint16_t>(ws, L.h);
+  K3_TRY(cudaMemsetAsync(status, 0, 256, s));
+  const bool tc = T >= tc_min_t();
+  // [g | u] = x . Wgu^T
+  if (tc) {
+    TcDenseParams tcp{};
+    tcp.out0 = gu;
+    tcp.status = status;
+    K3_TRY(launch_tc_dense<TC_PLAIN>(x, T, H, w_gate_up, 2 * Is, nullptr, 0, tcp, dev, sms, s, false));
+  } else {
+    DenseParams dp{};
+    dp.W0 = w_gate_up; dp.R0 = 2 * Is; dp.K = H; dp.act = x; dp.T = T; dp.out0 = gu; dp.status = status;
+    K3_TRY(launch_dense<DN_PLAIN>(dp, dev, sms, s, false));
+  }
+  // h = bf16(SiTU(g, u))
+  const size_t items = (size_t)T * (Is / 4);
+  const int gblocks = (int)((items + 255) / 256 < (size_t)sms * 8 ? (items + 255) / 256 : (size_t)sms * 8);
+  K3_TRY(launch(k3_shared_glu_kernel, dim3(gblocks), dim3(256), 0, s, true, (const float*)gu, (int)T, Is, h));
+  // out += h . Wdn^T
+  if (tc) {
+    TcDenseParams tcp{};
+    tcp.out0 = out;
+    tcp.status = status;
+    K3_TRY(launch_tc_dense<TC_ACC>(h, T, Is, w_down, H, nullptr, 0, tcp, dev, sms, s, true));
+  } else {
+    DenseParams dp{};
+    dp.W0 = w_down; dp.R0 = H; dp.K = Is; dp.act = h; dp.T = T; dp.out0 = out; dp.status = status;
+    K3_TRY(launch_dense<DN_ACC>(dp, dev, sms, s, true));
+  }
   return K3MOE_OK;
 }
 

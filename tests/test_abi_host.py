@@ -162,3 +162,21 @@ def test_tensor_core_threshold_moves_the_workspace_step():
     finally:
         k3.set_tc_min_tokens(prev)
     assert L.k3moe_set_tc_min_tokens(9) == 9
+
+
+def test_shared_forward_validates_on_the_host():
+    L = k3.lib()
+    d = _d()
+    assert L.k3moe_shared_workspace_bytes(ctypes.byref(d), 1, 6144) > 1 * 2 * 6144 * 4
+    for bad in (0, -64, 100):
+        assert L.k3moe_shared_workspace_bytes(ctypes.byref(d), 1, bad) == 0
+    v = ctypes.c_void_p(16)
+    nb = L.k3moe_shared_workspace_bytes(ctypes.byref(d), 1, 6144)
+    assert L.k3moe_shared_forward(ctypes.byref(d), 0, 6144, v, v, v, v, v, nb, None) == 0
+    assert L.k3moe_shared_forward(ctypes.byref(d), 1, 100, v, v, v, v, v, nb, None) == ERR_SHAPE
+    assert L.k3moe_shared_forward(ctypes.byref(d), 1, 6144, None, v, v, v, v, nb, None) == ERR_ARG
+    assert L.k3moe_shared_forward(ctypes.byref(d), 1, 6144, ctypes.c_void_p(24), v, v, v, v, nb, None) == ERR_ALIGN
+    assert L.k3moe_shared_forward(ctypes.byref(d), 1, 6144, v, v, v, v, v, nb - 1, None) == ERR_WS
+    import torch
+    if not torch.cuda.is_available():
+        assert L.k3moe_shared_forward(ctypes.byref(d), 1, 6144, v, v, v, v, v, nb, None) == ERR_DEVICE
