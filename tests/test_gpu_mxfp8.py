@@ -144,3 +144,21 @@ def test_variant_forward_against_variant_oracle(k3, mx_prefill, T, n_rows):
           f"variant oracle vs exact oracle {cost:.3e}")
     assert pooled <= MX_BAR, pooled
     assert max(per) <= MX_PER_TOKEN_BAR, max(per)
+
+
+def test_variant_with_top_p_pruning(k3, mx_prefill):
+    """The variant on the tensor-core path with K3_TOPP pruning (slots with id -1 take no
+    part in the batches): ids and weights as the oracle's, outputs within the variant's bars."""
+    cfg = dataclasses.replace(MX_PREFILL.with_tokens(300, x_seed=61), top_p=0.5)
+    L = mx_prefill.with_tokens(k3, cfg)
+    L.d = k3.dims(**cfg.dims)
+    got, ids, w, ws = L.forward(k3)
+    assert k3.device_status(ws) == 0
+    assert (ids == -1).any()
+    rows = [0, 1, 150, 299]
+    ref = oracle_forward(cfg, token_rows=rows)
+    assert np.array_equal(ids[rows], ref["ids"])
+    assert np.allclose(w[rows], ref["w"], rtol=0, atol=2e-6)
+    pooled = rel_l2(got[rows], ref["out"])
+    print(f"MXFP8 variant with top-p 0.5 at T=300: rel-L2 {pooled:.3e}")
+    assert pooled <= MX_BAR

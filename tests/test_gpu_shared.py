@@ -56,3 +56,32 @@ def test_shared_forward_accumulates_the_fused_experts(k3, shared_w, T):
     print(f"shared experts T={T} ({path}): rel-L2 {pooled:.3e}, worst token {max(per):.3e}")
     assert pooled <= REL_L2_BAR, pooled
     assert max(per) <= PER_TOKEN_BAR, max(per)
+
+
+def test_shared_forward_edge_cases(k3, shared_w):
+    """Zero tokens launch nothing; two calls add the experts twice (the accumulation is exact
+    in its order: out + s + s); the first tensor-core batch (T = the threshold) and the last
+    weight-streaming one (T = threshold - 1) agree with the oracle."""
+    from datagen import device as D
+    W, wgu, wdn = shared_w
+    d = k3.dims(**C.DECODE.dims)
+    ws = torch.empty(k3.shared_workspace_bytes(d, 16, C.SHARED_INTER), dtype=torch.uint8, device="cuda")
+    out = torch.zeros(0, C.DECODE.hidden, dtype=torch.float32, device="cuda")
+    k3.shared_forward(d, torch.zeros(0, C.DECODE.hidden, dtype=torch.bfloat16, device="cuda"), wgu, wdn, out, ws)
+    t0 = k3.tc_min_tokens()
+    for T in (t0 - 1, t0):
+        cfg = C.DECODE.with_tokens(T, x_seed=71 + T)
+        xb = C.layer_x(cfg)
+        x = D.bf16_tensor(xb, "cuda")
+        out = torch.zeros(T, cfg.hidden, dtype=torch.float32, device="cuda")
+        k3.shared_forward(d, x, wgu, wdn, out, ws)
+        once = out.clone()
+        k3.shared_forward(d, x, wgu, wdn, out, ws)
+        torch.cuda.synchronize()
+        assert k3.device_status(ws) == 0
+        assert torch.equal(out, once + once)
+        _, ref = oracle.shared(oracle.dims(**cfg.dims), xb, W["wgu"], W["wdn"], True)
+        got = once.double().cpu().numpy()
+        print(f"shared experts T={T}: rel-L2 {rel_l2(got, ref):.3e}")
+        assert rel_l2(got, ref) <= REL_L2_BAR
+        assert max(rel_l2(got[i], ref[i]) for i in range(T)) <= PER_TOKEN_BAR
