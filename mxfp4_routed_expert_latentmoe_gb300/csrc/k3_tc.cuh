@@ -231,6 +231,12 @@ struct TcDenseParams {
   uint16_t* out1;  // PROJ: z [M, N1] bf16
   uint32_t* zmax;  // PROJ: per-row max |z| (f32 bits)
   uint32_t* status;
+  // split-K (few rows: too few output tiles to fill the GPU): ksplit > 1 CTAs share each
+  // tile, each over kblocks / ksplit of the k-blocks, and write raw fp32 partial sums to
+  // part [ksplit][M][N0 + N1]; k3_tc_splitk_reduce_kernel adds them in order and applies
+  // the epilogue
+  int ksplit;
+  float* part;
 };
 
 template <int EPI>
@@ -253,8 +259,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   const int m_tiles = (p.M + TC_BM - 1) / TC_BM;
   const int n_t0 = (p.N0 + TC_BN - 1) / TC_BN, n_t1 = (p.N1 + TC_BN - 1) / TC_BN;
-  const int tiles = m_tiles * (n_t0 + n_t1);
-  const int kblocks = p.K / TC_BK;
+  const int otiles = m_tiles * (n_t0 + n_t1);  // output tiles
+  const int ks = p.ksplit > 1 ? p.ksplit : 1;
+  const int tiles = otiles * ks;               // work units: output tile x k-range
+  const int kblocks = p.K / TC_BK / ks;        // k-blocks per work unit
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
@@ -290,11 +298,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (lane == 0) {
       int it = 0;
       for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x) {
-        const int tm = tile % m_tiles, tn = tile / m_tiles;
+        const int ot = tile % otiles, kb0 = (tile / otiles) * kblocks;
+        const int tm = ot % m_tiles, tn = ot / m_tiles;
         const bool b1 = tn >= n_t0;
         const CUtensorMap* mb = b1 ? &mapB1 : &mapB0;
         const int n0 = (b1 ? tn - n_t0 : tn) * TC_BN;
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        for (int kb = kb0; kb < kb0 + kblocks; ++kb, ++it) {
           const int s = it % TC_STAGES;
           if (!mbar_wait(empty_bar(s), ((it / TC_STAGES) & 1) ^ 1, abort_flag)) break;
           const uint32_t st = base + s * TC_STAGE_BYTES;
@@ -323,7 +332,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem + b * TC_BN;
         bool ok = true;
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {  // k-blocks of the work unit, counted from 0
           const int s = it % TC_STAGES;
           if (!mbar_wait(full_bar(s), (it / TC_STAGES) & 1, abort_flag)) {
             ok = false;
@@ -352,7 +361,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int b = lt & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(b), (lt >> 1) & 1, abort_flag))) break;
       tc_fence_after();
-      const int tm = tile % m_tiles, tn = tile / m_tiles;
+      const int ot = tile % otiles, kq = tile / otiles;
+      const int tm = ot % m_tiles, tn = ot / m_tiles;
       const bool b1 = tn >= n_t0;
       const int n0 = (b1 ? tn - n_t0 : tn) * TC_BN;
       const int row = tm * TC_BM + q * 32 + lane;
@@ -365,7 +375,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tmem_ld_wait();
         const int col0 = n0 + c * 32;
         if (row < p.M && col0 < N) {
-          if (EPI == TC_PROJ && b1) {
+          if (ks > 1) {
+            // raw partial sums of this k-range: part[kq][row][(N0 if b1) + col]
+            const int NT = p.N0 + p.N1;
+            float* dst = p.part + ((size_t)kq * p.M + row) * NT + (b1 ? p.N0 : 0) + col0;
+            if (col0 + 32 <= N && (NT % 4) == 0 && (p.N0 % 4) == 0) {
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                reinterpret_cast<float4*>(dst)[v] =
+                    make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+            } else {
+              for (int e = 0; e < 32 && col0 + e < N; ++e) dst[e] = __uint_as_float(r[e]);
+            }
+          } else if (EPI == TC_PROJ && b1) {
             uint16_t* dst = p.out1 + (size_t)row * p.N1 + col0;
             if (col0 + 32 <= N) {
 #pragma unroll
@@ -407,7 +430,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
         }
       }
-      if (EPI == TC_PROJ && b1 && row < p.M) atomicMax(p.zmax + row, __float_as_uint(zm));
+      if (EPI == TC_PROJ && b1 && ks == 1 && row < p.M) atomicMax(p.zmax + row, __float_as_uint(zm));
       tc_fence_before();
       mbar_arrive(tempty_bar(b));
     }
@@ -417,6 +440,43 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+}
+
+// Split-K epilogue: CTA (row, column chunk of TC_RED_COLS); out = sum of the ksplit
+// partials in order, then the dense epilogue (PLAIN: out0; ACC: out0 +=; PROJ: logits for
+// the first N0 columns, z (bf16) and the row's max |z| for the next N1)
+constexpr int TC_RED_COLS = 1024;
+template <int EPI>
+__global__ void __launch_bounds__(256) k3_tc_splitk_reduce_kernel(TcDenseParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int row = blockIdx.x, NT = p.N0 + p.N1;
+  const int c_end = min(NT, (int)(blockIdx.y + 1) * TC_RED_COLS);
+  __shared__ float wmax[8];
+  float zm = 0.f;
+  for (int c = blockIdx.y * TC_RED_COLS + threadIdx.x; c < c_end; c += blockDim.x) {
+    float sum = 0.f;
+    for (int kq = 0; kq < p.ksplit; ++kq) sum += p.part[((size_t)kq * p.M + row) * NT + c];
+    if (c < p.N0) {
+      float* o = p.out0 + (size_t)row * p.N0 + c;
+      *o = (EPI == TC_ACC) ? *o + sum : sum;
+    } else {
+      const uint16_t zb = f32_to_bf16_bits(sum);
+      p.out1[(size_t)row * p.N1 + (c - p.N0)] = zb;
+      zm = fmaxf(zm, fabsf(bf16_bits_to_f32(zb)));
+    }
+  }
+  if (EPI == TC_PROJ && p.N1 > 0) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, off));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = zm;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float m = 0.f;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, wmax[w]);
+      atomicMax(p.zmax + row, __float_as_uint(m));
+    }
   }
 }
 

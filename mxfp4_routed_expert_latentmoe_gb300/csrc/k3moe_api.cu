@@ -22,6 +22,7 @@ using namespace k3;
 constexpr float kTieTau = 3e-5f;
 constexpr int kMaxDevices = 64;
 constexpr int kTcMinTokensDefault = 9;  // measured crossover on GB300 at K3 shapes (bench.py --sweep)
+constexpr int kSplitKMaxT = 512;        // the projections split K only when they have few output tiles
 
 size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 int tc_min_t();
@@ -29,6 +30,7 @@ int tc_min_t();
 struct WsLayout {
   size_t status, logits, ids, w, zmax, zpow, counts, offsets, slot_of, slot_tok, inv, uniq, n_uniq, nb_prefix,
       n_batches, cta_cnt, cta_base, batches, z, z16, h16, o, y, yhat, cpart, ccount, act, tmaps, zero_end, total;
+  size_t part = 0, part_bytes = 0;
 };
 
 WsLayout ws_layout(const k3moe_dims& d, int T) {
@@ -78,6 +80,9 @@ WsLayout ws_layout(const k3moe_dims& d, int T) {
   const bool tc = T >= tc_min_t();
   L.act = take(tc ? slots * Lt * 2 : 0);
   L.tmaps = take(tc ? (size_t)TM_MAX_CTAS * TM_BLOCKS * 2 * 128 : 0);  // packed-weight tensor maps
+  // split-K partial sums of the projections (few tokens on the tensor-core path)
+  L.part_bytes = (tc && T <= kSplitKMaxT) ? (size_t)8 * T * std::max<size_t>((size_t)E + Lt, d.hidden) * 4 : 0;
+  L.part = take(L.part_bytes);
   L.total = off;
   return L;
 }
@@ -318,7 +323,8 @@ cudaError_t launch_mx8_moe(const uint8_t* act, Mx8Params p, int dev, int sms, cu
 // D[M, N0 (+N1)] = A[M, K] . [B0; B1]^T on tcgen05 (A, B bf16 row-major)
 template <int EPI>
 cudaError_t launch_tc_dense(const uint16_t* A, int M, int K, const uint16_t* B0, int N0, const uint16_t* B1, int N1,
-                            TcDenseParams p, int dev, int sms, cudaStream_t st, bool pdl) {
+                            TcDenseParams p, int dev, int sms, cudaStream_t st, bool pdl, float* part = nullptr,
+                            size_t part_bytes = 0) {
   CUtensorMap ma, mb0, mb1;
   if (!map_bf16(&ma, A, M, K, TC_BM) || !map_bf16(&mb0, B0, N0, K, TC_BN)) return cudaErrorInvalidValue;
   if (N1 > 0) {
@@ -332,8 +338,23 @@ cudaError_t launch_tc_dense(const uint16_t* A, int M, int K, const uint16_t* B0,
   p.K = K;
   if (!set_smem<k3_tc_dense_kernel<EPI>>(dev, TC_SMEM)) return cudaErrorInvalidValue;
   const int tiles = ((M + TC_BM - 1) / TC_BM) * ((N0 + TC_BN - 1) / TC_BN + (N1 + TC_BN - 1) / TC_BN);
-  const int grid = tiles < sms ? tiles : sms;
-  return launch(k3_tc_dense_kernel<EPI>, dim3(grid), dim3(TC_THREADS), TC_SMEM, st, pdl, ma, mb0, mb1, p);
+  // few output tiles (few tokens): split K over up to 8 CTAs per tile, partial sums in
+  // `part`, so that the weight stream is spread over the SMs
+  p.ksplit = 1;
+  p.part = part;
+  const int kb = K / TC_BK;
+  for (int ks = 8; ks >= 2 && part; ks >>= 1)
+    if (2 * tiles <= sms && kb % ks == 0 && kb / ks >= TC_STAGES && (size_t)ks * M * (N0 + N1) * 4 <= part_bytes) {
+      p.ksplit = ks;
+      break;
+    }
+  const int units = tiles * p.ksplit;
+  const int grid = units < sms ? units : sms;
+  cudaError_t e = launch(k3_tc_dense_kernel<EPI>, dim3(grid), dim3(TC_THREADS), TC_SMEM, st, pdl, ma, mb0, mb1, p);
+  if (e == cudaSuccess && p.ksplit > 1)
+    e = launch(k3_tc_splitk_reduce_kernel<EPI>, dim3(M, (N0 + N1 + TC_RED_COLS - 1) / TC_RED_COLS), dim3(256), 0,
+               st, true, p);
+  return e;
 }
 
 template <int MODE, int NBLK, int STAGES, bool FULL>
@@ -570,7 +591,8 @@ k3moe_status k3moe_route(const k3moe_dims* dims, int32_t T, const uint16_t* x, c
     TcDenseParams tcp{};
     tcp.out0 = at<float>(ws, L.logits);
     tcp.status = at<uint32_t>(ws, L.status);
-    K3_TRY(launch_tc_dense<TC_PLAIN>(x, T, d.hidden, wr, d.n_experts, nullptr, 0, tcp, dev, sms, s, false));
+    K3_TRY(launch_tc_dense<TC_PLAIN>(x, T, d.hidden, wr, d.n_experts, nullptr, 0, tcp, dev, sms, s, false,
+                                     at<float>(ws, L.part), L.part_bytes));
   } else {
     DenseParams dp{};
     dp.W0 = wr; dp.R0 = d.n_experts; dp.W1 = nullptr; dp.R1 = 0; dp.K = d.hidden; dp.act = x; dp.T = T;
@@ -656,7 +678,8 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
       TcDenseParams tcp{};
       tcp.out0 = at<float>(ws, L.logits); tcp.out1 = at<uint16_t>(ws, L.z); tcp.zmax = at<uint32_t>(ws, L.zmax);
       tcp.status = status;
-      K3_TRY(launch_tc_dense<TC_PROJ>(x, T, d.hidden, wr, d.n_experts, w_down, d.latent, tcp, dev, sms, s, false));
+      K3_TRY(launch_tc_dense<TC_PROJ>(x, T, d.hidden, wr, d.n_experts, w_down, d.latent, tcp, dev, sms, s, false,
+                                      at<float>(ws, L.part), L.part_bytes));
     } else {
       K3_TRY(launch_dense<DN_PROJ>(dp, dev, sms, s, false));
     }
@@ -736,7 +759,7 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
     tcp.out0 = out;
     tcp.status = status;
     K3_TRY(launch_tc_dense<TC_PLAIN>(at<uint16_t>(ws, L.yhat), T, d.latent, w_up, d.hidden, nullptr, 0, tcp, dev, sms,
-                                     s, pdl));
+                                     s, pdl, at<float>(ws, L.part), L.part_bytes));
   } else {
     DenseParams up{};
     up.W0 = w_up; up.R0 = d.hidden; up.K = d.latent; up.act = at<uint16_t>(ws, L.yhat); up.T = T; up.out0 = out;
