@@ -64,6 +64,10 @@ def parse(argv=None):
                          "(weight-streaming GEMVs and tensor-core GEMMs) and print one JSON line per count")
     ap.add_argument("--tc-min-tokens", type=int, default=None,
                     help="token count from which the tensor-core path runs (library default if omitted)")
+    ap.add_argument("--tc-split-max-tokens", type=int, default=None,
+                    help="token count below which the exact tensor-core expert GEMMs take the two-term "
+                         "MXFP8 split (from it on the bf16 weight decode; 0 = never; library default if "
+                         "omitted)")
     ap.add_argument("--no-flush", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--oracle-sample", choices=WORKLOADS, default=None, help=argparse.SUPPRESS)
     a = ap.parse_args(argv)
@@ -113,7 +117,22 @@ def kernels_per_step(cfg, tc: bool) -> int:
     if not tc and cfg.T <= 64:
         return 6
     perm = 4 if cfg.T * cfg.top_k > 2 * 2048 else 1
-    return 7 + perm
+    return 7 + perm + (splitk_reductions(cfg) if tc else 0)
+
+
+def splitk_reductions(cfg, sms: int = 152) -> int:
+    """The tensor-core projections split K over up to 8 CTAs per output tile when the tiles
+    (128 tokens x 256 columns) number at most half the SMs (up to 512 tokens), each split
+    launch followed by its reduction: the router + latent-down launch (E + L columns, K = H)
+    and the latent up (H columns, K = L)."""
+    if cfg.T > 512:
+        return 0
+    m = -(-cfg.T // 128)
+    n = 0
+    for cols, K in ((-(-cfg.n_experts // 256) + -(-cfg.latent // 256), cfg.hidden), (-(-cfg.hidden // 256), cfg.latent)):
+        kb = K // 64
+        n += any(2 * m * cols <= sms and kb % ks == 0 and kb // ks >= 4 for ks in (8, 4, 2))
+    return n
 
 
 def uses_grouped_gemm(cfg, tc_min_tokens: int) -> bool:
@@ -579,7 +598,9 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
     elif tc:
         # the grouped GEMM runs for milliseconds inside a step of a few milliseconds: the
         # burst bf16 peak is its tensor denominator; with few tokens per expert (chunks) the
-        # weight bytes bound it instead -- the tighter of the two is reported
+        # weight bytes bound it instead -- the tighter of the two is reported.  The split
+        # form does the bf16 products exactly as two fp8 passes (twice the fp8 work at
+        # twice the bf16 rate): the algorithmic flops against the bf16 peak are its bound too
         t_s = phase_ms[dom] / 1e3
         tf, gb = alg[dom]["flops"] / t_s / 1e12, alg[dom]["bytes"] / t_s / 1e9
         f_t, f_h = tf / peaks["bf16_tflops"], gb / peaks["hbm_gbs"]
@@ -590,7 +611,10 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
         else:
             roof = {"bound": "hbm", "achieved": gb, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": f_h,
                     "peak_kind": f"{peak_kind} HBM copy", "other_bound_frac": f_t}
-        roof.update({"traffic": profiled_traffic(dom, cfg.name), "kernel": "k3_tc_moe_kernel<0> (gate/up)",
+        split = cfg.T < k3.tc_split_max_tokens() and cfg.latent >= 512 and cfg.inter >= 512
+        roof.update({"traffic": profiled_traffic(dom, cfg.name),
+                     "kernel": "k3_mx8_moe_kernel<0, 1> (gate/up, exact two-term split)" if split
+                     else "k3_tc_moe_kernel<0> (gate/up, bf16 weight decode)",
                      "tensor_pipe_active_pct": float(kv["tensor_pipe_active_pct"]) if "tensor_pipe_active_pct" in kv
                      else None})
     else:
@@ -625,9 +649,10 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
 
 def sweep(a, local_rank):
     """The GEMV / tensor-core crossover: the whole forward of the prefill-shape layer at each
-    token count, once with the tensor-core path forced off and once forced on (the threshold
-    is the library's process-wide k3moe_set_tc_min_tokens), replayed from a CUDA graph with
-    the L2 flushed before each step."""
+    token count, once with the tensor-core path forced off and forced on in each operand
+    form of the exact grouped GEMM (the library's process-wide k3moe_set_tc_min_tokens and
+    k3moe_set_tc_split_max_tokens), replayed from a CUDA graph with the L2 flushed before
+    each step."""
     import torch
 
     import __graft_entry__ as g
@@ -642,7 +667,7 @@ def sweep(a, local_rank):
     pool, eb, offs = D.expert_pool(base, dev)
     tables = k3.ExpertTables.from_pool(pool, eb, offs)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    default = k3.tc_min_tokens()
+    default, default_split = k3.tc_min_tokens(), k3.tc_split_max_tokens()
     for T in [int(v) for v in a.sweep.split(",")]:
         cfg = base.with_tokens(T, x_seed=base.x_seed)
         d = k3.dims(**cfg.dims)
@@ -650,8 +675,9 @@ def sweep(a, local_rank):
         out = torch.empty(T, cfg.hidden, dtype=torch.float32, device=dev)
         row = {"sweep": "gemv_vs_tensor_core", "T": T, "default_tc_min_tokens": default}
         outs = {}
-        for path, thr in (("gemv", 1 << 30), ("tc", 1)):
+        for path, thr, split in (("gemv", 1 << 30, default_split), ("tc", 1, k3.SPLIT_ALWAYS), ("tc_decode", 1, 0)):
             k3.set_tc_min_tokens(thr)
+            k3.set_tc_split_max_tokens(split)
             ws = torch.empty(k3.workspace_bytes(d, T), dtype=torch.uint8, device=dev)
             args = (d, t["x"], t["wr"], t["bias"], t["wd"], t["wu"], t["gamma"], tables, out, ws)
             for _ in range(a.warmup):
@@ -680,9 +706,10 @@ def sweep(a, local_rank):
             outs[path] = out.clone()
             del graph, ws
         k3.set_tc_min_tokens(default)
-        rel = ((outs["tc"] - outs["gemv"]).norm() / outs["gemv"].norm()).item()
-        row["rel_l2_between_paths"] = rel
-        row["faster"] = "tc" if row["tc_us"] < row["gemv_us"] else "gemv"
+        k3.set_tc_split_max_tokens(default_split)
+        for path in ("tc", "tc_decode"):
+            row[f"rel_l2_{path}_vs_gemv"] = ((outs[path] - outs["gemv"]).norm() / outs["gemv"].norm()).item()
+        row["fastest"] = min(("gemv", "tc", "tc_decode"), key=lambda q: row[f"{q}_us"])
         print(json.dumps(row), flush=True)
         del t, out, outs
         torch.cuda.empty_cache()
@@ -787,6 +814,8 @@ def run_ours(a, cfgs, rank, world, local_rank):
 
     if a.tc_min_tokens:
         k3.set_tc_min_tokens(a.tc_min_tokens)
+    if a.tc_split_max_tokens is not None:
+        k3.set_tc_split_max_tokens(a.tc_split_max_tokens)
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)

@@ -100,6 +100,8 @@ def lib():
                 "k3moe_selftest_wait_timeout": ([p, sz, ctypes.c_int64, p], ctypes.c_int),
                 "k3moe_set_tc_min_tokens": ([i32], i32),
                 "k3moe_tc_min_tokens": ([], i32),
+                "k3moe_set_tc_split_max_tokens": ([i32], i32),
+                "k3moe_tc_split_max_tokens": ([], i32),
                 "k3moe_status_str": ([ctypes.c_int], ctypes.c_char_p),
                 "k3moe_abi_version": ([], i32),
             }
@@ -249,6 +251,24 @@ def set_tc_min_tokens(t: int) -> int:
 def tc_min_tokens() -> int:
     """k3moe_tc_min_tokens: the token count from which the tensor-core GEMMs run."""
     return int(lib().k3moe_tc_min_tokens())
+
+
+def set_tc_split_max_tokens(t: int) -> int:
+    """k3moe_set_tc_split_max_tokens: below t tokens the exact tensor-core expert GEMMs take
+    the bf16 activations as two exact MXFP8 terms on block-scaled MMAs, from t on the SMs
+    decode the weights to bf16 (process-wide; 0 = never split); returns the previous value."""
+    prev = int(lib().k3moe_set_tc_split_max_tokens(int(t)))
+    if prev < 0:
+        raise ValueError("token bound must be >= 0")
+    return prev
+
+
+def tc_split_max_tokens() -> int:
+    """k3moe_tc_split_max_tokens: the token count from which the weight-decode form runs."""
+    return int(lib().k3moe_tc_split_max_tokens())
+
+
+SPLIT_ALWAYS = 1 << 30  # a bound no call reaches: the split form at every token count
 
 
 def selftest_wait_timeout(ws, limit_cycles: int, stream=None):

@@ -58,31 +58,41 @@ constexpr int X8_BK = 128;             // contraction elements per stage
 constexpr int X8_STAGES = 4;
 constexpr int X8_A_BYTES = X8_ROWS * 128;  // shared-memory bytes of one block's stage
 constexpr int X8_A_TX = X8_ROWS * 64;      // bytes the copy reads (packed E2M1)
-constexpr int X8_B_BYTES = X8_NB * 128;
-constexpr int X8_STAGE_BYTES = X8_BLOCKS * X8_A_BYTES + X8_B_BYTES;
-constexpr int X8_EPI = 8;
+constexpr int X8_B_BYTES = X8_NB * 128;     // one activation term's stage (N rows x 128 bytes)
+constexpr int X8_EPI = 16;
 constexpr int X8_SCALE_W0 = 3;
 constexpr int X8_EPI_W0 = X8_SCALE_W0 + 4;
 constexpr int X8_THREADS = (X8_EPI_W0 + X8_EPI) * 32;
 constexpr int X8_PREF = 4;  // stages of scale words in flight per scale writer
 // TMEM columns: accumulators [buffer][block][X8_NB], then per stage SFA block 0 (4),
-// SFA block 1 (4), SFB (4: up to 128 tokens)
+// SFA block 1 (4), SFB of each activation term (4 each: up to 128 tokens)
 constexpr int X8_ACC_COLS = X8_BLOCKS * X8_NB;
 constexpr int X8_SF0 = 2 * X8_ACC_COLS;
-constexpr int X8_SF_COLS = 4 * (X8_BLOCKS + 1);
-static_assert(X8_SF0 + X8_STAGES * X8_SF_COLS <= 512, "TMEM columns");
 static_assert(X8_NB <= 128, "the B scale columns hold 128 tokens");
-constexpr int X8_SMEM = 1024 + X8_STAGES * X8_STAGE_BYTES + 512 + X8_BLOCKS * 2 * 128;
+// SPLIT = 0: one MXFP8 activation term (the lossy variant); SPLIT = 1: two terms hi + lo
+// that hold the bf16 activations exactly (see k3_split_rows_kernel)
+template <int SPLIT>
+struct X8Lay {
+  static constexpr int TERMS = 1 + SPLIT;
+  static constexpr int STAGE_BYTES = X8_BLOCKS * X8_A_BYTES + TERMS * X8_B_BYTES;
+  static constexpr int SF_COLS = 4 * (X8_BLOCKS + TERMS);
+  static constexpr int SMEM = 1024 + X8_STAGES * STAGE_BYTES + 512 + X8_BLOCKS * 2 * 128;
+  static_assert(X8_SF0 + X8_STAGES * SF_COLS <= 512, "TMEM columns");
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+  static_assert(STAGE_BYTES % 1024 == 0 && X8_B_BYTES % 1024 == 0, "128-byte swizzle atoms stay 1024-byte aligned");
+};
 
 struct Mx8Params {
   const MxBatch* batches;   // token batches of up to X8_NB tokens (one expert each)
   const int32_t* n_batches;
   int R;                    // rows per weight matrix (I for gate/up, L for down)
   int K;                    // contraction length (L or I), a multiple of 128, >= 128 * X8_STAGES
-  const uint8_t* act_s;     // activation scale bytes [slots, K / 32] (slot order)
-  int slots;                // rows of the activation operand
-  void* out;                // GATEUP: h codes [slots, R] E4M3; DOWN: o [slots, R] f32
-  uint8_t* out_s;           // GATEUP: h scale bytes [slots, R / 32]
+  // activation terms (one, or hi then lo when split): codes [terms][slots][K] E4M3 (the
+  // operand's tensor map), scale bytes [terms][slots][K / 32], slot order
+  const uint8_t* act_s;
+  int slots;                // slots (rows of one activation term)
+  void* out;                // GATEUP: h codes [terms][slots][R] E4M3; DOWN: o [slots, R] f32
+  uint8_t* out_s;           // GATEUP: h scale bytes [terms][slots][R / 32]
   uint32_t* status;
   void* tmaps;              // packed-weight tensor maps, [TM_MAX_CTAS][X8_BLOCKS][2] x 128 bytes
 };
@@ -104,6 +114,12 @@ K3_DEVI void tc_mma_mx8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_
       "}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
+}
+K3_DEVI void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
 }
 K3_DEVI void tmem_st1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n" ::"r"(taddr), "r"(v) : "memory");
@@ -135,6 +151,94 @@ K3_DEVI uint32_t e4m3x4_codes(float a, float b, float c, float d) {
   const uint32_t lo = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
   const uint32_t hi = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
   return lo | (hi << 16);
+}
+
+// ---------------------------------------------------------------------------- exact two-term split
+// A bf16 value x of a 32-element group is written as x = hi + lo with two MXFP8 terms:
+//   hi: E4M3 codes at the scale 2^(s_hi - 127), the smallest power of two that keeps the
+//       group's largest magnitude within 448 (the OCP shared exponent, raised by one where
+//       that element would saturate), nearest even;
+//   lo: the residual x - hi (exact in fp32) as E4M3 codes at the fixed scale s_lo = s_hi - 4.
+// In units of the hi scale an element of binade 2^k (k >= -6, the normal E4M3 range) has
+// 8 significant bits, hi keeps the top 4 and the residual is a multiple of 2^(k-7) of
+// magnitude at most 2^(k-4) <= 16: 16 times that (its lo value) is at most 256 <= 448 with at
+// most 4 significant bits and a step of at least 2^-9, the finest E4M3 step, so lo holds
+// it exactly and hi + lo == x for every element within 2^14 of the group's largest.  A
+// smaller element is held to within 2^-14 of the hi scale (under 2^-21 of the group's
+// largest), below the fp32 accumulation error of the contraction.  E2M1 x E4M3 products
+// are exact on the tensor core, so the two block-scaled MMAs of a k-block reproduce the
+// bf16 operand's products.
+K3_DEVI uint32_t split_hi_scale(float amax) {
+  uint32_t s = mx8_scale_byte(amax);
+  if (s < 254u && amax * mx8_inv_scale(s) > 448.0f) ++s;
+  return s;
+}
+K3_DEVI uint32_t split_lo_scale(uint32_t s_hi) { return s_hi >= 4u ? s_hi - 4u : 0u; }
+// E4M3 code -> its value (exact in f32)
+K3_DEVI float e4m3_value(uint32_t code) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
+  return __half2float(__half(h));
+}
+// 2^(s - 127) for a scale byte s (2^-127 is an f32 subnormal)
+K3_DEVI float e8m0_value(uint32_t s) { return s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u); }
+// one element: codes of hi and lo at the group's scales (inv_hi = 2^(127 - s_hi), sc_hi =
+// 2^(s_hi - 127), inv_lo = 2^(127 - s_lo))
+K3_DEVI void split_elem(float x, float inv_hi, float sc_hi, float inv_lo, uint32_t& c_hi, uint32_t& c_lo) {
+  c_hi = e4m3_code(x * inv_hi);
+  const float r = x - e4m3_value(c_hi) * sc_hi;  // exact
+  c_lo = e4m3_code(r * inv_lo);
+}
+
+// z rows (bf16, token order) -> the two split terms in slot order: codes [2][slots][L]
+// (hi rows, then lo rows), scale bytes [2][slots][L / 32].  One thread per 32-element group.
+__global__ void __launch_bounds__(256) k3_split_rows_kernel(const uint16_t* __restrict__ z,
+                                                            const int32_t* __restrict__ slot_tok,
+                                                            const int32_t* __restrict__ n_placed, int slots, int L,
+                                                            uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int G = L / 32;
+  const int np = min(*n_placed, slots);
+  const size_t total = (size_t)np * G;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int slot = (int)(i / G), g = (int)(i % G);
+    const int t = __ldg(slot_tok + slot);
+    const uint4* src = reinterpret_cast<const uint4*>(z + (size_t)t * L + g * 32);
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = __ldg(src + j);
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(v);
+    float x[32];
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      x[2 * j] = __uint_as_float(w[j] << 16);
+      x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      amax = fmaxf(amax, fmaxf(fabsf(x[2 * j]), fabsf(x[2 * j + 1])));
+    }
+    const uint32_t s_hi = split_hi_scale(amax), s_lo = split_lo_scale(s_hi);
+    const float inv_hi = mx8_inv_scale(s_hi), sc_hi = e8m0_value(s_hi), inv_lo = mx8_inv_scale(s_lo);
+    uint32_t ch[8], cl[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      ch[j] = cl[j] = 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        uint32_t a, b;
+        split_elem(x[4 * j + e], inv_hi, sc_hi, inv_lo, a, b);
+        ch[j] |= a << (8 * e);
+        cl[j] |= b << (8 * e);
+      }
+    }
+    uint4* dh = reinterpret_cast<uint4*>(codes + (size_t)slot * L + g * 32);
+    uint4* dl = reinterpret_cast<uint4*>(codes + ((size_t)slots + slot) * L + g * 32);
+    dh[0] = make_uint4(ch[0], ch[1], ch[2], ch[3]);
+    dh[1] = make_uint4(ch[4], ch[5], ch[6], ch[7]);
+    dl[0] = make_uint4(cl[0], cl[1], cl[2], cl[3]);
+    dl[1] = make_uint4(cl[4], cl[5], cl[6], cl[7]);
+    scales[(size_t)slot * G + g] = (uint8_t)s_hi;
+    scales[((size_t)slots + slot) * G + g] = (uint8_t)s_lo;
+  }
 }
 
 // z rows (bf16, token order) -> MXFP8 rows in slot order: codes [slots, L], scale bytes
@@ -177,21 +281,23 @@ __global__ void __launch_bounds__(256) k3_gather_mx8_kernel(const uint16_t* __re
 }
 
 // ---------------------------------------------------------------------------- grouped GEMM
-template <int MODE>
+template <int MODE, int SPLIT>
 __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_constant__ CUtensorMap mapB,
                                                                    const __grid_constant__ CUtensorMap mapA,
                                                                    Mx8Params p) {
+  using Lay = X8Lay<SPLIT>;
+  constexpr int TERMS = Lay::TERMS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;  // stage s: A block 0, A block 1, B
+  const uint32_t base = (raw + 1023u) & ~1023u;  // stage s: A block 0, A block 1, B term(s)
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t bars = base + X8_STAGES * X8_STAGE_BYTES;
+  const uint32_t bars = base + X8_STAGES * Lay::STAGE_BYTES;
   const uint32_t smaps = bars + 512;  // [X8_BLOCKS][128 bytes] tensor-map images
-  auto stage_a = [&](int s, int b) { return base + s * X8_STAGE_BYTES + b * X8_A_BYTES; };
-  auto stage_b = [&](int s) { return base + s * X8_STAGE_BYTES + X8_BLOCKS * X8_A_BYTES; };
+  auto stage_a = [&](int s, int b) { return base + s * Lay::STAGE_BYTES + b * X8_A_BYTES; };
+  auto stage_b = [&](int s, int t) { return base + s * Lay::STAGE_BYTES + X8_BLOCKS * X8_A_BYTES + t * X8_B_BYTES; };
   // full(s): the stage's copies landed (the load thread's arrival with the byte count) and
   // the four scale writers stored its scale words; kdone(s): both issuers' MMAs of the
   // stage completed (frees its shared memory and scale columns); tfull / tempty: the
@@ -239,7 +345,7 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
   auto blk_row0 = [](int tm, int b) {
     return (MODE == 0) ? tm * X8_ROWS : tm * (X8_BLOCKS * X8_ROWS) + b * X8_ROWS;
   };
-  auto sf_col = [&](int s) { return tmem + X8_SF0 + s * X8_SF_COLS; };
+  auto sf_col = [&](int s) { return tmem + X8_SF0 + s * Lay::SF_COLS; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ loads
@@ -291,12 +397,14 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
         tm = tile % mtiles;
       }
       if (lane == 0) {
-        mbar_expect_tx(full(s), X8_BLOCKS * X8_A_TX + X8_B_BYTES);
+        mbar_expect_tx(full(s), X8_BLOCKS * X8_A_TX + TERMS * X8_B_BYTES);
 #pragma unroll
         for (int b = 0; b < X8_BLOCKS; ++b)
           tma_load_2d(stage_a(s, b), reinterpret_cast<const CUtensorMap*>(gmap(b, par)), ks * X8_BK, blk_row0(tm, b),
                       full(s));
-        tma_load_2d(stage_b(s), &mapB, ks * X8_BK, slot0, full(s));
+        // term t's rows start at row t * slots of the operand
+#pragma unroll
+        for (int t = 0; t < TERMS; ++t) tma_load_2d(stage_b(s, t), &mapB, ks * X8_BK, t * p.slots + slot0, full(s));
       }
       issued = j + 1;
     }
@@ -314,7 +422,7 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
     // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       const int mm = warp - 1;
-      const uint64_t dA0 = sdesc_sw128(stage_a(0, mm)), dB0 = sdesc_sw128(stage_b(0));
+      const uint64_t dA0 = sdesc_sw128(stage_a(0, mm)), dB0 = sdesc_sw128(stage_b(0, 0));
       int j = 0, lt = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++lt) {
@@ -331,12 +439,16 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
             break;
           }
           tc_fence_after();
-          const uint64_t da = dA0 + ((uint32_t)(s * X8_STAGE_BYTES) >> 4);
-          const uint64_t db = dB0 + ((uint32_t)(s * X8_STAGE_BYTES) >> 4);
+          const uint64_t da = dA0 + ((uint32_t)(s * Lay::STAGE_BYTES) >> 4);
+          const uint64_t db = dB0 + ((uint32_t)(s * Lay::STAGE_BYTES) >> 4);
           const uint32_t sfa = sf_col(s) + 4 * mm, sfb = sf_col(s) + 4 * X8_BLOCKS;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
+          for (int kk = 0; kk < 4; ++kk) {
             tc_mma_mx8(d, da + 2 * kk, db + 2 * kk, idesc_mx8(N, kk), sfa, sfb, (ks | kk) != 0);
+            // the lo term: same weights, its own rows and scale columns, same accumulator
+            if (SPLIT)
+              tc_mma_mx8(d, da + 2 * kk, db + (X8_B_BYTES >> 4) + 2 * kk, idesc_mx8(N, kk), sfa, sfb + 4, 1u);
+          }
           tc_commit(kdone(s));
         }
         if (!ok) break;
@@ -354,7 +466,8 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
     const int q = warp & 3;
     const int KB = p.K / 32;  // scale bytes per row
     const uint32_t tq = (uint32_t)(q * 32) << 16;
-    auto load = [&](int j, uint32_t (&w)[5]) {
+    constexpr int W = 2 + 3 * TERMS;  // SFA of both blocks, then 3 words of SFB per term
+    auto load = [&](int j, uint32_t (&w)[W]) {
       if (j >= nst) return;
       const int tile = blockIdx.x + (j / kst) * gridDim.x, ks = j % kst;
       const MxBatch* rec = p.batches + tile / mtiles;
@@ -366,14 +479,17 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
       }
       const int n = rec->n, slot0 = rec->slot0;
 #pragma unroll
-      for (int c = 0; c < 3; ++c) {
-        const int col = c * 32 + lane;
-        w[2 + c] = (col < n && slot0 + col < p.slots)
-                       ? __ldg(reinterpret_cast<const uint32_t*>(p.act_s + (size_t)(slot0 + col) * KB + 4 * ks))
-                       : 0x7F7F7F7Fu;  // columns past the batch: scale 1, outputs unused
-      }
+      for (int t = 0; t < TERMS; ++t)
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+          const int col = c * 32 + lane;
+          w[2 + 3 * t + c] =
+              (col < n && slot0 + col < p.slots)
+                  ? __ldg(reinterpret_cast<const uint32_t*>(p.act_s + ((size_t)t * p.slots + slot0 + col) * KB + 4 * ks))
+                  : 0x7F7F7F7Fu;  // columns past the batch: scale 1, outputs unused
+        }
     };
-    uint32_t ring[X8_PREF][5];
+    uint32_t ring[X8_PREF][W];
 #pragma unroll
     for (int u = 0; u < X8_PREF - 1; ++u) load(u, ring[u]);
     bool ok = true;
@@ -395,6 +511,7 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
         tmem_st1(c0 + q, ring[u][0]);
         tmem_st1(c0 + 4 + q, ring[u][1]);
         tmem_st4(c0 + 8, ring[u][2], ring[u][3], ring[u][4], 0x7F7F7F7Fu);
+        if constexpr (SPLIT) tmem_st4(c0 + 12, ring[u][5], ring[u][6], ring[u][7], 0x7F7F7F7Fu);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -402,9 +519,11 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 7..14)
-    // warp w reads TMEM lane quarter w % 4 (32 weight rows of each block) and the 16-token
-    // chunks e, e + 2, ... of the batch (e = 0 for warps 7..10, 1 for 11..14)
+    // ------------------------------------------------------------ epilogue (warps 7..22)
+    // warp w reads TMEM lane quarter w % 4 (32 weight rows of each block) and the 8-token
+    // chunks e, e + 4, ... of the batch (e = (w - 7) / 4): four warps per lane quarter share
+    // a tile's tokens within one chunk of each other (gate/up: SiTU-GLU and the MXFP8
+    // encoding are most of the epilogue's work)
     const int q = warp & 3;
     const int e0 = (warp - X8_EPI_W0) >> 2;
     int lt = 0;
@@ -417,33 +536,46 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
       const int tm = tile % mtiles;
       const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + buf * X8_ACC_COLS;
 #pragma unroll 1
-      for (int c = e0; c * 16 < n; c += 2) {
-        uint32_t r0[16], r1[16];
-        tmem_ld16(tq + c * 16, r0);
-        tmem_ld16(tq + X8_NB + c * 16, r1);
+      for (int c = e0; c * 8 < n; c += X8_EPI / 4) {
+        uint32_t r0[8], r1[8];
+        tmem_ld8(tq + c * 8, r0);
+        tmem_ld8(tq + X8_NB + c * 8, r1);
         tmem_ld_wait();
         if (MODE == 0) {
-          // h of feature `feat` for 16 tokens; the 32 features of the warp are one MXFP8 group
+          // h of feature `feat` for 8 tokens; the 32 features of the warp are one MXFP8 group
           const int feat = tm * X8_ROWS + q * 32 + lane;
           uint8_t* hq = reinterpret_cast<uint8_t*>(p.out);
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int col = c * 16 + jj;  // warp-uniform
+          for (int jj = 0; jj < 8; ++jj) {
+            const int col = c * 8 + jj;  // warp-uniform
+            if (col >= n) break;
             const float h = bf16_bits_to_f32(f32_to_bf16_bits(situ_fast(__uint_as_float(r0[jj]), __uint_as_float(r1[jj]))));
             // largest |h| of the group: the bit patterns of non-negative floats order as integers
             const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
-            const uint32_t sb = mx8_scale_byte(m);
-            const uint32_t code = e4m3_code(h * mx8_inv_scale(sb));
-            if (col < n) {
-              hq[(size_t)(slot0 + col) * p.R + feat] = (uint8_t)code;
-              if (lane == 0) p.out_s[(size_t)(slot0 + col) * (p.R / 32) + (feat >> 5)] = (uint8_t)sb;
+            const size_t slot = (size_t)(slot0 + col);
+            if constexpr (SPLIT) {
+              // h exactly as two terms (hi rows, then lo rows p.slots further on)
+              const uint32_t sh = split_hi_scale(m), sl = split_lo_scale(sh);
+              uint32_t ch, cl;
+              split_elem(h, mx8_inv_scale(sh), e8m0_value(sh), mx8_inv_scale(sl), ch, cl);
+              hq[slot * p.R + feat] = (uint8_t)ch;
+              hq[((size_t)p.slots + slot) * p.R + feat] = (uint8_t)cl;
+              if (lane == 0) {
+                p.out_s[slot * (p.R / 32) + (feat >> 5)] = (uint8_t)sh;
+                p.out_s[((size_t)p.slots + slot) * (p.R / 32) + (feat >> 5)] = (uint8_t)sl;
+              }
+            } else {
+              const uint32_t sb = mx8_scale_byte(m);
+              const uint32_t code = e4m3_code(h * mx8_inv_scale(sb));
+              hq[slot * p.R + feat] = (uint8_t)code;
+              if (lane == 0) p.out_s[slot * (p.R / 32) + (feat >> 5)] = (uint8_t)sb;
             }
           }
         } else {
           const int row0 = tm * (X8_BLOCKS * X8_ROWS) + q * 32 + lane;
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int col = c * 16 + jj;
+          for (int jj = 0; jj < 8; ++jj) {
+            const int col = c * 8 + jj;
             if (col < n) {
               float* o = reinterpret_cast<float*>(p.out) + (size_t)(slot0 + col) * p.R + row0;
               o[0] = __uint_as_float(r0[jj]);

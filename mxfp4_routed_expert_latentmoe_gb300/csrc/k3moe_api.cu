@@ -23,9 +23,14 @@ constexpr float kTieTau = 3e-5f;
 constexpr int kMaxDevices = 64;
 constexpr int kTcMinTokensDefault = 9;  // measured crossover on GB300 at K3 shapes (bench.py --sweep)
 constexpr int kSplitKMaxT = 512;        // the projections split K only when they have few output tiles
+// exact tensor-core experts: two-term MXFP8 split below this many tokens, bf16 weight decode
+// from it on (measured on GB300 at K3 shapes: 3072 tokens 5226 us split against 5258 us
+// decode, 3584 tokens 5621 us against 5418 us; bench.py --sweep)
+constexpr int kSplitMaxTokensDefault = 3328;
 
 size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 int tc_min_t();
+bool split_experts(const k3moe_dims& d, int T);
 
 struct WsLayout {
   size_t status, logits, ids, w, zmax, zpow, counts, offsets, slot_of, slot_tok, inv, uniq, n_uniq, nb_prefix,
@@ -71,14 +76,18 @@ WsLayout ws_layout(const k3moe_dims& d, int T) {
   L.batches = take((slots / 8 + 1 + (E < slots ? E : slots)) * sizeof(MxBatch));
   L.z = take(Tz * Lt * 2);
   L.z16 = take(Tz * Lt * 2);
-  L.h16 = take(slots * I * 2);
+  // bf16 h (weight-decode path), or the h codes and scale bytes of the MXFP8 variant (one
+  // term) or of the exact split (two terms: 2 slots I codes + 2 slots I / 32 scale bytes)
+  const bool split = split_experts(d, T);
+  L.h16 = take(slots * I * 2 + (split ? slots * I / 16 : 0));
   L.o = take(slots * Lt * 4);
   L.y = take(Tz * Lt * 4);
   L.yhat = take(Tz * Lt * 2);
   L.cpart = take(Tz * COMB_MAX_SPLIT * 4);
   // slot-order bf16 activation rows for the tensor-core expert path (large T only)
   const bool tc = T >= tc_min_t();
-  L.act = take(tc ? slots * Lt * 2 : 0);
+  // (bf16 rows; or the variant's codes and scale bytes; or the split's two terms of each)
+  L.act = take(tc ? slots * Lt * 2 + (split ? slots * Lt / 16 : 0) : 0);
   L.tmaps = take(tc ? (size_t)TM_MAX_CTAS * TM_BLOCKS * 2 * 128 : 0);  // packed-weight tensor maps
   // split-K partial sums of the projections (few tokens on the tensor-core path)
   L.part_bytes = (tc && T <= kSplitKMaxT) ? (size_t)8 * T * std::max<size_t>((size_t)E + Lt, d.hidden) * 4 : 0;
@@ -292,6 +301,17 @@ constexpr int kCombRowMinT = 256;
 // needs both expert contraction lengths to be multiples of 256; other shapes keep the
 // weight-streaming kernels at every T
 bool tc_experts(const k3moe_dims& d, int T) { return T >= tc_min_t() && d.latent % 256 == 0 && d.inter % 256 == 0; }
+// operand form of the exact grouped GEMM: below g_split_max_t tokens (process-wide,
+// k3moe_set_tc_split_max_tokens) the bf16 activations are split exactly into two MXFP8
+// terms for block-scaled MMAs over the stored weights (k3_mx8_moe_kernel<.., 1>); from it
+// on the SMs decode the weights to bf16 (k3_tc_moe_kernel), which wins once the batches
+// hold enough tokens per expert to amortise the decode.  The split needs both contraction
+// lengths >= 512.
+std::atomic<int> g_split_max_t{kSplitMaxTokensDefault};
+bool split_experts(const k3moe_dims& d, int T) {
+  return T < g_split_max_t.load(std::memory_order_relaxed) && !d.act_mxfp8 && tc_experts(d, T) &&
+         d.latent >= X8_BK * X8_STAGES && d.inter >= X8_BK * X8_STAGES;
+}
 
 // grouped MXFP4 expert GEMM on tcgen05; act [slots, K] f16 in slot order
 template <int MODE>
@@ -308,16 +328,18 @@ cudaError_t launch_tc_moe(const uint16_t* act, int slots, TcMoeParams p, int dev
 }
 
 // grouped expert GEMM of the MXFP8-activation variant; act [slots, K] E4M3 codes in slot order
-template <int MODE>
+template <int MODE, int SPLIT>
 cudaError_t launch_mx8_moe(const uint8_t* act, Mx8Params p, int dev, int sms, cudaStream_t st, bool pdl) {
   CUtensorMap mb, ma;
-  if (!map_u8(&mb, act, (uint64_t)p.slots, (uint64_t)p.K, X8_NB)) return cudaErrorInvalidValue;
+  // the activation terms' rows, one after the other
+  if (!map_u8(&mb, act, (uint64_t)(1 + SPLIT) * p.slots, (uint64_t)p.K, X8_NB)) return cudaErrorInvalidValue;
   // template of the weight maps ([R, K] E2M1): the kernel writes each expert tensor's address
   // into its copies; the (256-byte aligned) workspace stands in until then
   if (!map_e2m1(&ma, p.tmaps, (uint64_t)p.R, (uint64_t)p.K)) return cudaErrorInvalidValue;
-  if (!set_smem<k3_mx8_moe_kernel<MODE>>(dev, X8_SMEM)) return cudaErrorInvalidValue;
+  constexpr int smem = X8Lay<SPLIT>::SMEM;
+  if (!set_smem<k3_mx8_moe_kernel<MODE, SPLIT>>(dev, smem)) return cudaErrorInvalidValue;
   const int grid = sms < TM_MAX_CTAS ? sms : TM_MAX_CTAS;
-  return launch(k3_mx8_moe_kernel<MODE>, dim3(grid), dim3(X8_THREADS), X8_SMEM, st, pdl, mb, ma, p);
+  return launch(k3_mx8_moe_kernel<MODE, SPLIT>, dim3(grid), dim3(X8_THREADS), smem, st, pdl, mb, ma, p);
 }
 
 // D[M, N0 (+N1)] = A[M, K] . [B0; B1]^T on tcgen05 (A, B bf16 row-major)
@@ -643,6 +665,7 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   tp.ids = at<int32_t>(ws, L.ids); tp.w = at<float>(ws, L.w); tp.ids_out = ids_out; tp.w_out = w_out;
   tp.status = status;
   const bool tc = tc_experts(d, T);
+  const bool split = split_experts(d, T);
   const int nblk = mx_nblk(T);
   const int NB = tc ? TM_NB : 8 * nblk;  // tokens per expert batch
   const PermParams pp = perm_params(d, T, d.top_k, at<int32_t>(ws, L.ids), 0, NB, ws, L, experts);
@@ -689,15 +712,17 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
       // grouped GEMM (the f16 copy of z that the weight-streaming kernels read is not needed)
       K3_TRY(launch_topk(tp, dev, s, pdl));
       K3_TRY(launch_permute(pp, dev, s, pdl));
-      if (d.act_mxfp8) {
-        // z quantized to MXFP8 rows in slot order (codes, then the scale bytes)
+      if (d.act_mxfp8 || split) {
+        // z in slot order as MXFP8 rows (codes, then the scale bytes): one term (the
+        // variant's quantization) or the two exact split terms
         uint8_t* a8 = at<uint8_t>(ws, L.act);
         const size_t groups = (size_t)slots * (d.latent / 32);
         const int gblocks = (int)((groups + 255) / 256 < (size_t)sms * 8 ? (groups + 255) / 256 : (size_t)sms * 8);
-        K3_TRY(launch(k3_gather_mx8_kernel, dim3(gblocks), dim3(256), 0, s, pdl, (const uint16_t*)at<uint16_t>(ws, L.z),
-                      (const int32_t*)at<int32_t>(ws, L.slot_tok),
+        const int terms = split ? 2 : 1;
+        K3_TRY(launch(split ? k3_split_rows_kernel : k3_gather_mx8_kernel, dim3(gblocks), dim3(256), 0, s, pdl,
+                      (const uint16_t*)at<uint16_t>(ws, L.z), (const int32_t*)at<int32_t>(ws, L.slot_tok),
                       (const int32_t*)(at<int32_t>(ws, L.offsets) + d.n_experts), slots, (int)d.latent, a8,
-                      a8 + (size_t)slots * d.latent));
+                      a8 + (size_t)terms * slots * d.latent));
       } else {
         // bf16 rows in slot order (interleaved K order)
         const int per = d.latent / 8;
@@ -714,18 +739,31 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   }
   K3_TRY(mark(events, n_events, 2, s));
   // experts
-  if (tc && d.act_mxfp8) {
+  if (split) {
+    // exact: the bf16 z and h as two MXFP8 terms each, block-scaled MMAs on the stored
+    // MXFP4 weights (terms' codes [2][slots][K], then their scale bytes [2][slots][K / 32])
+    const uint8_t* a8 = at<uint8_t>(ws, L.act);
+    uint8_t* h8 = at<uint8_t>(ws, L.h16);
+    Mx8Params gp{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.inter, d.latent,
+                 a8 + (size_t)2 * slots * d.latent, slots, h8, h8 + (size_t)2 * slots * d.inter, status,
+                 at<void>(ws, L.tmaps)};
+    K3_TRY((launch_mx8_moe<0, 1>(a8, gp, dev, sms, s, pdl)));
+    K3_TRY(mark(events, n_events, 3, s));
+    Mx8Params dp2{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.latent, d.inter,
+                  h8 + (size_t)2 * slots * d.inter, slots, at<void>(ws, L.o), nullptr, status, at<void>(ws, L.tmaps)};
+    K3_TRY((launch_mx8_moe<1, 1>(h8, dp2, dev, sms, s, pdl)));
+  } else if (tc && d.act_mxfp8) {
     // MXFP8 activations, block-scaled MMAs on the stored MXFP4 weights; h leaves the gate/up
     // epilogue as MXFP8 rows in slot order (codes, then the scale bytes)
     const uint8_t* a8 = at<uint8_t>(ws, L.act);
     uint8_t* h8 = at<uint8_t>(ws, L.h16);
     Mx8Params gp{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.inter, d.latent,
                  a8 + (size_t)slots * d.latent, slots, h8, h8 + (size_t)slots * d.inter, status, at<void>(ws, L.tmaps)};
-    K3_TRY(launch_mx8_moe<0>(a8, gp, dev, sms, s, pdl));
+    K3_TRY((launch_mx8_moe<0, 0>(a8, gp, dev, sms, s, pdl)));
     K3_TRY(mark(events, n_events, 3, s));
     Mx8Params dp2{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.latent, d.inter,
                   h8 + (size_t)slots * d.inter, slots, at<void>(ws, L.o), nullptr, status, at<void>(ws, L.tmaps)};
-    K3_TRY(launch_mx8_moe<1>(h8, dp2, dev, sms, s, pdl));
+    K3_TRY((launch_mx8_moe<1, 0>(h8, dp2, dev, sms, s, pdl)));
   } else if (tc) {
     TcMoeParams gp{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.inter, d.latent,
                    at<void>(ws, L.h16), status, at<void>(ws, L.tmaps)};
@@ -933,6 +971,13 @@ int32_t k3moe_set_tc_min_tokens(int32_t t) {
 
 int32_t k3moe_tc_min_tokens(void) { return tc_min_t(); }
 
+int32_t k3moe_set_tc_split_max_tokens(int32_t t) {
+  if (t < 0) return -1;
+  return g_split_max_t.exchange(t);
+}
+
+int32_t k3moe_tc_split_max_tokens(void) { return g_split_max_t.load(std::memory_order_relaxed); }
+
 k3moe_status k3moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_cycles, void* stream) {
   if (!ws || ws_bytes < 256 || limit_cycles <= 0 || limit_cycles > (1ll << 32)) return K3MOE_ERR_ARG;
   if (!a16(ws)) return K3MOE_ERR_ALIGN;
@@ -956,10 +1001,17 @@ void* k3moe_workspace_view(const k3moe_dims* dims, int32_t T, void* ws, int32_t 
     case 3: return at<void>(ws, L.logits);
     case 4: return at<void>(ws, L.h16);
     case 5: return at<void>(ws, L.o);
-    case 6: return dims->act_mxfp8 ? at<void>(ws, L.act) : nullptr;
-    case 7: return dims->act_mxfp8 ? at<uint8_t>(ws, L.act) + (size_t)T * dims->top_k * dims->latent : nullptr;
-    case 8: return dims->act_mxfp8 ? at<void>(ws, L.h16) : nullptr;
-    case 9: return dims->act_mxfp8 ? at<uint8_t>(ws, L.h16) + (size_t)T * dims->top_k * dims->inter : nullptr;
+    default: break;
+  }
+  // MXFP8 rows: the variant's one term, or the exact split's two (hi rows, then lo rows)
+  const size_t terms = dims->act_mxfp8 ? 1 : (split_experts(*dims, T) ? 2 : 0);
+  if (!terms) return nullptr;
+  const size_t slots = (size_t)T * dims->top_k;
+  switch (which) {
+    case 6: return at<void>(ws, L.act);
+    case 7: return at<uint8_t>(ws, L.act) + terms * slots * dims->latent;
+    case 8: return at<void>(ws, L.h16);
+    case 9: return at<uint8_t>(ws, L.h16) + terms * slots * dims->inter;
     default: return nullptr;
   }
 }

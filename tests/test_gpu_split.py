@@ -1,0 +1,93 @@
+"""GPU: the exact split form of the tensor-core expert GEMMs (below
+k3moe_tc_split_max_tokens tokens).  The bf16 activations z and h reach the block-scaled MMAs as two MXFP8 terms
+x = hi + lo per 32-element group: hi at the smallest E8M0 scale that keeps the group's
+largest magnitude within 448 (the E4M3 maximum), lo -- the residual -- at that scale times
+2^-4.  Checked on the terms the library wrote, against the definitions restated here:
+the two scale rules; hi + lo == x exactly for every element within 2^14 of its group's
+largest and within 2^-21 of the group's largest for the others (the error bound stated in
+the library's header); h's terms sum to bf16 values.  The products with the terms are those
+of the exact path, which the parity tests check through the outputs."""
+import numpy as np
+import pytest
+
+import oracle
+from datagen import configs as C
+from tests.test_gpu_parity import Layer, _slot_map, _ws_view, split_terms
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def k3():
+    import __graft_entry__ as g
+    g.build()
+    import mxfp4_routed_expert_latentmoe_gb300 as mod
+    torch.cuda.set_device(0)
+    return mod
+
+
+@pytest.fixture(scope="module")
+def prefill(k3):
+    L = Layer(k3, C.PREFILL)
+    yield L
+    del L
+    torch.cuda.empty_cache()
+
+
+def smallest_scale_within_448(amax):
+    """Per group: the smallest scale byte s (0..254) with amax <= 448 * 2^(s - 127); 0 for a
+    group of zeros.  Searched directly from a frexp estimate."""
+    s = np.zeros(amax.shape, np.int64)
+    nz = amax > 0
+    _, ex = np.frexp(amax[nz])
+    c = ex.astype(np.int64) + 127 - 9  # 448 < 2^9
+    lim = lambda c: 448.0 * np.exp2(c.astype(np.float64) - 127)
+    for _ in range(4):
+        c = np.where(amax[nz] > lim(c), c + 1, c)
+    for _ in range(4):
+        c = np.where((c > 0) & (amax[nz] <= lim(c - 1)), c - 1, c)
+    s[nz] = np.clip(c, 0, 254)
+    return s
+
+
+def _check_terms(x, hi, lo, s_hi, s_lo, what):
+    rows, width = x.shape
+    amax = np.abs(x).reshape(rows, width // 32, 32).max(-1)
+    assert np.array_equal(s_hi.astype(np.int64), smallest_scale_within_448(amax)), what
+    assert np.array_equal(s_lo.astype(np.int64), np.maximum(s_hi.astype(np.int64) - 4, 0)), what
+    rec = hi + lo
+    A = np.repeat(amax, 32, axis=1)
+    inside = np.abs(x) >= A * 2.0 ** -14
+    assert np.array_equal(rec[inside], x[inside]), what
+    assert np.all(np.abs(rec - x)[~inside] <= A[~inside] * 2.0 ** -21), what
+    return float(np.mean(~inside))
+
+
+@pytest.mark.parametrize("T", [9, 300])
+def test_split_terms_hold_z_and_h(k3, prefill, T):
+    """9 tokens (the smallest tensor-core batch) and 300 (ragged tiles): z's terms against
+    the GPU's own z rows in slot order; h's terms sum to bf16 values, exactly h where
+    inside the range (the grouped GEMM's h is compared with the oracle's by the parity
+    tests)."""
+    cfg = C.PREFILL.with_tokens(T, x_seed=41 + T)
+    L = prefill.with_tokens(k3, cfg)
+    assert k3.tc_min_tokens() <= T < k3.tc_split_max_tokens()
+    got, ids, w, ws = L.forward(k3)
+    assert k3.device_status(ws) == 0
+    Lt, I, K = cfg.latent, cfg.inter, cfg.top_k
+    slots = T * K
+    z = _ws_view(k3, L, ws, 0, T, T * Lt, torch.bfloat16).reshape(T, Lt)
+    _, s_tok, _ = _slot_map(ids, cfg.n_experts)
+    hi, lo, s_hi, s_lo = split_terms(k3, L, ws, 6, 7, slots, Lt)
+    frac_z = _check_terms(z[s_tok].astype(np.float64), hi, lo, s_hi, s_lo, "z")
+    # h: the GPU's bf16 h is not stored on this form; its terms' sum is it inside the range,
+    # so there it must be a bf16 value, and the largest of each group (inside) fixes the scales
+    hi, lo, s_hi, s_lo = split_terms(k3, L, ws, 8, 9, slots, I)
+    h = hi + lo
+    frac_h = _check_terms(h, hi, lo, s_hi, s_lo, "h")
+    amax = np.repeat(np.abs(h).reshape(slots, I // 32, 32).max(-1), 32, axis=1)
+    inside = np.abs(h) >= amax * 2.0 ** -14
+    assert np.array_equal(oracle.round_bf16(h[inside]), h[inside])
+    print(f"T={T}: elements below 2^-14 of their group's largest: z {frac_z:.1e}, h {frac_h:.1e}")
