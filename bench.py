@@ -104,7 +104,7 @@ def selected_cfgs(a):
     return out
 
 
-def kernels_per_step(cfg, tc: bool) -> int:
+def kernels_per_step(cfg, tc: bool, split_max: int = 1 << 30) -> int:
     """Kernel launches of one forward (the memsets are not kernels): for one token the
     router GEMV, then the routing and the latent down projection in one kernel (6 in all);
     up to 64 tokens the routing
@@ -117,7 +117,13 @@ def kernels_per_step(cfg, tc: bool) -> int:
     if not tc and cfg.T <= 64:
         return 6
     perm = 4 if cfg.T * cfg.top_k > 2 * 2048 else 1
-    return 7 + perm + (splitk_reductions(cfg) if tc else 0)
+    return 7 + perm + (splitk_reductions(cfg) + split_form(cfg, split_max) if tc else 0)
+
+
+def split_form(cfg, split_max: int) -> bool:
+    """The exact tensor-core experts take the two-term MXFP8 split below split_max tokens
+    (k3moe_tc_split_max_tokens; one more launch: h's terms between the two GEMMs)."""
+    return (cfg.T < split_max and not cfg.act_mxfp8 and cfg.latent >= 512 and cfg.inter >= 512)
 
 
 def splitk_reductions(cfg, sms: int = 152) -> int:
@@ -611,7 +617,7 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
         else:
             roof = {"bound": "hbm", "achieved": gb, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": f_h,
                     "peak_kind": f"{peak_kind} HBM copy", "other_bound_frac": f_t}
-        split = cfg.T < k3.tc_split_max_tokens() and cfg.latent >= 512 and cfg.inter >= 512
+        split = split_form(cfg, k3.tc_split_max_tokens())
         roof.update({"traffic": profiled_traffic(dom, cfg.name),
                      "kernel": "k3_mx8_moe_kernel<0, 1> (gate/up, exact two-term split)" if split
                      else "k3_tc_moe_kernel<0> (gate/up, bf16 weight decode)",
@@ -642,7 +648,7 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
            "expert_phase": {"us": expert_us, "GB_s": exp_bytes / (expert_us / 1e6) / 1e9,
                             "frac_hbm": exp_bytes / (expert_us / 1e6) / 1e9 / peaks["hbm_gbs"]},
            "phases": phases, "profiled_ms_per_step": profiled_ms, "e2e": e2e,
-           "gpu_launches": kernels_per_step(cfg, tc) * a.steps, "device_status": status,
+           "gpu_launches": kernels_per_step(cfg, tc, k3.tc_split_max_tokens()) * a.steps, "device_status": status,
            "_window": (w0, w1)}
     return res
 

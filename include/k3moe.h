@@ -253,16 +253,16 @@ int32_t k3moe_set_tc_min_tokens(int32_t t);
 int32_t k3moe_tc_min_tokens(void);
 
 /* Operand form of the exact tensor-core expert GEMMs (act_mxfp8 = 0, T >=
- * k3moe_tc_min_tokens), by token count.  Below t tokens (default 3328, the crossover
- * measured on GB300 at K3 shapes) the bf16 activations z and h are each split into two
+ * k3moe_tc_min_tokens), by token count.  Below t tokens (default 2^30: every count; on
+ * GB300 at K3 shapes the split form measured faster from 9 to 8192 tokens, e.g. the 4096-
+ * token forward 4.85 ms against 5.78 ms) the bf16 activations z and h are each split into two
  * MXFP8 terms, x = hi + lo (hi: E4M3 at the smallest power-of-two scale per 32 elements
  * that keeps the group's largest within 448; lo: the residual x - hi at a scale 2^-4 of
  * hi's), which holds every element within 2^14 of its group's largest exactly and the rest
  * to within 2^-21 of the group's largest; two block-scaled MMAs per k-block then read the
  * E2M1 weights and E8M0 scales as stored (E2M1 x E4M3 products are exact), so no weight
  * decode runs on the SMs.  From t tokens on (and for latent or inter < 512) the SMs decode
- * the weights exactly to bf16 and the MMAs read the bf16 activations; with many tokens per
- * expert the decode is amortised and that form is faster.  t = 0: never split.
+ * the weights exactly to bf16 and the MMAs read the bf16 activations.  t = 0: never split.
  * Process-wide like k3moe_set_tc_min_tokens (it changes the workspace size): set it before
  * sizing workspaces, with no call in flight.  Returns the previous value, or -1 for t < 0
  * (nothing changed). */
@@ -283,12 +283,14 @@ k3moe_status k3moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limi
  * 0 = z [T, L] bf16, 1 = yhat [T, L] bf16, 2 = y [T, L] f32 (combined, before the
  * norm), 3 = logits [T, E] f32, 4 = h [T*K, I] in expert-sorted slot order (on the
  * weight-decode tensor-core path: bf16 with the 8 elements of each group stored in the
- * order 0, 4, 1, 5, 2, 6, 3, 7; on the weight-streaming GEMVs: f16 holding h * 2^8; on the
- * MXFP8 paths: see 8), 5 = o [T*K, L] f32 in expert-sorted slot order.  When the expert
+ * order 0, 4, 1, 5, 2, 6, 3, 7; on the split form: bf16 in natural order; on the
+ * weight-streaming GEMVs: f16 holding h * 2^8; on the MXFP8 variant: see 8), 5 = o
+ * [T*K, L] f32 in expert-sorted slot order.  When the expert
  * GEMMs read MXFP8 rows (the act_mxfp8 variant: one term; the exact split form: two terms,
  * hi rows then lo rows), 6 = the z codes [terms][T*K][L] E4M3 in slot order, 7 = their
- * scale bytes [terms][T*K][L/32] E8M0, 8 = the h codes [terms][T*K][I], 9 = their scale
- * bytes [terms][T*K][I/32]; NULL otherwise.  Returns a device pointer inside ws, or NULL. */
+ * E8M0 scale bytes, 8 = the h codes [terms][T*K][I], 9 = their scale bytes; NULL
+ * otherwise.  Scale bytes are stored k-block-major over the terms * T*K rows: the bytes of
+ * row r for the 32-element groups 4w .. 4w+3 form 32-bit word w * rows + r.  Returns a device pointer inside ws, or NULL. */
 void* k3moe_workspace_view(const k3moe_dims* dims, int32_t T, void* ws, int32_t which);
 
 /* Static text for a status code. */

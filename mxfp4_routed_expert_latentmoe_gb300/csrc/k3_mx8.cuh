@@ -88,11 +88,12 @@ struct Mx8Params {
   int R;                    // rows per weight matrix (I for gate/up, L for down)
   int K;                    // contraction length (L or I), a multiple of 128, >= 128 * X8_STAGES
   // activation terms (one, or hi then lo when split): codes [terms][slots][K] E4M3 (the
-  // operand's tensor map), scale bytes [terms][slots][K / 32], slot order
+  // operand's tensor map), rows in slot order; scale bytes k-block-major (act_scale_idx)
   const uint8_t* act_s;
   int slots;                // slots (rows of one activation term)
-  void* out;                // GATEUP: h codes [terms][slots][R] E4M3; DOWN: o [slots, R] f32
-  uint8_t* out_s;           // GATEUP: h scale bytes [terms][slots][R / 32]
+  void* out;                // GATEUP: h codes [slots, R] E4M3 (one term) or h [slots, R] bf16
+                            // (split: k3_split_rows_kernel makes its terms); DOWN: o [slots, R] f32
+  uint8_t* out_s;           // GATEUP, one term: h scale bytes, k-block-major (act_scale_idx)
   uint32_t* status;
   void* tmaps;              // packed-weight tensor maps, [TM_MAX_CTAS][X8_BLOCKS][2] x 128 bytes
 };
@@ -153,6 +154,12 @@ K3_DEVI uint32_t e4m3x4_codes(float a, float b, float c, float d) {
   return lo | (hi << 16);
 }
 
+// Activation scale bytes are stored k-block-major: the four bytes of row r for the
+// 32-element groups 4w .. 4w + 3 form 32-bit word w of the rows (word index w * rows + r),
+// so that a stage's scale words for a batch's consecutive rows are consecutive in memory
+// (one coalesced load per 32 tokens).  rows = terms x slots (term t's row s is t x slots + s).
+K3_DEVI size_t act_scale_idx(size_t row, int g, size_t rows) { return ((size_t)(g >> 2) * rows + row) * 4 + (g & 3); }
+
 // ---------------------------------------------------------------------------- exact two-term split
 // A bf16 value x of a 32-element group is written as x = hi + lo with two MXFP8 terms:
 //   hi: E4M3 codes at the scale 2^(s_hi - 127), the smallest power of two that keeps the
@@ -189,8 +196,10 @@ K3_DEVI void split_elem(float x, float inv_hi, float sc_hi, float inv_lo, uint32
   c_lo = e4m3_code(r * inv_lo);
 }
 
-// z rows (bf16, token order) -> the two split terms in slot order: codes [2][slots][L]
-// (hi rows, then lo rows), scale bytes [2][slots][L / 32].  One thread per 32-element group.
+// bf16 rows -> the two split terms in slot order: codes [2][slots][L] (hi rows, then lo
+// rows), scale bytes of the 2 slots rows k-block-major (act_scale_idx).  Row of slot s: z row slot_tok[s] (the gather of
+// the activations), or row s itself when slot_tok is null (h, already in slot order).  One
+// thread per 32-element group.
 __global__ void __launch_bounds__(256) k3_split_rows_kernel(const uint16_t* __restrict__ z,
                                                             const int32_t* __restrict__ slot_tok,
                                                             const int32_t* __restrict__ n_placed, int slots, int L,
@@ -202,7 +211,7 @@ __global__ void __launch_bounds__(256) k3_split_rows_kernel(const uint16_t* __re
   const size_t total = (size_t)np * G;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const int slot = (int)(i / G), g = (int)(i % G);
-    const int t = __ldg(slot_tok + slot);
+    const int t = slot_tok ? __ldg(slot_tok + slot) : slot;
     const uint4* src = reinterpret_cast<const uint4*>(z + (size_t)t * L + g * 32);
     uint4 v[4];
 #pragma unroll
@@ -236,13 +245,13 @@ __global__ void __launch_bounds__(256) k3_split_rows_kernel(const uint16_t* __re
     dh[1] = make_uint4(ch[4], ch[5], ch[6], ch[7]);
     dl[0] = make_uint4(cl[0], cl[1], cl[2], cl[3]);
     dl[1] = make_uint4(cl[4], cl[5], cl[6], cl[7]);
-    scales[(size_t)slot * G + g] = (uint8_t)s_hi;
-    scales[((size_t)slots + slot) * G + g] = (uint8_t)s_lo;
+    scales[act_scale_idx(slot, g, 2 * (size_t)slots)] = (uint8_t)s_hi;
+    scales[act_scale_idx((size_t)slots + slot, g, 2 * (size_t)slots)] = (uint8_t)s_lo;
   }
 }
 
 // z rows (bf16, token order) -> MXFP8 rows in slot order: codes [slots, L], scale bytes
-// [slots, L / 32].  One thread per 32-element group.
+// k-block-major (act_scale_idx).  One thread per 32-element group.
 __global__ void __launch_bounds__(256) k3_gather_mx8_kernel(const uint16_t* __restrict__ z,
                                                             const int32_t* __restrict__ slot_tok,
                                                             const int32_t* __restrict__ n_placed, int slots, int L,
@@ -276,7 +285,7 @@ __global__ void __launch_bounds__(256) k3_gather_mx8_kernel(const uint16_t* __re
     uint4* dst = reinterpret_cast<uint4*>(codes + (size_t)slot * L + g * 32);
     dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
     dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-    scales[(size_t)slot * G + g] = (uint8_t)s;
+    scales[act_scale_idx(slot, g, slots)] = (uint8_t)s;
   }
 }
 
@@ -485,7 +494,8 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
           const int col = c * 32 + lane;
           w[2 + 3 * t + c] =
               (col < n && slot0 + col < p.slots)
-                  ? __ldg(reinterpret_cast<const uint32_t*>(p.act_s + ((size_t)t * p.slots + slot0 + col) * KB + 4 * ks))
+                  ? __ldg(reinterpret_cast<const uint32_t*>(p.act_s) + (size_t)ks * TERMS * p.slots +
+                          (size_t)t * p.slots + slot0 + col)
                   : 0x7F7F7F7Fu;  // columns past the batch: scale 1, outputs unused
         }
     };
@@ -549,26 +559,20 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
           for (int jj = 0; jj < 8; ++jj) {
             const int col = c * 8 + jj;  // warp-uniform
             if (col >= n) break;
-            const float h = bf16_bits_to_f32(f32_to_bf16_bits(situ_fast(__uint_as_float(r0[jj]), __uint_as_float(r1[jj]))));
-            // largest |h| of the group: the bit patterns of non-negative floats order as integers
-            const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
+            const uint16_t hb = f32_to_bf16_bits(situ_fast(__uint_as_float(r0[jj]), __uint_as_float(r1[jj])));
             const size_t slot = (size_t)(slot0 + col);
             if constexpr (SPLIT) {
-              // h exactly as two terms (hi rows, then lo rows p.slots further on)
-              const uint32_t sh = split_hi_scale(m), sl = split_lo_scale(sh);
-              uint32_t ch, cl;
-              split_elem(h, mx8_inv_scale(sh), e8m0_value(sh), mx8_inv_scale(sl), ch, cl);
-              hq[slot * p.R + feat] = (uint8_t)ch;
-              hq[((size_t)p.slots + slot) * p.R + feat] = (uint8_t)cl;
-              if (lane == 0) {
-                p.out_s[slot * (p.R / 32) + (feat >> 5)] = (uint8_t)sh;
-                p.out_s[((size_t)p.slots + slot) * (p.R / 32) + (feat >> 5)] = (uint8_t)sl;
-              }
+              // bf16 h in slot order; its two terms are made by a separate pass (the split
+              // here would double the epilogue's work, which bounds this kernel)
+              reinterpret_cast<uint16_t*>(p.out)[slot * p.R + feat] = hb;
             } else {
+              const float h = bf16_bits_to_f32(hb);
+              // largest |h| of the group: the bit patterns of non-negative floats order as integers
+              const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
               const uint32_t sb = mx8_scale_byte(m);
               const uint32_t code = e4m3_code(h * mx8_inv_scale(sb));
               hq[slot * p.R + feat] = (uint8_t)code;
-              if (lane == 0) p.out_s[slot * (p.R / 32) + (feat >> 5)] = (uint8_t)sb;
+              if (lane == 0) p.out_s[act_scale_idx(slot, feat >> 5, p.slots)] = (uint8_t)sb;
             }
           }
         } else {

@@ -24,9 +24,10 @@ constexpr int kMaxDevices = 64;
 constexpr int kTcMinTokensDefault = 9;  // measured crossover on GB300 at K3 shapes (bench.py --sweep)
 constexpr int kSplitKMaxT = 512;        // the projections split K only when they have few output tiles
 // exact tensor-core experts: two-term MXFP8 split below this many tokens, bf16 weight decode
-// from it on (measured on GB300 at K3 shapes: 3072 tokens 5226 us split against 5258 us
-// decode, 3584 tokens 5621 us against 5418 us; bench.py --sweep)
-constexpr int kSplitMaxTokensDefault = 3328;
+// from it on.  Default: the split at every token count (measured on GB300 at K3 shapes, the
+// whole forward: 9 tokens 586 us split against 766 us decode, 1024 tokens 3633 against
+// 4716, 4096 tokens 4854 against 5780, 8192 tokens 9284 against 10833; bench.py --sweep)
+constexpr int kSplitMaxTokensDefault = 1 << 30;
 
 size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 int tc_min_t();
@@ -36,6 +37,7 @@ struct WsLayout {
   size_t status, logits, ids, w, zmax, zpow, counts, offsets, slot_of, slot_tok, inv, uniq, n_uniq, nb_prefix,
       n_batches, cta_cnt, cta_base, batches, z, z16, h16, o, y, yhat, cpart, ccount, act, tmaps, zero_end, total;
   size_t part = 0, part_bytes = 0;
+  size_t hterm = 0;  // the split form's two terms of h
 };
 
 WsLayout ws_layout(const k3moe_dims& d, int T) {
@@ -76,10 +78,12 @@ WsLayout ws_layout(const k3moe_dims& d, int T) {
   L.batches = take((slots / 8 + 1 + (E < slots ? E : slots)) * sizeof(MxBatch));
   L.z = take(Tz * Lt * 2);
   L.z16 = take(Tz * Lt * 2);
-  // bf16 h (weight-decode path), or the h codes and scale bytes of the MXFP8 variant (one
-  // term) or of the exact split (two terms: 2 slots I codes + 2 slots I / 32 scale bytes)
+  // bf16 h (weight-decode and split forms), or the h codes and scale bytes of the MXFP8
+  // variant (one term); the split form's two terms of h follow in their own region (2 slots I
+  // codes + 2 slots I / 32 scale bytes)
   const bool split = split_experts(d, T);
-  L.h16 = take(slots * I * 2 + (split ? slots * I / 16 : 0));
+  L.h16 = take(slots * I * 2);
+  L.hterm = take(split ? slots * I * 2 + slots * I / 16 : 0);
   L.o = take(slots * Lt * 4);
   L.y = take(Tz * Lt * 4);
   L.yhat = take(Tz * Lt * 2);
@@ -302,11 +306,10 @@ constexpr int kCombRowMinT = 256;
 // weight-streaming kernels at every T
 bool tc_experts(const k3moe_dims& d, int T) { return T >= tc_min_t() && d.latent % 256 == 0 && d.inter % 256 == 0; }
 // operand form of the exact grouped GEMM: below g_split_max_t tokens (process-wide,
-// k3moe_set_tc_split_max_tokens) the bf16 activations are split exactly into two MXFP8
-// terms for block-scaled MMAs over the stored weights (k3_mx8_moe_kernel<.., 1>); from it
-// on the SMs decode the weights to bf16 (k3_tc_moe_kernel), which wins once the batches
-// hold enough tokens per expert to amortise the decode.  The split needs both contraction
-// lengths >= 512.
+// k3moe_set_tc_split_max_tokens; by default at every count) the bf16 activations are split
+// exactly into two MXFP8 terms for block-scaled MMAs over the stored weights
+// (k3_mx8_moe_kernel<.., 1>); from it on the SMs decode the weights to bf16
+// (k3_tc_moe_kernel).  The split needs both contraction lengths >= 512.
 std::atomic<int> g_split_max_t{kSplitMaxTokensDefault};
 bool split_experts(const k3moe_dims& d, int T) {
   return T < g_split_max_t.load(std::memory_order_relaxed) && !d.act_mxfp8 && tc_experts(d, T) &&
@@ -743,11 +746,17 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
     // exact: the bf16 z and h as two MXFP8 terms each, block-scaled MMAs on the stored
     // MXFP4 weights (terms' codes [2][slots][K], then their scale bytes [2][slots][K / 32])
     const uint8_t* a8 = at<uint8_t>(ws, L.act);
-    uint8_t* h8 = at<uint8_t>(ws, L.h16);
+    uint16_t* hb = at<uint16_t>(ws, L.h16);
+    uint8_t* h8 = at<uint8_t>(ws, L.hterm);
     Mx8Params gp{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.inter, d.latent,
-                 a8 + (size_t)2 * slots * d.latent, slots, h8, h8 + (size_t)2 * slots * d.inter, status,
-                 at<void>(ws, L.tmaps)};
+                 a8 + (size_t)2 * slots * d.latent, slots, hb, nullptr, status, at<void>(ws, L.tmaps)};
     K3_TRY((launch_mx8_moe<0, 1>(a8, gp, dev, sms, s, pdl)));
+    // h (bf16, slot order) -> its two terms for the down GEMM
+    const size_t hgroups = (size_t)slots * (d.inter / 32);
+    const int hblocks = (int)((hgroups + 255) / 256 < (size_t)sms * 8 ? (hgroups + 255) / 256 : (size_t)sms * 8);
+    K3_TRY(launch(k3_split_rows_kernel, dim3(hblocks), dim3(256), 0, s, pdl, (const uint16_t*)hb,
+                  (const int32_t*)nullptr, (const int32_t*)(at<int32_t>(ws, L.offsets) + d.n_experts), slots,
+                  (int)d.inter, h8, h8 + (size_t)2 * slots * d.inter));
     K3_TRY(mark(events, n_events, 3, s));
     Mx8Params dp2{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.latent, d.inter,
                   h8 + (size_t)2 * slots * d.inter, slots, at<void>(ws, L.o), nullptr, status, at<void>(ws, L.tmaps)};
@@ -1010,8 +1019,8 @@ void* k3moe_workspace_view(const k3moe_dims* dims, int32_t T, void* ws, int32_t 
   switch (which) {
     case 6: return at<void>(ws, L.act);
     case 7: return at<uint8_t>(ws, L.act) + terms * slots * dims->latent;
-    case 8: return at<void>(ws, L.h16);
-    case 9: return at<uint8_t>(ws, L.h16) + terms * slots * dims->inter;
+    case 8: return at<void>(ws, terms == 2 ? L.hterm : L.h16);
+    case 9: return at<uint8_t>(ws, terms == 2 ? L.hterm : L.h16) + terms * slots * dims->inter;
     default: return nullptr;
   }
 }

@@ -40,15 +40,15 @@ def test_workspace_bytes_is_monotone_and_rejects_bad_dims():
     assert L.k3moe_workspace_bytes(ctypes.byref(d), -1) == 0
 
 
-T_SPLIT_DEFAULT = 3328
+T_SPLIT_DEFAULT = 1 << 30
 
 
 def test_workspace_holds_the_tensor_core_path_buffers_from_the_threshold():
     # from k3moe_tc_min_tokens tokens the grouped expert GEMM needs the slot-ordered
     # activations (bf16 rows, or two MXFP8 terms plus their scale bytes), the weight tensor
-    # maps (256 CTAs x 2 blocks x 2 x 128 bytes), the split form's h scale bytes and the
-    # projections' split-K partial sums (8 x T x max(E + L, H) f32); below that the
-    # workspace grows by the per-token buffers only
+    # maps (256 CTAs x 2 blocks x 2 x 128 bytes), the split form's two terms of h (codes and
+    # scale bytes) and the projections' split-K partial sums (8 x T x max(E + L, H) f32);
+    # below that the workspace grows by the per-token buffers only
     L = k3.lib()
     d = _d()
     t0 = k3.tc_min_tokens()
@@ -57,31 +57,32 @@ def test_workspace_holds_the_tensor_core_path_buffers_from_the_threshold():
     ws = {T: L.k3moe_workspace_bytes(ctypes.byref(d), T) for T in (t0 - 2, t0 - 1, t0)}
     per_token = ws[t0 - 1] - ws[t0 - 2]
     slots = t0 * 16
-    split_scales = slots * 3584 // 16 + slots * 3072 // 16
+    split_extra = slots * 3584 // 16 + slots * 3072 * 2 + slots * 3072 // 16
     part = 8 * t0 * max(896 + 3584, 7168) * 4
-    tc_bytes = slots * 3584 * 2 + 256 * 2 * 2 * 128 + split_scales + part
+    tc_bytes = slots * 3584 * 2 + 256 * 2 * 2 * 128 + split_extra + part
     assert ws[t0] - ws[t0 - 1] >= tc_bytes
     assert ws[t0] - ws[t0 - 1] <= tc_bytes + 2 * per_token + 6 * 256
 
 
 def test_split_form_token_bound():
     """k3moe_set_tc_split_max_tokens sets the token count below which the exact tensor-core
-    expert GEMMs take the two-term MXFP8 split (default 3328, the measured crossover),
+    expert GEMMs take the two-term MXFP8 split (default 2^30: every count, as measured),
     returns the previous value, rejects t < 0, and sizes the workspace: the split form adds
-    the two terms' scale bytes of z and h (slots x (L + I) / 16) on top of the bf16-sized
-    buffers; below the tensor-core threshold the form does not matter."""
+    z's terms' scale bytes (slots x L / 16) and h's two terms (slots x I x 2 codes and
+    slots x I / 16 scale bytes) to the bf16-sized buffers; below the tensor-core threshold the
+    form does not matter."""
     L = k3.lib()
     d = _d()
-    assert k3.tc_split_max_tokens() == 3328
+    assert k3.tc_split_max_tokens() == 1 << 30 == k3.SPLIT_ALWAYS
     T = 64
     slots = T * 16
     on = L.k3moe_workspace_bytes(ctypes.byref(d), T)
     below = L.k3moe_workspace_bytes(ctypes.byref(d), 8)
     prev = k3.set_tc_split_max_tokens(0)
     try:
-        assert prev == 3328 and k3.tc_split_max_tokens() == 0
+        assert prev == 1 << 30 and k3.tc_split_max_tokens() == 0
         off = L.k3moe_workspace_bytes(ctypes.byref(d), T)
-        assert 0 <= on - off - slots * (3584 + 3072) // 16 < 2 * 256
+        assert 0 <= on - off - (slots * (3584 + 3072) // 16 + slots * 3072 * 2) < 3 * 256
         assert L.k3moe_workspace_bytes(ctypes.byref(d), 8) == below
         with pytest.raises(ValueError):
             k3.set_tc_split_max_tokens(-1)
@@ -93,11 +94,11 @@ def test_split_form_token_bound():
         assert L.k3moe_workspace_bytes(ctypes.byref(d), T) == on
     finally:
         k3.set_tc_split_max_tokens(prev)
-    assert k3.tc_split_max_tokens() == 3328
+    assert k3.tc_split_max_tokens() == 1 << 30
     # the MXFP8-activation variant never takes the split form
     dv = k3.dims(hidden=7168, latent=3584, n_experts=896, top_k=16, inter=3072, act_mxfp8=1)
     v = L.k3moe_workspace_bytes(ctypes.byref(dv), T)
-    assert 0 <= on - v - slots * (3584 + 3072) // 16 < 2 * 256
+    assert v == off
 
 def test_device_status_bits_match_the_header():
     import re

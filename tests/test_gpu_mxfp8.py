@@ -27,7 +27,7 @@ import pytest
 import oracle
 from datagen import configs as C
 from tests._harness import REL_L2_BAR, oracle_forward, oracle_route, rel_l2
-from tests.test_gpu_parity import PER_TOKEN_BAR, Layer, _slot_map, _ws_view  # noqa: F401
+from tests.test_gpu_parity import PER_TOKEN_BAR, Layer, _slot_map, _ws_view, scales_by_row  # noqa: F401
 
 pytestmark = pytest.mark.gpu
 
@@ -89,14 +89,14 @@ def test_variant_quantized_z_and_expert_slots(k3, mx_prefill, T):
     slots = T * K
     z = _ws_view(k3, L, ws, 0, T, T * Lt, torch.bfloat16).reshape(T, Lt)
     zc = _codes_view(k3, L, ws, 6, slots * Lt).reshape(slots, Lt)
-    zs = _codes_view(k3, L, ws, 7, slots * Lt // 32).reshape(slots, Lt // 32)
+    zs = scales_by_row(_codes_view(k3, L, ws, 7, slots * Lt // 32), slots, Lt // 32)
     s_exp, s_tok, offs = _slot_map(ids, cfg.n_experts)
     rc, rs = oracle.mxfp8_quant(z[s_tok])
     assert np.array_equal(zs, rs)
     assert np.array_equal(zc, rc)
     # per slot, three experts: the most used, the least used and one in between
     hc = _codes_view(k3, L, ws, 8, slots * I).reshape(slots, I)
-    hs = _codes_view(k3, L, ws, 9, slots * I // 32).reshape(slots, I // 32)
+    hs = scales_by_row(_codes_view(k3, L, ws, 9, slots * I // 32), slots, I // 32)
     o_all = _ws_view(k3, L, ws, 5, T, slots * Lt, torch.float32).reshape(slots, Lt)
     counts = np.bincount(ids.ravel(), minlength=cfg.n_experts)
     used = np.nonzero(counts)[0]
