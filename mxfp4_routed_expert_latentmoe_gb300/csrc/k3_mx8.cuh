@@ -188,19 +188,45 @@ K3_DEVI float e4m3_value(uint32_t code) {
 }
 // 2^(s - 127) for a scale byte s (2^-127 is an f32 subnormal)
 K3_DEVI float e8m0_value(uint32_t s) { return s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u); }
-// one element: codes of hi and lo at the group's scales (inv_hi = 2^(127 - s_hi), sc_hi =
-// 2^(s_hi - 127), inv_lo = 2^(127 - s_lo))
-K3_DEVI void split_elem(float x, float inv_hi, float sc_hi, float inv_lo, uint32_t& c_hi, uint32_t& c_lo) {
-  c_hi = e4m3_code(x * inv_hi);
-  const float r = x - e4m3_value(c_hi) * sc_hi;  // exact
-  c_lo = e4m3_code(r * inv_lo);
+// two elements: the codes of hi and lo at the group's scales (inv_hi = 2^(127 - s_hi),
+// sc_hi = 2^(s_hi - 127), inv_lo = 2^(127 - s_lo)), two codes per 16 bits (x0 low)
+K3_DEVI void split_pair(float x0, float x1, float inv_hi, float sc_hi, float inv_lo, uint32_t& c_hi,
+                        uint32_t& c_lo) {
+  c_hi = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x0 * inv_hi, x1 * inv_hi), __NV_SATFINITE, __NV_E4M3);
+  const __half2_raw hv = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)c_hi, __NV_E4M3);
+  const float2 v = __half22float2(__half2(hv));  // exact: every E4M3 value is an f16 value
+  const float r0 = x0 - v.x * sc_hi, r1 = x1 - v.y * sc_hi;  // exact
+  c_lo = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(r0 * inv_lo, r1 * inv_lo), __NV_SATFINITE, __NV_E4M3);
 }
 
-// bf16 rows -> the two split terms in slot order: codes [2][slots][L] (hi rows, then lo
-// rows), scale bytes of the 2 slots rows k-block-major (act_scale_idx).  Row of slot s: z row slot_tok[s] (the gather of
-// the activations), or row s itself when slot_tok is null (h, already in slot order).  One
-// thread per 32-element group.
-__global__ void __launch_bounds__(256) k3_split_rows_kernel(const uint16_t* __restrict__ z,
+// A 32-element group (bf16 pairs in w[16], low element first) -> its two terms' codes (8
+// words each, byte j of word i = element 4 i + j) and scale bytes
+K3_DEVI void split_group(const uint32_t (&w)[16], uint32_t (&ch)[8], uint32_t (&cl)[8], uint32_t& s_hi,
+                         uint32_t& s_lo) {
+  uint32_t mx = 0u;  // largest |x| as bf16 magnitude bits (they order as integers)
+#pragma unroll
+  for (int j = 0; j < 16; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+  s_hi = split_hi_scale(__uint_as_float(mx << 16));
+  s_lo = split_lo_scale(s_hi);
+  const float inv_hi = mx8_inv_scale(s_hi), sc_hi = e8m0_value(s_hi), inv_lo = mx8_inv_scale(s_lo);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t h0, l0, h1, l1;
+    split_pair(__uint_as_float(w[2 * j] << 16), __uint_as_float(w[2 * j] & 0xFFFF0000u), inv_hi, sc_hi, inv_lo, h0,
+               l0);
+    split_pair(__uint_as_float(w[2 * j + 1] << 16), __uint_as_float(w[2 * j + 1] & 0xFFFF0000u), inv_hi, sc_hi,
+               inv_lo, h1, l1);
+    ch[j] = (h0 & 0xFFFFu) | (h1 << 16);
+    cl[j] = (l0 & 0xFFFFu) | (l1 << 16);
+  }
+}
+
+// bf16 rows -> the two split terms of every routed slot: codes [2][slots][L] (hi rows,
+// then lo rows), scale bytes of the 2 slots rows k-block-major (act_scale_idx).  The row of
+// slot s is row slot_tok[s] of x (z: the gather into slot order), or row s itself when
+// slot_tok is null (h, already in slot order).  One thread per 32-element group; the first
+// n_placed slots are the routed ones.
+__global__ void __launch_bounds__(256) k3_split_rows_kernel(const uint16_t* __restrict__ x,
                                                             const int32_t* __restrict__ slot_tok,
                                                             const int32_t* __restrict__ n_placed, int slots, int L,
                                                             uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
@@ -211,34 +237,16 @@ __global__ void __launch_bounds__(256) k3_split_rows_kernel(const uint16_t* __re
   const size_t total = (size_t)np * G;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const int slot = (int)(i / G), g = (int)(i % G);
-    const int t = slot_tok ? __ldg(slot_tok + slot) : slot;
-    const uint4* src = reinterpret_cast<const uint4*>(z + (size_t)t * L + g * 32);
-    uint4 v[4];
+    const int row = slot_tok ? __ldg(slot_tok + slot) : slot;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * L + g * 32);
+    uint32_t w[16];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = __ldg(src + j);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(v);
-    float x[32];
-    float amax = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      x[2 * j] = __uint_as_float(w[j] << 16);
-      x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-      amax = fmaxf(amax, fmaxf(fabsf(x[2 * j]), fabsf(x[2 * j + 1])));
+    for (int j = 0; j < 4; ++j) {
+      const uint4 v = __ldg(src + j);
+      w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
     }
-    const uint32_t s_hi = split_hi_scale(amax), s_lo = split_lo_scale(s_hi);
-    const float inv_hi = mx8_inv_scale(s_hi), sc_hi = e8m0_value(s_hi), inv_lo = mx8_inv_scale(s_lo);
-    uint32_t ch[8], cl[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      ch[j] = cl[j] = 0u;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        uint32_t a, b;
-        split_elem(x[4 * j + e], inv_hi, sc_hi, inv_lo, a, b);
-        ch[j] |= a << (8 * e);
-        cl[j] |= b << (8 * e);
-      }
-    }
+    uint32_t ch[8], cl[8], s_hi, s_lo;
+    split_group(w, ch, cl, s_hi, s_lo);
     uint4* dh = reinterpret_cast<uint4*>(codes + (size_t)slot * L + g * 32);
     uint4* dl = reinterpret_cast<uint4*>(codes + ((size_t)slots + slot) * L + g * 32);
     dh[0] = make_uint4(ch[0], ch[1], ch[2], ch[3]);

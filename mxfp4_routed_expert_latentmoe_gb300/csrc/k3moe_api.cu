@@ -715,17 +715,24 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
       // grouped GEMM (the f16 copy of z that the weight-streaming kernels read is not needed)
       K3_TRY(launch_topk(tp, dev, s, pdl));
       K3_TRY(launch_permute(pp, dev, s, pdl));
-      if (d.act_mxfp8 || split) {
-        // z in slot order as MXFP8 rows (codes, then the scale bytes): one term (the
-        // variant's quantization) or the two exact split terms
+      if (split) {
+        // z's two exact MXFP8 terms in slot order (codes, then the scale bytes)
         uint8_t* a8 = at<uint8_t>(ws, L.act);
         const size_t groups = (size_t)slots * (d.latent / 32);
         const int gblocks = (int)((groups + 255) / 256 < (size_t)sms * 8 ? (groups + 255) / 256 : (size_t)sms * 8);
-        const int terms = split ? 2 : 1;
-        K3_TRY(launch(split ? k3_split_rows_kernel : k3_gather_mx8_kernel, dim3(gblocks), dim3(256), 0, s, pdl,
+        K3_TRY(launch(k3_split_rows_kernel, dim3(gblocks), dim3(256), 0, s, pdl,
                       (const uint16_t*)at<uint16_t>(ws, L.z), (const int32_t*)at<int32_t>(ws, L.slot_tok),
                       (const int32_t*)(at<int32_t>(ws, L.offsets) + d.n_experts), slots, (int)d.latent, a8,
-                      a8 + (size_t)terms * slots * d.latent));
+                      a8 + (size_t)2 * slots * d.latent));
+      } else if (d.act_mxfp8) {
+        // z quantized to MXFP8 rows in slot order (codes, then the scale bytes)
+        uint8_t* a8 = at<uint8_t>(ws, L.act);
+        const size_t groups = (size_t)slots * (d.latent / 32);
+        const int gblocks = (int)((groups + 255) / 256 < (size_t)sms * 8 ? (groups + 255) / 256 : (size_t)sms * 8);
+        K3_TRY(launch(k3_gather_mx8_kernel, dim3(gblocks), dim3(256), 0, s, pdl, (const uint16_t*)at<uint16_t>(ws, L.z),
+                      (const int32_t*)at<int32_t>(ws, L.slot_tok),
+                      (const int32_t*)(at<int32_t>(ws, L.offsets) + d.n_experts), slots, (int)d.latent, a8,
+                      a8 + (size_t)slots * d.latent));
       } else {
         // bf16 rows in slot order (interleaved K order)
         const int per = d.latent / 8;
