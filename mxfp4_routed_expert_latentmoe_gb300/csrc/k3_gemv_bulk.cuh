@@ -39,6 +39,15 @@ K3_DEVI void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t ba
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+// the same with an L2 eviction-priority policy (createpolicy)
+K3_DEVI void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;\n" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 
 template <int MODE>
 struct MxbLayout {
@@ -96,6 +105,7 @@ __global__ void __launch_bounds__((2 + MXB_MAX_WARPS) * 32) k3_mxb_gemv_kernel(M
   const size_t qrow = (size_t)K / 2, srow = (size_t)K / 32;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    const uint64_t pol = l2_policy_evict_first();  // expert weights are read once per call
     if (!PRE) grid_dep_wait();
     const int total = tiles * (*p.n_batches);
     const int n_mine = (total > (int)blockIdx.x) ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -125,9 +135,10 @@ __global__ void __launch_bounds__((2 + MXB_MAX_WARPS) * 32) k3_mxb_gemv_kernel(M
       const uint8_t* sptr = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, wcur, WOFF + 2 * mq + 1));
       if (lane < 8 * M) {  // row pair lane & 7 of matrix lane >> 3
         const int pr = lane & 7;
-        bulk_g2s(sbase + mq * MB + pr * PS, qptr + (row0 + 2 * pr) * qrow, (uint32_t)(2 * qrow), full(st));
+        bulk_g2s_hint(sbase + mq * MB + pr * PS, qptr + (row0 + 2 * pr) * qrow, (uint32_t)(2 * qrow), full(st), pol);
       } else if (lane >= 16 && lane < 16 + M) {  // scale bytes of matrix lane - 16
-        bulk_g2s(sbase + mq * MB + (MX_ROWS / 2) * PS, sptr + row0 * srow, (uint32_t)(MX_ROWS * srow), full(st));
+        bulk_g2s_hint(sbase + mq * MB + (MX_ROWS / 2) * PS, sptr + row0 * srow, (uint32_t)(MX_ROWS * srow), full(st),
+                      pol);
       }
       if (lane == 31) bulk_g2s(sbase + M * MB, rec, 128, full(st));
     }

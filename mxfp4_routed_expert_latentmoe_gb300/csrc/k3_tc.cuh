@@ -117,6 +117,13 @@ K3_DEVI void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, u
       "l"(map), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+// an L2 policy that makes the lines a copy brings in the first to be evicted (the weight
+// streams of the decode GEMVs: read once per call)
+K3_DEVI uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+  return pol;
+}
 K3_DEVI void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(map) : "memory");
 }
