@@ -236,6 +236,14 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def tensor_peak(peaks):
+    """The tensor denominator: the measured bf16 rate sustained over seconds under the power
+    cap.  Every workload's step is replayed back to back for the whole timed region (the
+    prefill step draws the part's power limit: SM clocks near 1.8 GHz against 2.07), so its
+    GEMMs run in the sustained regime, not as an isolated burst."""
+    return peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]), "bf16 sustained"
+
+
 def csrc_hash() -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "mxfp4_routed_expert_latentmoe_gb300", "csrc")
@@ -584,36 +592,39 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
     alg = algorithmic(cfg, n_unique)
     dom = "gateup"
     tc = uses_grouped_gemm(cfg, k3.tc_min_tokens())
+    tpeak, tkind = tensor_peak(peaks)
     if tc and cfg.act_mxfp8:
-        # block-scaled MMAs at the fp8 rate: peak = the measured bf16 burst x the nominal
+        # block-scaled MMAs at the fp8 rate: peak = the measured bf16 rate x the nominal
         # 2x fp8/bf16 ratio; the weights also stream from HBM once -- report the tighter bound
         t_s = phase_ms[dom] / 1e3
         tf = alg[dom]["flops"] / t_s / 1e12
         gb = alg[dom]["bytes"] / t_s / 1e9
-        fp8_peak = 2 * peaks["bf16_tflops"]
+        fp8_peak = 2 * tpeak
         f_t, f_h = tf / fp8_peak, gb / peaks["hbm_gbs"]
         if f_h >= f_t:
             roof = {"bound": "hbm", "achieved": gb, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": f_h,
                     "peak_kind": f"{peak_kind} HBM copy"}
         else:
             roof = {"bound": "tensor", "achieved": tf, "peak": fp8_peak, "unit": "TFLOP/s", "frac": f_t,
-                    "peak_kind": f"{peak_kind} bf16 burst x 2 (nominal fp8/bf16 ratio)"}
-        roof.update({"traffic": profiled_traffic(dom, cfg.name), "kernel": "k3_mx8_moe_kernel<0> (gate/up)",
+                    "peak_kind": f"{peak_kind} {tkind} x 2 (nominal fp8/bf16 ratio)"}
+        roof.update({"traffic": profiled_traffic(dom, cfg.name), "kernel": "k3_mx8_moe_kernel<0, 0> (gate/up)",
                      "other_bound_frac": f_t if f_h >= f_t else f_h,
-                     "tflops_bf16_equivalent_frac": tf / peaks["bf16_tflops"]})
+                     "tflops_bf16_equivalent_frac": tf / tpeak})
     elif tc:
-        # the grouped GEMM runs for milliseconds inside a step of a few milliseconds: the
-        # burst bf16 peak is its tensor denominator; with few tokens per expert (chunks) the
-        # weight bytes bound it instead -- the tighter of the two is reported.  The split
-        # form does the bf16 products exactly as two fp8 passes (twice the fp8 work at
-        # twice the bf16 rate): the algorithmic flops against the bf16 peak are its bound too
+        # the grouped GEMM runs for milliseconds inside a step replayed back to back: the
+        # sustained bf16 rate is its tensor denominator (the burst fraction is reported
+        # beside it); with few tokens per expert (chunks) the weight bytes bound it instead
+        # -- the tighter of the two is reported.  The split form does the bf16 products
+        # exactly as two fp8 passes (twice the fp8 work at twice the bf16 rate): the
+        # algorithmic flops against the bf16 rate are its bound too
         t_s = phase_ms[dom] / 1e3
         tf, gb = alg[dom]["flops"] / t_s / 1e12, alg[dom]["bytes"] / t_s / 1e9
-        f_t, f_h = tf / peaks["bf16_tflops"], gb / peaks["hbm_gbs"]
+        f_t, f_h = tf / tpeak, gb / peaks["hbm_gbs"]
         kv = profiled(dom, cfg.name) or {}
         if f_t >= f_h:
-            roof = {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": f_t,
-                    "peak_kind": f"{peak_kind} bf16 burst", "other_bound_frac": f_h}
+            roof = {"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s", "frac": f_t,
+                    "peak_kind": f"{peak_kind} {tkind}", "other_bound_frac": f_h,
+                    "frac_vs_bf16_burst": tf / peaks["bf16_tflops"]}
         else:
             roof = {"bound": "hbm", "achieved": gb, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": f_h,
                     "peak_kind": f"{peak_kind} HBM copy", "other_bound_frac": f_t}
@@ -644,7 +655,8 @@ def measure(a, cfg, k3, dev, world, pools, sampler):
            "layer": {"GB_s": step_bytes(cfg, n_unique) / (ms / 1e3) / 1e9,
                      "frac_hbm": step_bytes(cfg, n_unique) / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
                      "TFLOP_s": step_flops(cfg) / (ms / 1e3) / 1e12,
-                     "frac_bf16_burst": step_flops(cfg) / (ms / 1e3) / 1e12 / peaks["bf16_tflops"]},
+                     "frac_bf16_burst": step_flops(cfg) / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                     "frac_bf16_sustained": step_flops(cfg) / (ms / 1e3) / 1e12 / tpeak},
            "expert_phase": {"us": expert_us, "GB_s": exp_bytes / (expert_us / 1e6) / 1e9,
                             "frac_hbm": exp_bytes / (expert_us / 1e6) / 1e9 / peaks["hbm_gbs"]},
            "phases": phases, "profiled_ms_per_step": profiled_ms, "e2e": e2e,
@@ -791,9 +803,11 @@ def measure_shared(a, cfg, k3, dev, world):
     flops = 2 * T * 3 * H * Is
     gbs = bytes_ / (ms / 1e3) / 1e9
     tfs = flops / (ms / 1e3) / 1e12
+    tpeak, tkind = tensor_peak(peaks)
     if T >= k3.tc_min_tokens():
-        roof = {"bound": "tensor", "achieved": tfs, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": tfs / peaks["bf16_tflops"], "peak_kind": f"{peak_kind} bf16 burst",
+        roof = {"bound": "tensor", "achieved": tfs, "peak": tpeak, "unit": "TFLOP/s",
+                "frac": tfs / tpeak, "peak_kind": f"{peak_kind} {tkind}",
+                "frac_vs_bf16_burst": tfs / peaks["bf16_tflops"],
                 "kernel": "whole call: k3_tc_dense_kernel<PLAIN>, k3_shared_glu_kernel, k3_tc_dense_kernel<ACC>"}
     else:
         roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
