@@ -183,11 +183,19 @@ K3_DEVI double refine_logit(const TopkParams& p, int t, int e, int lane) {
     lo += er;
   };
   if ((p.H & 7) == 0 && ((reinterpret_cast<uintptr_t>(p.x) | reinterpret_cast<uintptr_t>(p.wr)) & 15u) == 0) {
-    // 16-byte loads, eight per operand in flight per lane (a refinement is latency-bound:
-    // one row pair is read once)
+    // 16-byte loads, eight per operand in flight per lane; four independent double-f32
+    // accumulators (word j of each load feeds accumulator j), so the two-sum chains run
+    // four at a time instead of one long dependent chain
     const uint4* xv = reinterpret_cast<const uint4*>(xr);
     const uint4* wv = reinterpret_cast<const uint4*>(wrr);
     const int nv = p.H >> 3;
+    float h4[4] = {0.f, 0.f, 0.f, 0.f}, l4[4] = {0.f, 0.f, 0.f, 0.f};
+    auto acc4 = [&](int j, float pr) {
+      float s, er;
+      two_sum(h4[j], pr, s, er);
+      h4[j] = s;
+      l4[j] += er;
+    };
     for (int v0 = lane; v0 < nv; v0 += 32 * 8) {
       uint4 a[8], b[8];
 #pragma unroll
@@ -202,10 +210,18 @@ K3_DEVI double refine_logit(const TopkParams& p, int t, int e, int lane) {
         const uint32_t bw[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          acc(__uint_as_float(aw[j] << 16) * __uint_as_float(bw[j] << 16));
-          acc(__uint_as_float(aw[j] & 0xFFFF0000u) * __uint_as_float(bw[j] & 0xFFFF0000u));
+          acc4(j, __uint_as_float(aw[j] << 16) * __uint_as_float(bw[j] << 16));
+          acc4(j, __uint_as_float(aw[j] & 0xFFFF0000u) * __uint_as_float(bw[j] & 0xFFFF0000u));
         }
       }
+    }
+    // the four accumulators into one (error-free sums of the leading parts)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float s, er;
+      two_sum(hi, h4[j], s, er);
+      hi = s;
+      lo += l4[j] + er;
     }
   } else {
     for (int h = lane; h < p.H; h += 32) acc(bf16_bits_to_f32(__ldg(xr + h)) * bf16_bits_to_f32(__ldg(wrr + h)));
