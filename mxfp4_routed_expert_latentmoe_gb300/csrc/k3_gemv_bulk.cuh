@@ -39,6 +39,13 @@ K3_DEVI void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t ba
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+// 0, through an instruction the compiler cannot see through: a value computed from x that
+// the hardware can produce only once x is available
+K3_DEVI uint32_t opaque_zero(uint32_t x) {
+  uint32_t z;
+  asm volatile("and.b32 %0, %1, 0;\n" : "=r"(z) : "r"(x));
+  return z;
+}
 // the same with an L2 eviction-priority policy (createpolicy)
 K3_DEVI void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t policy) {
   asm volatile(
@@ -260,16 +267,44 @@ __global__ void __launch_bounds__((2 + MXB_MAX_WARPS) * 32) k3_mxb_gemv_kernel(M
         sc_lo[m] = *reinterpret_cast<const uint2*>(ss + g * srow);
         sc_hi[m] = *reinterpret_cast<const uint2*>(ss + (g + 8) * srow);
       }
+      // this warp's packed words of the item (row r sits at pair r / 2, half r % 2).  GATEUP
+      // (one CTA per SM) loads them all into registers first and gives the stage back to the
+      // producer before the decode and the MMAs, so the copies in flight do not wait for the
+      // compute; DOWN runs two CTAs per SM, whose registers do not allow it
+      constexpr bool EARLY = MODE == MX_GATEUP;
+      uint32_t wlo_[MX_GPW][M], whi_[MX_GPW][M];
+      if (EARLY) {
+#pragma unroll
+        for (int j = 0; j < MX_GPW; ++j)
+#pragma unroll
+          for (int m = 0; m < M; ++m) {
+            const uint8_t* sq = stp + m * MB + c * 128 + j * 16 + 4 * t + (g >> 1) * PS + (g & 1) * (K / 2);
+            wlo_[j][m] = *reinterpret_cast<const uint32_t*>(sq);
+            whi_[j][m] = *reinterpret_cast<const uint32_t*>(sq + 4 * PS);
+          }
+      }
+      if (EARLY) {
+        // every lane's loads have landed (the fold reads each loaded register, and the warp
+        // reduction reads each lane's fold) before lane 0 releases the stage
+        uint32_t chk = 0u;
+#pragma unroll
+        for (int m = 0; m < M; ++m) chk ^= sc_lo[m].x ^ sc_lo[m].y ^ sc_hi[m].x ^ sc_hi[m].y;
+#pragma unroll
+        for (int j = 0; j < MX_GPW; ++j)
+#pragma unroll
+          for (int m = 0; m < M; ++m) chk ^= wlo_[j][m] ^ whi_[j][m];
+        const uint32_t zero = __reduce_or_sync(0xffffffffu, opaque_zero(chk));
+        if (lane == 0) mbar_arrive(empty(st) + zero);
+      }
 #pragma unroll
       for (int j = 0; j < MX_GPW; ++j) {
         uint32_t a0[M][4], a1[M][4];
         float slo[M], shi[M];
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-          // row r sits at pair r / 2, half r % 2
           const uint8_t* sq = stp + m * MB + c * 128 + j * 16 + 4 * t + (g >> 1) * PS + (g & 1) * (K / 2);
-          const uint32_t wlo = *reinterpret_cast<const uint32_t*>(sq);
-          const uint32_t whi = *reinterpret_cast<const uint32_t*>(sq + 4 * PS);
+          const uint32_t wlo = EARLY ? wlo_[j][m] : *reinterpret_cast<const uint32_t*>(sq);
+          const uint32_t whi = EARLY ? whi_[j][m] : *reinterpret_cast<const uint32_t*>(sq + 4 * PS);
           uint32_t plo[4], phi[4];
           e2m1x8_to_f16x8(wlo, plo);
           e2m1x8_to_f16x8(whi, phi);
@@ -301,9 +336,11 @@ __global__ void __launch_bounds__((2 + MXB_MAX_WARPS) * 32) k3_mxb_gemv_kernel(M
           }
         }
       }
-      // the stage's bytes are consumed: hand it back to the producer
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty(st));
+      if (!EARLY) {
+        // the stage's bytes are consumed: hand it back to the producer
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(st));
+      }
       // partial sums -> red[s & 1][c][m][nb][row 16][col 8] once the reducer released it
       const int b = s & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(rempty(b), ((s >> 1) & 1) ^ 1, abort_flag))) break;
