@@ -202,9 +202,10 @@ __global__ void __launch_bounds__((2 + MXB_MAX_WARPS) * 32) k3_mxb_gemv_kernel(M
     const int total = tiles * (*p.n_batches);
     const int n_mine = (total > (int)blockIdx.x) ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     // single-token batches keep this warp's activation fragments in registers while
-    // consecutive items use the same activation row (GATEUP: the same token; DOWN: the
-    // same slot, i.e. the same batch)
-    constexpr bool CACHE_B = (NBLK == 1);
+    // consecutive items use the same activation row (GATEUP: the same token, every item of
+    // a one-token call; DOWN would need the same slot, i.e. the same expert, which a CTA's
+    // consecutive items almost never share: it keeps the registers for the early release)
+    constexpr bool CACHE_B = (NBLK == 1) && MODE == MX_GATEUP;
     uint4 bcache[CACHE_B ? MX_GPW : 1];
     int bkey = -1;
     for (int s = 0; s < n_mine; ++s) {
@@ -267,11 +268,10 @@ __global__ void __launch_bounds__((2 + MXB_MAX_WARPS) * 32) k3_mxb_gemv_kernel(M
         sc_lo[m] = *reinterpret_cast<const uint2*>(ss + g * srow);
         sc_hi[m] = *reinterpret_cast<const uint2*>(ss + (g + 8) * srow);
       }
-      // this warp's packed words of the item (row r sits at pair r / 2, half r % 2).  GATEUP
-      // (one CTA per SM) loads them all into registers first and gives the stage back to the
-      // producer before the decode and the MMAs, so the copies in flight do not wait for the
-      // compute; DOWN runs two CTAs per SM, whose registers do not allow it
-      constexpr bool EARLY = MODE == MX_GATEUP;
+      // this warp's packed words of the item (row r sits at pair r / 2, half r % 2), all
+      // loaded into registers first: the stage goes back to the producer before the decode
+      // and the MMAs, so the copies in flight do not wait for the compute
+      constexpr bool EARLY = true;
       uint32_t wlo_[MX_GPW][M], whi_[MX_GPW][M];
       if (EARLY) {
 #pragma unroll
