@@ -168,16 +168,26 @@ __global__ void __launch_bounds__((2 + MXB_MAX_WARPS) * 32) k3_mxb_gemv_kernel(M
       const int* mt = meta + b * Lay::META;
       const int slot0 = mt[0], n = mt[1], row0 = mt[2];
       const float* rs = red + b * W * RED;
-      for (int idx = lane; idx < MX_ROWS * n; idx += 32) {
+      // one token: the 16 rows' sums on all 32 lanes, each half of the warp over half of the
+      // compute warps' partials (lane and lane + 16 hold the same row), then added
+      const bool halves = (n == 1);
+      for (int idx = halves ? (lane & 15) : lane; idx < MX_ROWS * n; idx += 32) {
         const int row = idx & 15, col = idx >> 4, nb = col >> 3, cc = col & 7;
         float v[M];
 #pragma unroll
         for (int mm = 0; mm < M; ++mm) {
           float sum = 0.f;
+          if (halves) {
+#pragma unroll 4
+            for (int w = lane >> 4; w < W; w += 2) sum += rs[w * RED + (mm * NBLK + nb) * 128 + row * 8 + cc];
+            sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+          } else {
 #pragma unroll 6
-          for (int w = 0; w < W; ++w) sum += rs[w * RED + (mm * NBLK + nb) * 128 + row * 8 + cc];
+            for (int w = 0; w < W; ++w) sum += rs[w * RED + (mm * NBLK + nb) * 128 + row * 8 + cc];
+          }
           v[mm] = sum;
         }
+        if (halves && lane >= 16) continue;
         const int slot = slot0 + col;
         if (MODE == MX_GATEUP) {
           const int pw = mt[19 + col];
