@@ -8,6 +8,8 @@ largest and within 2^-21 of the group's largest for the others (the error bound 
 the library's header), for z (the gather's terms) and h (the terms the pass between the two
 GEMMs makes from the gate/up GEMM's bf16 h).  The products with the terms are those of the
 exact path, which the parity tests check through the outputs."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -85,3 +87,39 @@ def test_split_terms_hold_z_and_h(k3, prefill, T):
     hi, lo, s_hi, s_lo = split_terms(k3, L, ws, 8, 9, slots, I)
     frac_h = _check_terms(h, hi, lo, s_hi, s_lo, "h")
     print(f"T={T}: elements below 2^-14 of their group's largest: z {frac_z:.1e}, h {frac_h:.1e}")
+
+
+# a layer with other widths: latent 768 (gate/up contraction of 6 stages of 128, a count
+# that is not a multiple of 4), inter 512 (the down contraction at the 4-stage minimum),
+# hidden 1024, 32 experts, top-4
+MID = dataclasses.replace(C.TINY, name="mid", T=40, hidden=1024, latent=768, n_experts=32, top_k=4, inter=512,
+                          seed=3, bias_range=0.05)
+
+
+@pytest.mark.parametrize("split", [1, 0])
+def test_both_forms_on_other_widths(k3, split):
+    """The tensor-core expert path on a layer of other widths, in both operand forms, against
+    the oracle for every token (ids bit-exact, outputs within the bars); the split form's
+    terms of z and h against the GPU's own z and h as above."""
+    from tests.test_gpu_parity import PER_TOKEN_BAR, _check_block, tc_form
+    from tests._harness import oracle_forward, rel_l2
+    L = Layer(k3, MID)
+    with tc_form(k3, split):
+        assert MID.T >= k3.tc_min_tokens()
+        got, ids, w, ws = L.forward(k3)
+        assert k3.device_status(ws) == 0
+        ref = oracle_forward(MID)
+        r = _check_block(got, ids, w, ref)
+        worst = max(rel_l2(got[t], ref["out"][t]) for t in range(MID.T))
+        assert worst <= PER_TOKEN_BAR, worst
+        if split:
+            T, Lt, I, K = MID.T, MID.latent, MID.inter, MID.top_k
+            slots = T * K
+            z = _ws_view(k3, L, ws, 0, T, T * Lt, torch.bfloat16).reshape(T, Lt)
+            _, s_tok, _ = _slot_map(ids, MID.n_experts)
+            hi, lo, s_hi, s_lo = split_terms(k3, L, ws, 6, 7, slots, Lt)
+            _check_terms(z[s_tok].astype(np.float64), hi, lo, s_hi, s_lo, "z")
+            h = _ws_view(k3, L, ws, 4, T, slots * I, torch.bfloat16).reshape(slots, I).astype(np.float64)
+            hi, lo, s_hi, s_lo = split_terms(k3, L, ws, 8, 9, slots, I)
+            _check_terms(h, hi, lo, s_hi, s_lo, "h")
+    print(f"mid widths, split {split}: rel-L2 {r:.2e}, worst token {worst:.2e}")
