@@ -89,9 +89,9 @@ typedef enum {
 #define K3MOE_DEV_BAD_ID 0x4u     /* an expert id outside [0, E) reached the permutation */
 #define K3MOE_DEV_SCALE_RANGE 0x8u /* never set: every path decodes every scale byte exactly
                                       (the value is kept so that the bit stays reserved) */
-#define K3MOE_DEV_ALIGN 0x10u      /* the tensor-core expert path (T >= 256) met an expert weight
-                                      tensor that is not 16-byte aligned; the call was abandoned
-                                      and its outputs are invalid */
+#define K3MOE_DEV_ALIGN 0x10u      /* the tensor-core expert path (T >= k3moe_tc_min_tokens) met an
+                                      expert weight tensor below its alignment (see k3moe_experts);
+                                      the call was abandoned and its outputs are invalid */
 
 /* The six vendor tensors of every expert, as DEVICE arrays of n_experts DEVICE
  * pointers (the pointer tables themselves live in device memory):
@@ -100,9 +100,14 @@ typedef enum {
  *   down_q[e] [L, I/2], down_s[e] [L, I/32]    down projection
  * A checkpoint that stores gate and up as one fused [2I, L] matrix (gate rows first)
  * passes up_q[e] = gate_q[e] + I*L/2 and up_s[e] = gate_s[e] + I*L/32.
- * Every pointer in the tables must be 16-byte aligned like any other tensor; the host
- * cannot see them, so the tensor-core path (T >= 256) checks the packed tensors on the
- * device, reports K3MOE_DEV_ALIGN and abandons the call when one is not. */
+ * Every pointer in the tables must be 16-byte aligned like any other tensor.  The
+ * tensor-core path's block-scaled GEMMs (the split form and the act_mxfp8 variant) copy the
+ * packed tensors gate_q, up_q and down_q with 4-bit tensor copies, which need them 32-byte
+ * aligned (true of any pool whose tensors start at multiples of 32 bytes, e.g. 256-byte
+ * padded); run a pool with 16- but not 32-byte aligned packed tensors on the weight-decode
+ * form (k3moe_set_tc_split_max_tokens(0)).  The host cannot see the pointers, so the
+ * tensor-core path checks them on the device, reports K3MOE_DEV_ALIGN and abandons the
+ * call when one falls short. */
 typedef struct {
   const uint8_t* const* gate_q;
   const uint8_t* const* gate_s;

@@ -304,8 +304,8 @@ def test_forward_tensor_core_path_ragged_tokens(k3, prefill):
 
 
 def test_misaligned_expert_tensor_sets_the_align_status(k3, prefill):
-    """From 256 tokens the grouped GEMM writes expert tensor addresses into its weight
-    tensor maps on the device.  Gate tensors 8 bytes off the 16-byte alignment the ABI
+    """On the tensor-core path the grouped GEMM writes expert tensor addresses into its
+    weight tensor maps on the device.  Gate tensors 8 bytes off the 16-byte alignment the ABI
     requires are refused by the kernel's own check before any copy: the status word gets
     K3MOE_DEV_ALIGN and the call is abandoned (its outputs are invalid)."""
     cfg = C.PREFILL.with_tokens(256, x_seed=11)

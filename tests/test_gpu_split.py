@@ -123,3 +123,33 @@ def test_both_forms_on_other_widths(k3, split):
             hi, lo, s_hi, s_lo = split_terms(k3, L, ws, 8, 9, slots, I)
             _check_terms(h, hi, lo, s_hi, s_lo, "h")
     print(f"mid widths, split {split}: rel-L2 {r:.2e}, worst token {worst:.2e}")
+
+
+def test_pool_aligned_to_16_bytes_only(k3):
+    """A pool whose tensors start 16 bytes past 32-byte boundaries (the same bytes, copied
+    16 bytes further on): the split form's 4-bit tensor copies need 32-byte aligned packed
+    tensors, so it reports K3MOE_DEV_ALIGN and abandons the call (no copy issued); the
+    weight-decode form, which needs 16, runs it and gives bit for bit what it gives on the
+    aligned pool."""
+    from tests.test_gpu_parity import tc_form
+    L = Layer(k3, MID)
+    n = L.pool.numel()
+    raw = torch.zeros(n + 64, dtype=torch.uint8, device="cuda")
+    start = (-raw.data_ptr()) % 32 + 16  # 16 bytes past a 32-byte boundary
+    shifted = raw[start:start + n]
+    shifted.copy_(L.pool)
+    assert shifted.data_ptr() % 32 == 16
+    S = Layer.__new__(Layer)
+    S.cfg, S.d, S.t = L.cfg, L.d, L.t
+    S.pool, S.eb, S.offs = shifted, L.eb, L.offs
+    S.tables = k3.ExpertTables.from_pool(shifted, L.eb, L.offs)
+    with tc_form(k3, 1):
+        _, _, _, ws = S.forward(k3)
+        assert k3.device_status(ws) & k3.DEV_ALIGN
+    with tc_form(k3, 0):
+        got_s, ids_s, _, ws = S.forward(k3)
+        assert k3.device_status(ws) == 0
+        got_a, ids_a, _, ws = L.forward(k3)
+        assert k3.device_status(ws) == 0
+    assert np.array_equal(ids_s, ids_a)
+    assert np.array_equal(got_s.view(np.uint32), got_a.view(np.uint32))
