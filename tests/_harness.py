@@ -37,3 +37,19 @@ def oracle_forward(cfg, token_rows=None, spec=True, chunk=0):
     ids, _, _, _ = oracle.route(d, x, W["wr"], W["bias"])
     ex = {int(e): C.expert_tensors(cfg, int(e)) for e in np.unique(ids) if e >= 0}
     return oracle.forward(d, x, W["wr"], W["bias"], W["wd"], W["wu"], W["gamma"], ex, spec, chunk)
+
+
+def smallest_scale_within_448(amax):
+    """Per group: the smallest scale byte s (0..254) with amax <= 448 * 2^(s - 127); 0 for a
+    group of zeros.  Searched directly from a frexp estimate."""
+    s = np.zeros(amax.shape, np.int64)
+    nz = amax > 0
+    _, ex = np.frexp(amax[nz])
+    c = ex.astype(np.int64) + 127 - 9  # 448 < 2^9
+    lim = lambda c: 448.0 * np.exp2(c.astype(np.float64) - 127)
+    for _ in range(4):
+        c = np.where(amax[nz] > lim(c), c + 1, c)
+    for _ in range(4):
+        c = np.where((c > 0) & (amax[nz] <= lim(c - 1)), c - 1, c)
+    s[nz] = np.clip(c, 0, 254)
+    return s

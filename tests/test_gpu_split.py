@@ -14,6 +14,7 @@ import numpy as np
 import pytest
 
 from datagen import configs as C
+from tests._harness import smallest_scale_within_448
 from tests.test_gpu_parity import Layer, _slot_map, _ws_view, split_terms
 
 pytestmark = pytest.mark.gpu
@@ -36,22 +37,6 @@ def prefill(k3):
     yield L
     del L
     torch.cuda.empty_cache()
-
-
-def smallest_scale_within_448(amax):
-    """Per group: the smallest scale byte s (0..254) with amax <= 448 * 2^(s - 127); 0 for a
-    group of zeros.  Searched directly from a frexp estimate."""
-    s = np.zeros(amax.shape, np.int64)
-    nz = amax > 0
-    _, ex = np.frexp(amax[nz])
-    c = ex.astype(np.int64) + 127 - 9  # 448 < 2^9
-    lim = lambda c: 448.0 * np.exp2(c.astype(np.float64) - 127)
-    for _ in range(4):
-        c = np.where(amax[nz] > lim(c), c + 1, c)
-    for _ in range(4):
-        c = np.where((c > 0) & (amax[nz] <= lim(c - 1)), c - 1, c)
-    s[nz] = np.clip(c, 0, 254)
-    return s
 
 
 def _check_terms(x, hi, lo, s_hi, s_lo, what):
