@@ -1,6 +1,8 @@
-// k3_mx8.cuh -- the low-precision-activation variant of the grouped expert GEMM:
-// block-scaled tcgen05.mma (kind::mxf8f6f4) on the MXFP4 weights as stored and MXFP8
-// activations, no weight decode.
+// k3_mx8.cuh -- the grouped expert GEMM on block-scaled tcgen05.mma (kind::mxf8f6f4):
+// the MXFP4 weights as stored against MXFP8 activation rows, no weight decode on the SMs.
+// Two uses: the exact path's split form (SPLIT = 1: each bf16 activation as two MXFP8 terms
+// hi + lo that hold it exactly, two MMAs per k-block into one accumulator; see the split
+// helpers below), and the low-precision-activation variant (SPLIT = 0: one MXFP8 term).
 //
 // The variant follows the per-32-group quantized-activation kernel of colibri PR #676
 // ("What's in the commits" item 7) and colibri PR #684 (quant.h commit: matmul_mxfp4_i8),
@@ -32,16 +34,18 @@
 // exact path's permutation):
 //   warp 0      loads: per stage one 16U4 TMA copy per block (tensor maps whose global
 //               address is rewritten on the device to the tile's expert tensors) and one
-//               TMA copy of the batch's activation rows, into an X8_STAGES ring;
-//   warps 1, 2  MMA issuers, block 0 and block 1 (4 MMAs of K 32 per stage each);
+//               TMA copy of the batch's activation rows per term, into an X8_STAGES ring;
+//   warps 1, 2  MMA issuers, block 0 and block 1 (4 MMAs of K 32 per stage and term);
 //   warps 3..6  scale writers: each holds one TMEM lane quarter; per stage it loads the
 //               weight scale words of its 32 rows (both blocks) and the activation scale
-//               words of the batch's tokens, several stages ahead, and stores them into
-//               the stage's scale columns (tcgen05.st);
-//   warps 7..14 epilogue, double-buffered accumulators: GATEUP applies SiTU-GLU, rounds
-//               h to bf16, quantizes it to MXFP8 (one scale per 32 features of a token =
-//               the 32 lanes of a warp) and stores codes and scales in slot order for the
-//               down GEMM; DOWN stores o (fp32) in slot order.
+//               words of the batch's tokens (k-block-major, coalesced), several stages
+//               ahead, and stores them into the stage's scale columns (tcgen05.st);
+//   warps 7..22 epilogue, double-buffered accumulators, four warps per TMEM lane quarter
+//               on alternate 8-token chunks: GATEUP applies SiTU-GLU and rounds h to bf16,
+//               then (variant) quantizes it to MXFP8 (one scale per 32 features of a token
+//               = the 32 lanes of a warp) and stores codes and scales, or (split form)
+//               stores the bf16 h, in slot order for the down GEMM; DOWN stores o (fp32)
+//               in slot order.
 // Every mbarrier wait is bounded; on expiry K3MOE_DEV_TIMEOUT is set and all roles drain.
 #pragma once
 
@@ -181,11 +185,6 @@ K3_DEVI uint32_t split_hi_scale(float amax) {
   return s;
 }
 K3_DEVI uint32_t split_lo_scale(uint32_t s_hi) { return s_hi >= 4u ? s_hi - 4u : 0u; }
-// E4M3 code -> its value (exact in f32)
-K3_DEVI float e4m3_value(uint32_t code) {
-  const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
-  return __half2float(__half(h));
-}
 // 2^(s - 127) for a scale byte s (2^-127 is an f32 subnormal)
 K3_DEVI float e8m0_value(uint32_t s) { return s ? __uint_as_float(s << 23) : __uint_as_float(0x00400000u); }
 // two elements: the codes of hi and lo at the group's scales (inv_hi = 2^(127 - s_hi),
