@@ -92,7 +92,12 @@ DECODE = LayerConfig("decode", T=1, hidden=7168, latent=3584, n_experts=896, top
 CHUNK = dataclasses.replace(DECODE, name="chunk", T=32, x_kind="perturbed", n_bases=4, perturb_sigma=0.3)
 PREFILL = LayerConfig("prefill", T=4096, hidden=7168, latent=3584, n_experts=896, top_k=16, inter=3072,
                       seed=0, bias_range=0.0, scale_lo=117, scale_hi=127)
-LAYER_CONFIGS = {c.name: c for c in (TINY, DECODE, CHUNK, PREFILL)}
+# a small layer of other widths that runs the tensor-core path: latent 768 (a gate/up
+# contraction of six 128-element stages), inter 512 (a down contraction of four), hidden
+# 1024, 32 experts, top-4, 40 tokens
+MID = dataclasses.replace(TINY, name="mid", T=40, hidden=1024, latent=768, n_experts=32, top_k=4, inter=512,
+                          seed=3, bias_range=0.05)
+LAYER_CONFIGS = {c.name: c for c in (TINY, DECODE, CHUNK, PREFILL, MID)}
 
 
 @dataclasses.dataclass(frozen=True)

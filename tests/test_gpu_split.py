@@ -8,8 +8,6 @@ largest and within 2^-21 of the group's largest for the others (the error bound 
 the library's header), for z (the gather's terms) and h (the terms the pass between the two
 GEMMs makes from the gate/up GEMM's bf16 h).  The products with the terms are those of the
 exact path, which the parity tests check through the outputs."""
-import dataclasses
-
 import numpy as np
 import pytest
 
@@ -77,8 +75,7 @@ def test_split_terms_hold_z_and_h(k3, prefill, T):
 # a layer with other widths: latent 768 (gate/up contraction of 6 stages of 128, a count
 # that is not a multiple of 4), inter 512 (the down contraction at the 4-stage minimum),
 # hidden 1024, 32 experts, top-4
-MID = dataclasses.replace(C.TINY, name="mid", T=40, hidden=1024, latent=768, n_experts=32, top_k=4, inter=512,
-                          seed=3, bias_range=0.05)
+MID = C.MID
 
 
 @pytest.mark.parametrize("split", [1, 0])
