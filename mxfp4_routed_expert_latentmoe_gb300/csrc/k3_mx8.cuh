@@ -223,8 +223,10 @@ K3_DEVI void split_group(const uint32_t (&w)[16], uint32_t (&ch)[8], uint32_t (&
 // bf16 rows -> the two split terms of every routed slot: codes [2][slots][L] (hi rows,
 // then lo rows), scale bytes of the 2 slots rows k-block-major (act_scale_idx).  The row of
 // slot s is row slot_tok[s] of x (z: the gather into slot order), or row s itself when
-// slot_tok is null (h, already in slot order).  One thread per 32-element group; the first
-// n_placed slots are the routed ones.
+// slot_tok is null (h, already in slot order).  One thread per 32-element group (L / 32 a
+// multiple of 4, so the four groups of one scale word sit on four consecutive lanes of a
+// warp, and the first of them stores the word); the first n_placed slots are the routed
+// ones.
 __global__ void __launch_bounds__(256) k3_split_rows_kernel(const uint16_t* __restrict__ x,
                                                             const int32_t* __restrict__ slot_tok,
                                                             const int32_t* __restrict__ n_placed, int slots, int L,
@@ -233,27 +235,48 @@ __global__ void __launch_bounds__(256) k3_split_rows_kernel(const uint16_t* __re
   grid_dep_launch();
   const int G = L / 32;
   const int np = min(*n_placed, slots);
-  const size_t total = (size_t)np * G;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const int slot = (int)(i / G), g = (int)(i % G);
-    const int row = slot_tok ? __ldg(slot_tok + slot) : slot;
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * L + g * 32);
-    uint32_t w[16];
+  const size_t total = (size_t)np * G;  // a multiple of 4
+  const int lane = threadIdx.x & 31;
+  uint32_t* sw = reinterpret_cast<uint32_t*>(scales);
+  // whole warps run every iteration (the word's bytes are gathered by shuffles); a quad of
+  // lanes is entirely inside or entirely past the end
+  for (size_t i0 = (size_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31u); i0 < total;
+       i0 += (size_t)gridDim.x * blockDim.x) {
+    const size_t i = i0 + lane;
+    const bool in = i < total;
+    const int slot = in ? (int)(i / G) : 0, g = in ? (int)(i % G) : 0;
+    uint32_t s_hi = 0u, s_lo = 0u;
+    if (in) {
+      const int row = slot_tok ? __ldg(slot_tok + slot) : slot;
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * L + g * 32);
+      uint32_t w[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 v = __ldg(src + j);
+        w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
+      }
+      uint32_t ch[8], cl[8];
+      split_group(w, ch, cl, s_hi, s_lo);
+      uint4* dh = reinterpret_cast<uint4*>(codes + (size_t)slot * L + g * 32);
+      uint4* dl = reinterpret_cast<uint4*>(codes + ((size_t)slots + slot) * L + g * 32);
+      dh[0] = make_uint4(ch[0], ch[1], ch[2], ch[3]);
+      dh[1] = make_uint4(ch[4], ch[5], ch[6], ch[7]);
+      dl[0] = make_uint4(cl[0], cl[1], cl[2], cl[3]);
+      dl[1] = make_uint4(cl[4], cl[5], cl[6], cl[7]);
+    }
+    // the quad's four scale bytes (groups 4w .. 4w + 3 of one slot) into one word per term
+    const int q0 = lane & ~3;
+    uint32_t wh = 0u, wl = 0u;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint4 v = __ldg(src + j);
-      w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
+      wh |= __shfl_sync(0xffffffffu, s_hi, q0 + j) << (8 * j);
+      wl |= __shfl_sync(0xffffffffu, s_lo, q0 + j) << (8 * j);
     }
-    uint32_t ch[8], cl[8], s_hi, s_lo;
-    split_group(w, ch, cl, s_hi, s_lo);
-    uint4* dh = reinterpret_cast<uint4*>(codes + (size_t)slot * L + g * 32);
-    uint4* dl = reinterpret_cast<uint4*>(codes + ((size_t)slots + slot) * L + g * 32);
-    dh[0] = make_uint4(ch[0], ch[1], ch[2], ch[3]);
-    dh[1] = make_uint4(ch[4], ch[5], ch[6], ch[7]);
-    dl[0] = make_uint4(cl[0], cl[1], cl[2], cl[3]);
-    dl[1] = make_uint4(cl[4], cl[5], cl[6], cl[7]);
-    scales[act_scale_idx(slot, g, 2 * (size_t)slots)] = (uint8_t)s_hi;
-    scales[act_scale_idx((size_t)slots + slot, g, 2 * (size_t)slots)] = (uint8_t)s_lo;
+    if (in && (lane & 3) == 0) {
+      const size_t rows = 2 * (size_t)slots, wq = (size_t)(g >> 2);
+      sw[wq * rows + slot] = wh;
+      sw[wq * rows + slots + slot] = wl;
+    }
   }
 }
 
