@@ -34,7 +34,7 @@
 // exact path's permutation):
 //   warp 0      loads: per stage one 16U4 TMA copy per block (tensor maps whose global
 //               address is rewritten on the device to the tile's expert tensors) and one
-//               TMA copy of the batch's activation rows per term, into an X8_STAGES ring;
+//               TMA copy of the batch's activation rows per term, into a STAGES-deep ring;
 //   warps 1, 2  MMA issuers, block 0 and block 1 (4 MMAs of K 32 per stage and term);
 //   warps 3..6  scale writers: each holds one TMEM lane quarter; per stage it loads the
 //               weight scale words of its 32 rows (both blocks) and the activation scale
@@ -57,40 +57,45 @@ namespace k3 {
 
 constexpr int X8_ROWS = TM_ROWS;       // weight rows per MMA block (M)
 constexpr int X8_BLOCKS = 2;           // row blocks per tile (two issuers, two accumulators)
-constexpr int X8_NB = TM_NB;           // tokens per batch
+constexpr int X8_NB = TM_NB;           // tokens per batch (the large-batch layout)
 constexpr int X8_BK = 128;             // contraction elements per stage
-constexpr int X8_STAGES = 4;
+constexpr int X8_STAGES = 4;           // stages of the large-batch layout
+// small batches (at most 32 tokens): B tiles a third as large leave room for a fifth stage
+// of weight bytes in flight (needs contraction lengths of at least 5 stages)
+constexpr int X8_NB_SMALL = 32, X8_STAGES_SMALL = 5;
 constexpr int X8_A_BYTES = X8_ROWS * 128;  // shared-memory bytes of one block's stage
 constexpr int X8_A_TX = X8_ROWS * 64;      // bytes the copy reads (packed E2M1)
-constexpr int X8_B_BYTES = X8_NB * 128;     // one activation term's stage (N rows x 128 bytes)
 constexpr int X8_EPI = 16;
 constexpr int X8_SCALE_W0 = 3;
 constexpr int X8_EPI_W0 = X8_SCALE_W0 + 4;
 constexpr int X8_THREADS = (X8_EPI_W0 + X8_EPI) * 32;
 constexpr int X8_PREF = 4;  // stages of scale words in flight per scale writer
-// TMEM columns: accumulators [buffer][block][X8_NB], then per stage SFA block 0 (4),
-// SFA block 1 (4), SFB of each activation term (4 each: up to 128 tokens)
-constexpr int X8_ACC_COLS = X8_BLOCKS * X8_NB;
-constexpr int X8_SF0 = 2 * X8_ACC_COLS;
-static_assert(X8_NB <= 128, "the B scale columns hold 128 tokens");
 // SPLIT = 0: one MXFP8 activation term (the lossy variant); SPLIT = 1: two terms hi + lo
-// that hold the bf16 activations exactly (see k3_split_rows_kernel)
-template <int SPLIT>
+// that hold the bf16 activations exactly (see k3_split_rows_kernel).  NB: tokens per batch
+// (MMA N at most), STAGES: the ring's depth.
+// TMEM columns: accumulators [buffer][block][NB], then per stage SFA block 0 (4), SFA
+// block 1 (4), SFB of each activation term (4 each: up to 128 tokens)
+template <int SPLIT, int NB, int STAGES>
 struct X8Lay {
   static constexpr int TERMS = 1 + SPLIT;
-  static constexpr int STAGE_BYTES = X8_BLOCKS * X8_A_BYTES + TERMS * X8_B_BYTES;
+  static constexpr int B_BYTES = NB * 128;  // one activation term's stage (NB rows x 128 bytes)
+  static constexpr int STAGE_BYTES = X8_BLOCKS * X8_A_BYTES + TERMS * B_BYTES;
+  static constexpr int ACC_COLS = X8_BLOCKS * NB;
+  static constexpr int SF0 = 2 * ACC_COLS;
   static constexpr int SF_COLS = 4 * (X8_BLOCKS + TERMS);
-  static constexpr int SMEM = 1024 + X8_STAGES * STAGE_BYTES + 512 + X8_BLOCKS * 2 * 128;
-  static_assert(X8_SF0 + X8_STAGES * SF_COLS <= 512, "TMEM columns");
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 512 + X8_BLOCKS * 2 * 128;
+  static_assert(NB % 16 == 0 && NB <= 128, "the B scale columns hold 128 tokens");
+  static_assert(SF0 + STAGES * SF_COLS <= 512, "TMEM columns");
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
-  static_assert(STAGE_BYTES % 1024 == 0 && X8_B_BYTES % 1024 == 0, "128-byte swizzle atoms stay 1024-byte aligned");
+  static_assert(8 * (2 * STAGES + 5) <= 512, "barrier space");
+  static_assert(STAGE_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "128-byte swizzle atoms stay 1024-byte aligned");
 };
 
 struct Mx8Params {
-  const MxBatch* batches;   // token batches of up to X8_NB tokens (one expert each)
+  const MxBatch* batches;   // token batches of up to NB tokens (one expert each)
   const int32_t* n_batches;
   int R;                    // rows per weight matrix (I for gate/up, L for down)
-  int K;                    // contraction length (L or I), a multiple of 128, >= 128 * X8_STAGES
+  int K;                    // contraction length (L or I), a multiple of 128, >= 128 * STAGES
   // activation terms (one, or hi then lo when split): codes [terms][slots][K] E4M3 (the
   // operand's tensor map), rows in slot order; scale bytes k-block-major (act_scale_idx)
   const uint8_t* act_s;
@@ -320,11 +325,11 @@ __global__ void __launch_bounds__(256) k3_gather_mx8_kernel(const uint16_t* __re
 }
 
 // ---------------------------------------------------------------------------- grouped GEMM
-template <int MODE, int SPLIT>
+template <int MODE, int SPLIT, int NB, int STAGES>
 __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_constant__ CUtensorMap mapB,
                                                                    const __grid_constant__ CUtensorMap mapA,
                                                                    Mx8Params p) {
-  using Lay = X8Lay<SPLIT>;
+  using Lay = X8Lay<SPLIT, NB, STAGES>;
   constexpr int TERMS = Lay::TERMS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint32_t tmem_base_sh;
@@ -333,24 +338,24 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // stage s: A block 0, A block 1, B term(s)
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t bars = base + X8_STAGES * Lay::STAGE_BYTES;
+  const uint32_t bars = base + STAGES * Lay::STAGE_BYTES;
   const uint32_t smaps = bars + 512;  // [X8_BLOCKS][128 bytes] tensor-map images
   auto stage_a = [&](int s, int b) { return base + s * Lay::STAGE_BYTES + b * X8_A_BYTES; };
-  auto stage_b = [&](int s, int t) { return base + s * Lay::STAGE_BYTES + X8_BLOCKS * X8_A_BYTES + t * X8_B_BYTES; };
+  auto stage_b = [&](int s, int t) { return base + s * Lay::STAGE_BYTES + X8_BLOCKS * X8_A_BYTES + t * Lay::B_BYTES; };
   // full(s): the stage's copies landed (the load thread's arrival with the byte count) and
   // the four scale writers stored its scale words; kdone(s): both issuers' MMAs of the
   // stage completed (frees its shared memory and scale columns); tfull / tempty: the
   // accumulator buffer holds a finished tile / was read by all epilogue threads
   auto full = [&](int s) { return bars + 8 * s; };
-  auto kdone = [&](int s) { return bars + 8 * (X8_STAGES + s); };
-  auto tfull = [&](int b) { return bars + 8 * (2 * X8_STAGES + b); };
-  auto tempty = [&](int b) { return bars + 8 * (2 * X8_STAGES + 2 + b); };
-  const uint32_t done_bar = bars + 8 * (2 * X8_STAGES + 4);
+  auto kdone = [&](int s) { return bars + 8 * (STAGES + s); };
+  auto tfull = [&](int b) { return bars + 8 * (2 * STAGES + b); };
+  auto tempty = [&](int b) { return bars + 8 * (2 * STAGES + 2 + b); };
+  const uint32_t done_bar = bars + 8 * (2 * STAGES + 4);
   volatile int* abort_flag = &abort_sh;
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
-    for (int s = 0; s < X8_STAGES; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(full(s), 1 + 4);
       mbar_init(kdone(s), X8_BLOCKS);
     }
@@ -375,7 +380,7 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
 
   const int mtiles = p.R / (MODE == 0 ? X8_ROWS : X8_BLOCKS * X8_ROWS);
   const int tiles = mtiles * (*p.n_batches);
-  const int kst = p.K / X8_BK;  // stages per tile (>= X8_STAGES)
+  const int kst = p.K / X8_BK;  // stages per tile (>= STAGES)
   const int my_tiles = (tiles > (int)blockIdx.x) ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   const int nst = my_tiles * kst;
   // weight tensors of block b (index into MxBatch::w: packed, then scales) and the first row
@@ -384,7 +389,7 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
   auto blk_row0 = [](int tm, int b) {
     return (MODE == 0) ? tm * X8_ROWS : tm * (X8_BLOCKS * X8_ROWS) + b * X8_ROWS;
   };
-  auto sf_col = [&](int s) { return tmem + X8_SF0 + s * Lay::SF_COLS; };
+  auto sf_col = [&](int s) { return tmem + Lay::SF0 + s * Lay::SF_COLS; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ loads
@@ -398,15 +403,15 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
     int par = 1, slot0 = 0, tm = 0, issued = 0;
 #pragma unroll 1
     for (int j = 0; j < nst; ++j) {
-      const int s = j % X8_STAGES, ks = j % kst;
-      // the stage's previous contents (j - X8_STAGES) have been consumed by the MMAs
-      if (j >= X8_STAGES &&
-          !__all_sync(0xffffffffu, mbar_wait(kdone(s), ((j / X8_STAGES) - 1) & 1, abort_flag)))
+      const int s = j % STAGES, ks = j % kst;
+      // the stage's previous contents (j - STAGES) have been consumed by the MMAs
+      if (j >= STAGES &&
+          !__all_sync(0xffffffffu, mbar_wait(kdone(s), ((j / STAGES) - 1) & 1, abort_flag)))
         break;
       if (ks == 0) {
         // a new tile: point the block maps of this tile's parity at its expert tensors.  The
         // copies of the tile before last (same parity) have all landed: the wait above was
-        // for a stage of the previous tile or later (a tile has >= X8_STAGES stages).
+        // for a stage of the previous tile or later (a tile has >= STAGES stages).
         const int tile = blockIdx.x + (j / kst) * gridDim.x;
         const MxBatch* rec = p.batches + tile / mtiles;
         const uint8_t* q0 = rec->w[blk_tensor(0)];
@@ -436,7 +441,7 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
         tm = tile % mtiles;
       }
       if (lane == 0) {
-        mbar_expect_tx(full(s), X8_BLOCKS * X8_A_TX + TERMS * X8_B_BYTES);
+        mbar_expect_tx(full(s), X8_BLOCKS * X8_A_TX + TERMS * Lay::B_BYTES);
 #pragma unroll
         for (int b = 0; b < X8_BLOCKS; ++b)
           tma_load_2d(stage_a(s, b), reinterpret_cast<const CUtensorMap*>(gmap(b, par)), ks * X8_BK, blk_row0(tm, b),
@@ -451,9 +456,9 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
     // byte counts (their phases complete once the copies and the scale writers are done;
     // after an abort the writers may never arrive, so only a bounded time is spent)
     if (lane == 0) {
-      for (int j = (issued > X8_STAGES ? issued - X8_STAGES : 0); j < issued; ++j) {
+      for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j) {
         const long long t0 = clock64();
-        while (!mbar_test(full(j % X8_STAGES), (j / X8_STAGES) & 1) && clock64() - t0 < (1ll << 22)) {
+        while (!mbar_test(full(j % STAGES), (j / STAGES) & 1) && clock64() - t0 < (1ll << 22)) {
         }
       }
     }
@@ -470,10 +475,10 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
         const int buf = lt & 1;
         if (!mbar_wait_issue(tempty(buf), ((lt >> 1) & 1) ^ 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d = tmem + buf * X8_ACC_COLS + mm * X8_NB;
+        const uint32_t d = tmem + buf * Lay::ACC_COLS + mm * NB;
         for (int ks = 0; ks < kst; ++ks, ++j) {
-          const int s = j % X8_STAGES;
-          if (!mbar_wait_issue(full(s), (j / X8_STAGES) & 1, abort_flag)) {
+          const int s = j % STAGES;
+          if (!mbar_wait_issue(full(s), (j / STAGES) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -486,7 +491,7 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
             tc_mma_mx8(d, da + 2 * kk, db + 2 * kk, idesc_mx8(N, kk), sfa, sfb, (ks | kk) != 0);
             // the lo term: same weights, its own rows and scale columns, same accumulator
             if (SPLIT)
-              tc_mma_mx8(d, da + 2 * kk, db + (X8_B_BYTES >> 4) + 2 * kk, idesc_mx8(N, kk), sfa, sfb + 4, 1u);
+              tc_mma_mx8(d, da + 2 * kk, db + (Lay::B_BYTES >> 4) + 2 * kk, idesc_mx8(N, kk), sfa, sfb + 4, 1u);
           }
           tc_commit(kdone(s));
         }
@@ -540,9 +545,9 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
         const int j = j0 + u;
         if (j >= nst) break;
         load(j + X8_PREF - 1, ring[(u + X8_PREF - 1) % X8_PREF]);
-        const int s = j % X8_STAGES;
-        if (j >= X8_STAGES &&
-            !__all_sync(0xffffffffu, mbar_wait(kdone(s), ((j / X8_STAGES) - 1) & 1, abort_flag))) {
+        const int s = j % STAGES;
+        if (j >= STAGES &&
+            !__all_sync(0xffffffffu, mbar_wait(kdone(s), ((j / STAGES) - 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
@@ -574,12 +579,12 @@ __global__ void __launch_bounds__(X8_THREADS, 1) k3_mx8_moe_kernel(const __grid_
       const MxBatch* rec = p.batches + tile / mtiles;
       const int slot0 = rec->slot0, n = rec->n;
       const int tm = tile % mtiles;
-      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + buf * X8_ACC_COLS;
+      const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + buf * Lay::ACC_COLS;
 #pragma unroll 1
       for (int c = e0; c * 8 < n; c += X8_EPI / 4) {
         uint32_t r0[8], r1[8];
         tmem_ld8(tq + c * 8, r0);
-        tmem_ld8(tq + X8_NB + c * 8, r1);
+        tmem_ld8(tq + NB + c * 8, r1);
         tmem_ld_wait();
         if (MODE == 0) {
           // h of feature `feat` for 8 tokens; the 32 features of the warp are one MXFP8 group

@@ -331,18 +331,39 @@ cudaError_t launch_tc_moe(const uint16_t* act, int slots, TcMoeParams p, int dev
 }
 
 // grouped expert GEMM of the MXFP8-activation variant; act [slots, K] E4M3 codes in slot order
-template <int MODE, int SPLIT>
-cudaError_t launch_mx8_moe(const uint8_t* act, Mx8Params p, int dev, int sms, cudaStream_t st, bool pdl) {
+template <int MODE, int SPLIT, int NB, int STAGES>
+cudaError_t launch_mx8_t(const uint8_t* act, Mx8Params p, int dev, int sms, cudaStream_t st, bool pdl) {
+  if (p.K < X8_BK * STAGES) return cudaErrorInvalidValue;  // a tile has at least STAGES stages
   CUtensorMap mb, ma;
   // the activation terms' rows, one after the other
-  if (!map_u8(&mb, act, (uint64_t)(1 + SPLIT) * p.slots, (uint64_t)p.K, X8_NB)) return cudaErrorInvalidValue;
+  if (!map_u8(&mb, act, (uint64_t)(1 + SPLIT) * p.slots, (uint64_t)p.K, NB)) return cudaErrorInvalidValue;
   // template of the weight maps ([R, K] E2M1): the kernel writes each expert tensor's address
   // into its copies; the (256-byte aligned) workspace stands in until then
   if (!map_e2m1(&ma, p.tmaps, (uint64_t)p.R, (uint64_t)p.K)) return cudaErrorInvalidValue;
-  constexpr int smem = X8Lay<SPLIT>::SMEM;
-  if (!set_smem<k3_mx8_moe_kernel<MODE, SPLIT>>(dev, smem)) return cudaErrorInvalidValue;
+  constexpr int smem = X8Lay<SPLIT, NB, STAGES>::SMEM;
+  if (!set_smem<k3_mx8_moe_kernel<MODE, SPLIT, NB, STAGES>>(dev, smem)) return cudaErrorInvalidValue;
   const int grid = sms < TM_MAX_CTAS ? sms : TM_MAX_CTAS;
-  return launch(k3_mx8_moe_kernel<MODE, SPLIT>, dim3(grid), dim3(X8_THREADS), smem, st, pdl, mb, ma, p);
+  return launch(k3_mx8_moe_kernel<MODE, SPLIT, NB, STAGES>, dim3(grid), dim3(X8_THREADS), smem, st, pdl, mb, ma, p);
+}
+
+// the batches' token count (the permutation's NB) picks the layout: up to X8_NB_SMALL
+// tokens the small-batch layout with its deeper ring
+template <int MODE, int SPLIT>
+cudaError_t launch_mx8_moe(const uint8_t* act, Mx8Params p, int nb, int dev, int sms, cudaStream_t st, bool pdl) {
+  if (nb == X8_NB_SMALL)
+    return launch_mx8_t<MODE, SPLIT, X8_NB_SMALL, X8_STAGES_SMALL>(act, p, dev, sms, st, pdl);
+  if (nb == X8_NB) return launch_mx8_t<MODE, SPLIT, X8_NB, X8_STAGES>(act, p, dev, sms, st, pdl);
+  return cudaErrorInvalidValue;
+}
+
+// tokens per batch of the block-scaled expert GEMMs: small batches (deeper ring) when few
+// tokens reach each expert -- below kSmallBatchT tokens an expert rarely gets more than 32 of
+// them (one that does takes several batches) -- and both contractions are long enough for
+// the deeper ring
+constexpr int kSmallBatchT = 512;
+int mx8_batch(const k3moe_dims& d, int T) {
+  return (T <= kSmallBatchT && d.latent >= X8_BK * X8_STAGES_SMALL && d.inter >= X8_BK * X8_STAGES_SMALL)
+             ? X8_NB_SMALL : X8_NB;
 }
 
 // D[M, N0 (+N1)] = A[M, K] . [B0; B1]^T on tcgen05 (A, B bf16 row-major)
@@ -670,7 +691,9 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
   const bool tc = tc_experts(d, T);
   const bool split = split_experts(d, T);
   const int nblk = mx_nblk(T);
-  const int NB = tc ? TM_NB : 8 * nblk;  // tokens per expert batch
+  // tokens per expert batch: the block-scaled GEMMs' (split form, variant), the
+  // weight-decode GEMM's, or the weight-streaming kernels'
+  const int NB = (split || (tc && d.act_mxfp8)) ? mx8_batch(d, T) : (tc ? TM_NB : 8 * nblk);
   const PermParams pp = perm_params(d, T, d.top_k, at<int32_t>(ws, L.ids), 0, NB, ws, L, experts);
   // one token: the bulk gate/up GEMV reads z (bf16) and its max itself (converting it once
   // per warp), so no f16 copy of z is made; batches of several tokens convert per item and
@@ -757,7 +780,7 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
     uint8_t* h8 = at<uint8_t>(ws, L.hterm);
     Mx8Params gp{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.inter, d.latent,
                  a8 + (size_t)2 * slots * d.latent, slots, hb, nullptr, status, at<void>(ws, L.tmaps)};
-    K3_TRY((launch_mx8_moe<0, 1>(a8, gp, dev, sms, s, pdl)));
+    K3_TRY((launch_mx8_moe<0, 1>(a8, gp, NB, dev, sms, s, pdl)));
     // h (bf16, slot order) -> its two terms for the down GEMM
     const size_t hgroups = (size_t)slots * (d.inter / 32);
     const int hblocks = (int)((hgroups + 255) / 256 < (size_t)sms * 8 ? (hgroups + 255) / 256 : (size_t)sms * 8);
@@ -767,7 +790,7 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
     K3_TRY(mark(events, n_events, 3, s));
     Mx8Params dp2{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.latent, d.inter,
                   h8 + (size_t)2 * slots * d.inter, slots, at<void>(ws, L.o), nullptr, status, at<void>(ws, L.tmaps)};
-    K3_TRY((launch_mx8_moe<1, 1>(h8, dp2, dev, sms, s, pdl)));
+    K3_TRY((launch_mx8_moe<1, 1>(h8, dp2, NB, dev, sms, s, pdl)));
   } else if (tc && d.act_mxfp8) {
     // MXFP8 activations, block-scaled MMAs on the stored MXFP4 weights; h leaves the gate/up
     // epilogue as MXFP8 rows in slot order (codes, then the scale bytes)
@@ -775,11 +798,11 @@ k3moe_status k3moe_forward_profiled(const k3moe_dims* dims, int32_t T, const uin
     uint8_t* h8 = at<uint8_t>(ws, L.h16);
     Mx8Params gp{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.inter, d.latent,
                  a8 + (size_t)slots * d.latent, slots, h8, h8 + (size_t)slots * d.inter, status, at<void>(ws, L.tmaps)};
-    K3_TRY((launch_mx8_moe<0, 0>(a8, gp, dev, sms, s, pdl)));
+    K3_TRY((launch_mx8_moe<0, 0>(a8, gp, NB, dev, sms, s, pdl)));
     K3_TRY(mark(events, n_events, 3, s));
     Mx8Params dp2{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.latent, d.inter,
                   h8 + (size_t)slots * d.inter, slots, at<void>(ws, L.o), nullptr, status, at<void>(ws, L.tmaps)};
-    K3_TRY((launch_mx8_moe<1, 0>(h8, dp2, dev, sms, s, pdl)));
+    K3_TRY((launch_mx8_moe<1, 0>(h8, dp2, NB, dev, sms, s, pdl)));
   } else if (tc) {
     TcMoeParams gp{at<MxBatch>(ws, L.batches), at<int32_t>(ws, L.n_batches), d.inter, d.latent,
                    at<void>(ws, L.h16), status, at<void>(ws, L.tmaps)};
