@@ -60,9 +60,10 @@ constexpr int X8_BLOCKS = 2;           // row blocks per tile (two issuers, two 
 constexpr int X8_NB = TM_NB;           // tokens per batch (the large-batch layout)
 constexpr int X8_BK = 128;             // contraction elements per stage
 constexpr int X8_STAGES = 4;           // stages of the large-batch layout
-// small batches (at most 32 tokens): B tiles a third as large leave room for a fifth stage
-// of weight bytes in flight (needs contraction lengths of at least 5 stages)
+// small batches (at most 32, or 16, tokens): smaller B tiles leave room for a fifth (sixth)
+// stage of weight bytes in flight (needs contraction lengths of at least that many stages)
 constexpr int X8_NB_SMALL = 32, X8_STAGES_SMALL = 5;
+constexpr int X8_NB_TINY = 16, X8_STAGES_TINY = 6;
 constexpr int X8_A_BYTES = X8_ROWS * 128;  // shared-memory bytes of one block's stage
 constexpr int X8_A_TX = X8_ROWS * 64;      // bytes the copy reads (packed E2M1)
 constexpr int X8_EPI = 16;

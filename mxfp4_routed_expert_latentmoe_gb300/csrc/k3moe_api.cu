@@ -350,6 +350,7 @@ cudaError_t launch_mx8_t(const uint8_t* act, Mx8Params p, int dev, int sms, cuda
 // tokens the small-batch layout with its deeper ring
 template <int MODE, int SPLIT>
 cudaError_t launch_mx8_moe(const uint8_t* act, Mx8Params p, int nb, int dev, int sms, cudaStream_t st, bool pdl) {
+  if (nb == X8_NB_TINY) return launch_mx8_t<MODE, SPLIT, X8_NB_TINY, X8_STAGES_TINY>(act, p, dev, sms, st, pdl);
   if (nb == X8_NB_SMALL)
     return launch_mx8_t<MODE, SPLIT, X8_NB_SMALL, X8_STAGES_SMALL>(act, p, dev, sms, st, pdl);
   if (nb == X8_NB) return launch_mx8_t<MODE, SPLIT, X8_NB, X8_STAGES>(act, p, dev, sms, st, pdl);
@@ -360,10 +361,12 @@ cudaError_t launch_mx8_moe(const uint8_t* act, Mx8Params p, int nb, int dev, int
 // tokens reach each expert -- below kSmallBatchT tokens an expert rarely gets more than 32 of
 // them (one that does takes several batches) -- and both contractions are long enough for
 // the deeper ring
-constexpr int kSmallBatchT = 512;
+constexpr int kSmallBatchT = 512, kTinyBatchT = 64;
 int mx8_batch(const k3moe_dims& d, int T) {
-  return (T <= kSmallBatchT && d.latent >= X8_BK * X8_STAGES_SMALL && d.inter >= X8_BK * X8_STAGES_SMALL)
-             ? X8_NB_SMALL : X8_NB;
+  const int kmin = d.latent < d.inter ? d.latent : d.inter;
+  if (T <= kTinyBatchT && kmin >= X8_BK * X8_STAGES_TINY) return X8_NB_TINY;
+  if (T <= kSmallBatchT && kmin >= X8_BK * X8_STAGES_SMALL) return X8_NB_SMALL;
+  return X8_NB;
 }
 
 // D[M, N0 (+N1)] = A[M, K] . [B0; B1]^T on tcgen05 (A, B bf16 row-major)
