@@ -287,7 +287,9 @@ __global__ void __launch_bounds__(256) k3_split_rows_kernel(const uint16_t* __re
 }
 
 // z rows (bf16, token order) -> MXFP8 rows in slot order: codes [slots, L], scale bytes
-// k-block-major (act_scale_idx).  One thread per 32-element group.
+// k-block-major (act_scale_idx).  One thread per 32-element group; the four groups of a
+// scale word sit on four consecutive lanes (L / 32 a multiple of 4) and the first of them
+// stores the word.
 __global__ void __launch_bounds__(256) k3_gather_mx8_kernel(const uint16_t* __restrict__ z,
                                                             const int32_t* __restrict__ slot_tok,
                                                             const int32_t* __restrict__ n_placed, int slots, int L,
@@ -296,32 +298,47 @@ __global__ void __launch_bounds__(256) k3_gather_mx8_kernel(const uint16_t* __re
   grid_dep_launch();
   const int G = L / 32;
   const int np = min(*n_placed, slots);
-  const size_t total = (size_t)np * G;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const int slot = (int)(i / G), g = (int)(i % G);
-    const int t = __ldg(slot_tok + slot);
-    const uint4* src = reinterpret_cast<const uint4*>(z + (size_t)t * L + g * 32);
-    uint4 v[4];
+  const size_t total = (size_t)np * G;  // a multiple of 4
+  const int lane = threadIdx.x & 31;
+  uint32_t* sw = reinterpret_cast<uint32_t*>(scales);
+  // whole warps run every iteration (the word's bytes are gathered by shuffles); a quad of
+  // lanes is entirely inside or entirely past the end
+  for (size_t i0 = (size_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31u); i0 < total;
+       i0 += (size_t)gridDim.x * blockDim.x) {
+    const size_t i = i0 + lane;
+    const bool in = i < total;
+    const int slot = in ? (int)(i / G) : 0, g = in ? (int)(i % G) : 0;
+    uint32_t s = 0u;
+    if (in) {
+      const int t = __ldg(slot_tok + slot);
+      const uint4* src = reinterpret_cast<const uint4*>(z + (size_t)t * L + g * 32);
+      uint4 v[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = __ldg(src + j);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(v);
-    float x[32];
-    float amax = 0.f;
+      for (int j = 0; j < 4; ++j) v[j] = __ldg(src + j);
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(v);
+      float x[32];
+      float amax = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      x[2 * j] = __uint_as_float(w[j] << 16);
-      x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-      amax = fmaxf(amax, fmaxf(fabsf(x[2 * j]), fabsf(x[2 * j + 1])));
+      for (int j = 0; j < 16; ++j) {
+        x[2 * j] = __uint_as_float(w[j] << 16);
+        x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        amax = fmaxf(amax, fmaxf(fabsf(x[2 * j]), fabsf(x[2 * j + 1])));
+      }
+      s = mx8_scale_byte(amax);
+      const float inv = mx8_inv_scale(s);
+      uint32_t c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        c[j] = e4m3x4_codes(x[4 * j] * inv, x[4 * j + 1] * inv, x[4 * j + 2] * inv, x[4 * j + 3] * inv);
+      uint4* dst = reinterpret_cast<uint4*>(codes + (size_t)slot * L + g * 32);
+      dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+      dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
     }
-    const uint32_t s = mx8_scale_byte(amax);
-    const float inv = mx8_inv_scale(s);
-    uint32_t c[8];
+    const int q0 = lane & ~3;
+    uint32_t word = 0u;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) c[j] = e4m3x4_codes(x[4 * j] * inv, x[4 * j + 1] * inv, x[4 * j + 2] * inv, x[4 * j + 3] * inv);
-    uint4* dst = reinterpret_cast<uint4*>(codes + (size_t)slot * L + g * 32);
-    dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
-    dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
-    scales[act_scale_idx(slot, g, slots)] = (uint8_t)s;
+    for (int j = 0; j < 4; ++j) word |= __shfl_sync(0xffffffffu, s, q0 + j) << (8 * j);
+    if (in && (lane & 3) == 0) sw[(size_t)(g >> 2) * slots + slot] = word;
   }
 }
 
