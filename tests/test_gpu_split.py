@@ -8,6 +8,8 @@ largest and within 2^-21 of the group's largest for the others (the error bound 
 the library's header), for z (the gather's terms) and h (the terms the pass between the two
 GEMMs makes from the gate/up GEMM's bf16 h).  The products with the terms are those of the
 exact path, which the parity tests check through the outputs."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -135,3 +137,29 @@ def test_pool_aligned_to_16_bytes_only(k3):
         assert k3.device_status(ws) == 0
     assert np.array_equal(ids_s, ids_a)
     assert np.array_equal(got_s.view(np.uint32), got_a.view(np.uint32))
+
+
+# contractions of 6 stages (latent and inter 768) so that the small-batch layouts apply;
+# 32 experts, top-4: at 200 and 300 tokens experts get ~25 and ~38 tokens, more than the
+# 16- and 32-token batches of the layouts those counts use (several batches per expert)
+MID768 = dataclasses.replace(C.MID, name="mid768", inter=768, seed=5)
+
+
+@pytest.mark.parametrize("T", [200, 300])
+def test_small_batch_layouts_split_experts_over_batches(k3, T):
+    """The block-scaled GEMMs' small-batch layouts (16 tokens a batch up to 256 tokens, 32
+    up to 512) on experts that receive more tokens than a batch holds: every token of the
+    split form against the oracle."""
+    from tests.test_gpu_parity import PER_TOKEN_BAR, _check_block
+    from tests._harness import oracle_forward, rel_l2
+    cfg = MID768.with_tokens(T, x_seed=50 + T)
+    L = Layer(k3, cfg)
+    got, ids, w, ws = L.forward(k3)
+    assert k3.device_status(ws) == 0
+    counts = np.bincount(ids.ravel(), minlength=cfg.n_experts)
+    assert counts.max() > (16 if T <= 256 else 32)  # some expert spans several batches
+    ref = oracle_forward(cfg)
+    r = _check_block(got, ids, w, ref)
+    worst = max(rel_l2(got[t], ref["out"][t]) for t in range(T))
+    assert worst <= PER_TOKEN_BAR, worst
+    print(f"T={T}: max tokens per expert {counts.max()}, rel-L2 {r:.2e}, worst token {worst:.2e}")
